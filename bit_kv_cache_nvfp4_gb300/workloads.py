@@ -1,0 +1,396 @@
+"""Seeded synthetic inputs shaped like the pages' sparse-MLA decode workloads.
+
+This module holds none of the method's arithmetic (no quantization, no
+attention); it only draws inputs.  Both the GPU path and the CPU oracle take
+their inputs from here, so the two sides see identical bf16 values, index
+sets and page tables.
+
+Randomness is counter based, so any element can be regenerated on any device
+without drawing the ones before it: a 32-bit hash of (stream, row, column)
+from the MurmurHash3 ``fmix32`` finalizer (Austin Appleby, MurmurHash3,
+public domain), evaluated with exact int64 tensor arithmetic (no overflow),
+so CPU and CUDA produce the same integers.  Continuous values come from a
+65,536-entry inverse-CDF table rounded once to bf16 (N(0,1) or Laplace(0,1)),
+indexed by the top 16 hash bits: the table is built on the host in float64
+and shared by both sides, so the bf16 values are identical by construction.
+
+Workload shapes (GLM-5.3 DSA decode with a 352-byte NVFP4 row, page size 64;
+numinousmuses "inference-optimizations" README, "Headline results" and
+"4-bit KV cache"):
+  tiny        B=1,  Sq=1, H=16,  L=4096,              K=256 uniform unique
+  decode      B=16, Sq=1, H=64,  L~U{8192..32768},    K=2048 uniform unique
+  long        B=64, Sq=1, H=64,  L=204800,            K=2048: 1024 from the
+              most recent 4096 positions + 1024 from the rest
+  specverify  B=32, Sq=4, H=128, L~U{16384..131072},  K=2048 per draft token:
+              1024 shared by the request's 4 tokens, 1020 per token, and the
+              4 draft positions (causally masked beyond the token's own)
+  splitk      B=2,  Sq=1, H=16,  L=1048576,           K=8192 uniform unique
+Latent values are N(0,1) with a seeded 5 of 512 channels scaled by 8; rope
+and q are N(0,1); physical pages are a seeded permutation.
+"""
+from __future__ import annotations
+
+import math
+import statistics
+from dataclasses import dataclass, field
+
+import torch
+
+M32 = 0xFFFFFFFF
+PAGE = 64
+LATENT = 512
+ROPE = 64
+QK = 576
+
+# stream identifiers (any distinct integers)
+S_LATENT, S_ROPE, S_Q, S_TOPK, S_PAGES, S_LENS, S_CHANNELS, S_ZERO, S_TIES = range(1, 10)
+
+
+# ---------------------------------------------------------------------------
+# counter-based hashing on int64 tensors holding values in [0, 2^32)
+# ---------------------------------------------------------------------------
+def _mul32(x: torch.Tensor, c: int) -> torch.Tensor:
+    """(x * c) mod 2^32 for x in [0, 2^32), computed without int64 overflow."""
+    lo = x & 0xFFFF
+    hi = x >> 16
+    return (lo * c + (((hi * c) & 0xFFFF) << 16)) & M32
+
+
+def fmix32(x: torch.Tensor) -> torch.Tensor:
+    """MurmurHash3 32-bit finalizer; a bijection on [0, 2^32)."""
+    x = x ^ (x >> 16)
+    x = _mul32(x, 0x85EBCA6B)
+    x = x ^ (x >> 13)
+    x = _mul32(x, 0xC2B2AE35)
+    x = x ^ (x >> 16)
+    return x
+
+
+def _fmix32_int(v: int) -> int:
+    return int(fmix32(torch.tensor([v & M32], dtype=torch.int64))[0])
+
+
+def stream_key(seed: int, stream: int) -> int:
+    return _fmix32_int(_fmix32_int(seed) ^ _fmix32_int(0x9E3779B9 + stream))
+
+
+def hash_grid(key: int, rows: torch.Tensor, cols: torch.Tensor) -> torch.Tensor:
+    """32-bit hashes for every (row, col) pair: int64 [len(rows), len(cols)]."""
+    rh = fmix32((rows.to(torch.int64) + key) & M32)
+    ch = fmix32((cols.to(torch.int64) * 0x27D4EB2F + 0x165667B1) & M32)
+    return fmix32(rh[:, None] ^ ch[None, :])
+
+
+def hash_vec(key: int, idx: torch.Tensor) -> torch.Tensor:
+    return fmix32(fmix32((idx.to(torch.int64) + key) & M32) ^ 0x5BD1E995)
+
+
+# ---------------------------------------------------------------------------
+# bf16 quantile tables
+# ---------------------------------------------------------------------------
+_TABLES: dict = {}
+
+
+def quantile_table(kind: str, device) -> torch.Tensor:
+    """bf16[65536]: the distribution's quantile at (i + 0.5) / 65536."""
+    dev = torch.device(device)
+    key = (kind, str(dev))
+    if key in _TABLES:
+        return _TABLES[key]
+    host_key = (kind, "cpu")
+    if host_key not in _TABLES:
+        n = 1 << 16
+        probs = [(i + 0.5) / n for i in range(n)]
+        if kind == "normal":
+            nd = statistics.NormalDist()
+            vals = [nd.inv_cdf(p) for p in probs]
+        elif kind == "laplace":
+            vals = [math.log(2 * p) if p < 0.5 else -math.log(2 * (1 - p)) for p in probs]
+        else:
+            raise ValueError(kind)
+        _TABLES[host_key] = torch.tensor(vals, dtype=torch.float64).to(torch.float32).to(
+            torch.bfloat16)
+    t = _TABLES[host_key].to(dev)
+    _TABLES[key] = t
+    return t
+
+
+def draw(kind: str, key: int, rows: torch.Tensor, ncols: int, device) -> torch.Tensor:
+    """bf16 [len(rows), ncols] drawn from the table of ``kind``."""
+    dev = torch.device(device)
+    rows = rows.to(dev)
+    cols = torch.arange(ncols, dtype=torch.int64, device=dev)
+    h = hash_grid(key, rows, cols)
+    return quantile_table(kind, dev)[(h >> 16)]
+
+
+# ---------------------------------------------------------------------------
+# workload configuration
+# ---------------------------------------------------------------------------
+@dataclass
+class Workload:
+    name: str
+    B: int
+    Sq: int
+    H: int
+    K: int
+    seq_lens: torch.Tensor            # int32 [B] (includes the Sq draft tokens)
+    topk: torch.Tensor                # int32 [B, Sq, K]; -1 = padding
+    page_table: torch.Tensor          # int32 [B, pt_stride]; -1 = unused
+    num_slots: int
+    seed: int
+    sm_scale: float = 1.0 / math.sqrt(QK)
+    outlier_channels: torch.Tensor = field(default=None)  # int64 [5]
+    token_offset: torch.Tensor = field(default=None)      # int64 [B] global token id base
+
+    @property
+    def pt_stride(self) -> int:
+        return int(self.page_table.shape[1])
+
+    @property
+    def total_tokens(self) -> int:
+        return int(self.seq_lens.to(torch.int64).sum())
+
+
+def _unique_sample(key: int, lo: int, hi: int, n: int, device="cpu") -> torch.Tensor:
+    """n distinct integers from [lo, hi), in a seeded random order (int64)."""
+    assert hi - lo >= n, (lo, hi, n)
+    pos = torch.arange(lo, hi, dtype=torch.int64, device=device)
+    k = hash_vec(key, pos) * (1 << 21) + (pos - lo)   # unique keys (hi-lo < 2^21)
+    assert hi - lo <= (1 << 21)
+    sel = torch.topk(k, n, largest=False, sorted=True).indices
+    return pos[sel]
+
+
+def _permutation(key: int, n: int) -> torch.Tensor:
+    assert n < (1 << 24)
+    idx = torch.arange(n, dtype=torch.int64)
+    return torch.argsort(hash_vec(key, idx) * (1 << 24) + idx)   # unique keys
+
+
+def _page_table(seed: int, seq_lens: torch.Tensor):
+    pages = [(int(L) + PAGE - 1) // PAGE for L in seq_lens.tolist()]
+    total = sum(pages)
+    perm = _permutation(stream_key(seed, S_PAGES), total).to(torch.int32)
+    pt = torch.full((len(pages), max(pages)), -1, dtype=torch.int32)
+    off = 0
+    for b, p in enumerate(pages):
+        pt[b, :p] = perm[off:off + p]
+        off += p
+    return pt, total * PAGE
+
+
+def _outlier_channels(seed: int) -> torch.Tensor:
+    return _permutation(stream_key(seed, S_CHANNELS), LATENT)[:5].sort().values
+
+
+def _uniform_lens(key: int, B: int, lo: int, hi: int) -> torch.Tensor:
+    h = hash_vec(key, torch.arange(B, dtype=torch.int64))
+    return (lo + (h % (hi - lo + 1))).to(torch.int32)
+
+
+CONFIG_NAMES = ("tiny", "decode", "long", "specverify", "splitk")
+
+
+def make_workload(name: str, seed: int = 0) -> Workload:
+    """The five decode configurations, deterministic in ``seed``."""
+    cid = CONFIG_NAMES.index(name) + 1
+    sub = seed * 1000 + cid
+    kt = stream_key(sub, S_TOPK)
+    if name == "tiny":
+        B, Sq, H, K = 1, 1, 16, 256
+        lens = torch.tensor([4096], dtype=torch.int32)
+        topk = _unique_sample(kt, 0, 4096, K).view(1, 1, K)
+    elif name == "decode":
+        B, Sq, H, K = 16, 1, 64, 2048
+        lens = _uniform_lens(stream_key(sub, S_LENS), B, 8192, 32768)
+        topk = torch.stack([_unique_sample(kt + b, 0, int(lens[b]), K)
+                            for b in range(B)]).view(B, 1, K)
+    elif name == "long":
+        B, Sq, H, K = 64, 1, 64, 2048
+        L = 204800
+        lens = torch.full((B,), L, dtype=torch.int32)
+        rows = []
+        for b in range(B):
+            recent = _unique_sample(kt + 2 * b, L - 4096, L, K // 2)
+            older = _unique_sample(kt + 2 * b + 1, 0, L - 4096, K // 2)
+            both = torch.cat([recent, older])
+            rows.append(both[_permutation(kt ^ (b + 0x51), K)])
+        topk = torch.stack(rows).view(B, 1, K)
+    elif name == "specverify":
+        B, Sq, H, K = 32, 4, 128, 2048
+        lens = _uniform_lens(stream_key(sub, S_LENS), B, 16384, 131072)
+        rows = []
+        for b in range(B):
+            L = int(lens[b])
+            ctx = L - Sq                                     # positions before the draft
+            pool_idx = _unique_sample(kt + b, 0, ctx, 1024 + Sq * 1020)
+            shared = pool_idx[:1024]
+            draft = torch.arange(ctx, L, dtype=torch.int64)  # the Sq draft positions
+            for s in range(Sq):
+                own = pool_idx[1024 + s * 1020:1024 + (s + 1) * 1020]
+                rows.append(torch.cat([shared, own, draft]))
+        topk = torch.stack(rows).view(B, Sq, K)
+    elif name == "splitk":
+        B, Sq, H, K = 2, 1, 16, 8192
+        L = 1 << 20
+        lens = torch.full((B,), L, dtype=torch.int32)
+        topk = torch.stack([_unique_sample(kt + b, 0, L, K) for b in range(B)]).view(B, 1, K)
+    else:
+        raise ValueError(name)
+    pt, num_slots = _page_table(sub, lens)
+    offs = torch.zeros(B, dtype=torch.int64)
+    offs[1:] = torch.cumsum(lens.to(torch.int64), 0)[:-1]
+    return Workload(name=name, B=B, Sq=Sq, H=H, K=K, seq_lens=lens,
+                    topk=topk.to(torch.int32).contiguous(), page_table=pt,
+                    num_slots=num_slots, seed=sub,
+                    outlier_channels=_outlier_channels(sub), token_offset=offs)
+
+
+# ---------------------------------------------------------------------------
+# values
+# ---------------------------------------------------------------------------
+def token_rows(w: Workload, token_ids: torch.Tensor, device="cpu"):
+    """bf16 latent [n,512] and rope [n,64] for global token ids (any device)."""
+    dev = torch.device(device)
+    ids = token_ids.to(dev, torch.int64)
+    lat = draw("normal", stream_key(w.seed, S_LATENT), ids, LATENT, dev)
+    ch = w.outlier_channels.to(dev)
+    lat[:, ch] = lat[:, ch] * 8                   # exact in bf16
+    rope = draw("normal", stream_key(w.seed, S_ROPE), ids, ROPE, dev)
+    return lat, rope
+
+
+def token_slots(w: Workload, b: int, positions: torch.Tensor) -> torch.Tensor:
+    """Physical slot of logical positions of request b (int64, CPU)."""
+    pos = positions.to(torch.int64)
+    page = w.page_table[b].to(torch.int64)[pos // PAGE]
+    return page * PAGE + pos % PAGE
+
+
+def queries(w: Workload, device="cpu") -> torch.Tensor:
+    """bf16 q [B, Sq, H, 576]."""
+    n = w.B * w.Sq * w.H
+    q = draw("normal", stream_key(w.seed, S_Q), torch.arange(n, dtype=torch.int64), QK, device)
+    return q.view(w.B, w.Sq, w.H, QK)
+
+
+def iter_pool_chunks(w: Workload, chunk: int = 1 << 18, device="cpu"):
+    """Yield (latent, rope, slots) covering every token of every request."""
+    dev = torch.device(device)
+    for b in range(w.B):
+        L = int(w.seq_lens[b])
+        for p0 in range(0, L, chunk):
+            pos = torch.arange(p0, min(L, p0 + chunk), dtype=torch.int64)
+            lat, rope = token_rows(w, pos + int(w.token_offset[b]), dev)
+            yield lat, rope, token_slots(w, b, pos).to(dev)
+
+
+def newest_tokens(w: Workload, device="cpu"):
+    """The last Sq tokens of every request (the per-step cache write):
+    latent [B*Sq,512], rope [B*Sq,64], slots int64 [B*Sq]."""
+    pos_b, ids = [], []
+    for b in range(w.B):
+        L = int(w.seq_lens[b])
+        pos = torch.arange(L - w.Sq, L, dtype=torch.int64)
+        pos_b.append(token_slots(w, b, pos))
+        ids.append(pos + int(w.token_offset[b]))
+    lat, rope = token_rows(w, torch.cat(ids), device)
+    return lat, rope, torch.cat(pos_b).to(device)
+
+
+def compact_pool_plan(w: Workload, query_ids):
+    """For oracle runs on a subset of queries: the logical pages they touch.
+
+    Returns (pt_compact int32 [B, pt_stride], pages list of (b, page_index),
+    num_slots).  The compact page table maps each touched logical page to a
+    new physical page; untouched entries are -1.  Topk entries outside
+    [0, L_eff) are masked by the method itself, so only in-range positions
+    need pages.  Generated workloads have a valid page for every in-range
+    position; error cases are built separately with full pools.
+    """
+    pt_c = torch.full_like(w.page_table, -1)
+    pages = []
+    seen = {}
+    for (b, s) in query_ids:
+        L_eff = int(w.seq_lens[b]) - (w.Sq - 1 - s)
+        idx = w.topk[b, s].to(torch.int64)
+        idx = idx[(idx >= 0) & (idx < L_eff)]
+        for pi in torch.unique(idx // PAGE).tolist():
+            if (b, pi) in seen:
+                continue
+            if pi >= w.pt_stride:
+                continue
+            seen[(b, pi)] = len(pages)
+            pages.append((b, pi))
+            pt_c[b, pi] = len(pages) - 1
+    return pt_c, pages, len(pages) * PAGE
+
+
+def compact_pool_tokens(w: Workload, pages):
+    """Tokens that fill the compact pool: (global ids int64, compact slots int64)."""
+    ids, slots = [], []
+    for cp, (b, pi) in enumerate(pages):
+        L = int(w.seq_lens[b])
+        pos = torch.arange(pi * PAGE, min(L, (pi + 1) * PAGE), dtype=torch.int64)
+        ids.append(pos + int(w.token_offset[b]))
+        slots.append(cp * PAGE + pos % PAGE)
+    if not ids:
+        return torch.zeros(0, dtype=torch.int64), torch.zeros(0, dtype=torch.int64)
+    return torch.cat(ids), torch.cat(slots)
+
+
+# ---------------------------------------------------------------------------
+# quantize-write sweep inputs (1M tokens per distribution)
+# ---------------------------------------------------------------------------
+SWEEP_KINDS = ("normal", "laplace", "zeroblocks", "ties")
+
+
+def sweep_rows(kind: str, seed: int, first: int, n: int, device="cpu"):
+    """bf16 latent [n,512] and rope [n,64] for sweep tokens first..first+n-1.
+
+    normal / laplace: i.i.d. values.  zeroblocks: N(0,1) with 25 % of the
+    16-element blocks set to zero.  ties: blocks built on E2M1 / E4M3 grid
+    midpoints (exact in bf16) so that round-half-even decides every code:
+    each block holds one element 6*s (s a random E4M3 value) and the others
+    at +-{0.25,0.75,1.25,1.75,2.5,3.5,5}*s or on the grid; a quarter of the
+    blocks instead have amax = 6*m for an E4M3 midpoint m.
+    """
+    dev = torch.device(device)
+    ids = torch.arange(first, first + n, dtype=torch.int64, device=dev)
+    key = stream_key(seed * 1000 + 77, S_LATENT)
+    rope = draw("normal", stream_key(seed * 1000 + 77, S_ROPE), ids, ROPE, dev)
+    if kind in ("normal", "zeroblocks"):
+        lat = draw("normal", key, ids, LATENT, dev)
+        if kind == "zeroblocks":
+            hz = hash_grid(stream_key(seed, S_ZERO), ids, torch.arange(32, device=dev))
+            zero = (hz & 3) == 0                                  # 25 % of blocks
+            lat = lat.view(n, 32, 16).masked_fill(zero[:, :, None], 0).view(n, LATENT)
+        return lat, rope
+    if kind == "laplace":
+        return draw("laplace", key, ids, LATENT, dev), rope
+    if kind == "ties":
+        return _tie_rows(seed, ids, dev), rope
+    raise ValueError(kind)
+
+
+def _tie_rows(seed: int, ids: torch.Tensor, dev) -> torch.Tensor:
+    n = ids.shape[0]
+    h = hash_grid(stream_key(seed, S_TIES), ids, torch.arange(LATENT, device=dev))
+    hb = hash_grid(stream_key(seed, S_TIES) ^ 0xABCDEF, ids, torch.arange(32, device=dev))
+    # E4M3 magnitudes as numbers: exponent e in [-6, 8] (normal), mantissa 0..7
+    e = (hb % 15) - 6 - 3                                    # keep 6*s well inside bf16
+    m = (hb >> 8) % 8
+    s = (1.0 + m.to(torch.float64) / 8.0) * torch.pow(2.0, e.to(torch.float64))
+    # element multipliers: grid values and midpoints of the E2M1 magnitude grid
+    mults = torch.tensor([0.0, 0.25, 0.5, 0.75, 1.0, 1.25, 1.5, 1.75, 2.0, 2.5, 3.0, 3.5,
+                          4.0, 5.0, 6.0], dtype=torch.float64, device=dev)
+    pick = mults[(h >> 8) % mults.numel()]
+    sign = torch.where((h & 1) == 1, -1.0, 1.0).to(torch.float64)
+    x = (pick * sign).view(n, 32, 16) * s[:, :, None]
+    x[:, :, 0] = 6.0 * s                                     # amax = 6 s  -> scale s
+    # a quarter of the blocks: amax = 6 * (E4M3 midpoint) to tie the scale rounding
+    mid = (1.0 + (2 * m.to(torch.float64) + 1) / 16.0) * torch.pow(2.0, e.to(torch.float64))
+    tie_scale = ((hb >> 16) & 3) == 0
+    x[:, :, 0] = torch.where(tie_scale, 6.0 * mid, x[:, :, 0])
+    return x.view(n, LATENT).to(torch.float32).to(torch.bfloat16)
