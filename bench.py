@@ -1,0 +1,438 @@
+"""Benchmark: sparse-MLA NVFP4 decode step on GB300.
+
+One step = the whole hot path on one batch: the NVFP4 cache write of the
+step's new tokens (one per session), then the sparse MLA decode over the
+paged pool (index resolution, gather, in-SMEM dequantization, QK^T and PV on
+tcgen05, online softmax, split-K merge).  Workload: the long-context
+configuration -- 64 sessions x 204,800 tokens (4.6 GB pool of 352-byte rows),
+H = 64, top-k 2048 (1024 from the most recent 4096 positions, 1024 uniform
+over the rest), page size 64 -- synthetic, seeded, built on the device.
+
+Timing: W warm-up steps, then K steps, each bracketed by CUDA events on the
+launching stream, with a 256 MiB write between steps to flush L2 (outside the
+events); barrier + synchronize around the timed loop; max over ranks.
+value = gathered-KV bytes of all ranks / max step time (GB/s).  The decode
+kernel alone is timed with an event the library records between the decode
+and merge kernels.  e2e repeats the step through the public API from pinned
+host buffers (inputs in, out/lse back) inside the timed region.
+
+--impl reference times the CPU oracle (single-threaded C++, the method's
+plain definition) on a bounded sample of the same workload.
+Multi-GPU: torchrun, one process per GPU, each rank its own 64 sessions
+(independent requests; no collective on the data path): weak scaling.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import platform
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from bit_kv_cache_nvfp4_gb300 import workloads as wl  # noqa: E402
+
+METRIC = ("sparse-MLA NVFP4 decode µs/step and gathered-KV GB/s "
+          "(% of GB300 HBM peak)")
+CONFIG_NAME = "long"
+WORKLOAD_DESC = ("long-context sparse-MLA decode step: 64 sessions x 204,800 tokens, H=64, "
+                 "top-k 2048 (1024 recent + 1024 uniform), page 64, NVFP4 352-B rows; "
+                 "cache write of 64 new tokens + decode")
+FLUSH_BYTES = 256 << 20
+
+
+def algorithmic_bytes(w: wl.Workload, valid_keys: int) -> int:
+    """Bytes a perfect decode must move: the selected rows, the index and
+    page-table words, q, out and lse (one page-table word per key is an upper
+    bound)."""
+    n_q = w.B * w.Sq
+    return valid_keys * 352 + n_q * w.K * 4 * 2 + n_q * w.H * (1152 + 1024 + 4)
+
+
+def valid_key_count(w: wl.Workload) -> int:
+    n = 0
+    for b in range(w.B):
+        for s in range(w.Sq):
+            L_eff = int(w.seq_lens[b]) - (w.Sq - 1 - s)
+            row = w.topk[b, s]
+            n += int(((row >= 0) & (row < L_eff)).sum())
+    return n
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+def ncu_traffic_bytes():
+    """DRAM bytes per decode launch from the committed ncu summary, if any."""
+    path = os.path.join(ROOT, "profiles", "decode_long_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d.get("dram_bytes_per_launch")
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out = ""
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in getattr(self, "lines", []):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:8]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def reduce_over_ranks(t_ms: float, nbytes: float, device=None):
+    """(max step time over ranks, sum of bytes over ranks); the identity
+    without an initialized process group."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(t_ms), float(nbytes)
+    t = torch.tensor([float(t_ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    b = torch.tensor([float(nbytes)], dtype=torch.float64, device=device)
+    dist.all_reduce(b, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(b.item())
+
+
+def cpu_model() -> str:
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu part")):
+                    return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return platform.machine()
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle on a bounded sample
+# ---------------------------------------------------------------------------
+def oracle_sample(w: wl.Workload, requests, repeats: int = 1):
+    """Time the oracle's step (cache write of the requests' new tokens +
+    decode) on `requests`; returns (seconds per repeat, gathered bytes)."""
+    import oracle
+    bits = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)
+    qids = [(b, s) for b in requests for s in range(w.Sq)]
+    pt_c, pages, ns = wl.compact_pool_plan(w, qids)
+    ids, cslots = wl.compact_pool_tokens(w, pages, qids)
+    lat, rope = wl.token_rows(w, ids)
+    pool = np.zeros((max(ns, 64), 352), dtype=np.uint8)
+    oracle.quantize_write(bits(lat), bits(rope), cslots.numpy(), pool)
+    q = bits(wl.queries(w))
+    nl, nr, nslots = wl.newest_tokens(w)
+    sel = torch.tensor([b * w.Sq + s for b in requests for s in range(w.Sq)])
+    nl, nr = bits(nl[sel]), bits(nr[sel])
+    # the new tokens go to scratch rows past the compact pool (same work, no overlap)
+    scratch = np.zeros((len(sel), 352), dtype=np.uint8)
+    new_slots = np.arange(len(sel), dtype=np.int64)
+    per_req = [(np.ascontiguousarray(q[b:b + 1]), np.ascontiguousarray(pt_c[b:b + 1].numpy()),
+                np.ascontiguousarray(w.topk[b:b + 1].numpy()),
+                np.ascontiguousarray(w.seq_lens[b:b + 1].numpy())) for b in requests]
+    t0 = time.perf_counter()
+    for _ in range(repeats):
+        oracle.quantize_write(nl, nr, new_slots, scratch)
+        for qb, ptb, tb, lb in per_req:
+            oracle.sparse_mla_decode(qb, pool, ptb, tb, lb, w.sm_scale)
+    dt = (time.perf_counter() - t0) / repeats
+    valid = 0
+    for b in requests:
+        for s in range(w.Sq):
+            L_eff = int(w.seq_lens[b]) - (w.Sq - 1 - s)
+            row = w.topk[b, s]
+            valid += int(((row >= 0) & (row < L_eff)).sum())
+    return dt, valid * 352
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    w = wl.make_workload(CONFIG_NAME, seed=0)
+    reqs = list(range(4))                       # bounded per-step sample
+    for _ in range(args.warmup):
+        oracle_sample(w, reqs)
+    times = []
+    gathered = 0
+    for _ in range(args.steps):
+        dt, gathered = oracle_sample(w, reqs)
+        times.append(dt)
+    t = sum(times) / len(times)
+    gbs = gathered / t / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": t * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": WORKLOAD_DESC, "sample": f"{len(reqs)} of {w.B} sessions per step"},
+        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{len(reqs)} sessions (new-token write + decode) per step",
+                         "cpu": cpu_model()},
+        "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+def build_pool(w: wl.Workload, dev) -> torch.Tensor:
+    import bit_kv_cache_nvfp4_gb300 as kv
+    pool = torch.zeros((w.num_slots, 352), dtype=torch.uint8, device=dev)
+    for lat, rope, slots in wl.iter_pool_chunks(w, chunk=1 << 18, device=dev):
+        kv.quantize_write(lat, rope, slots, pool)
+    torch.cuda.synchronize(dev)
+    return pool
+
+
+def run_gpu(args):
+    import bit_kv_cache_nvfp4_gb300 as kv
+    world, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device for the GPU arm")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    w = wl.make_workload(CONFIG_NAME, seed=rank)
+    pool = build_pool(w, dev)
+    q = wl.queries(w, dev)
+    pt, topk, lens = w.page_table.to(dev), w.topk.to(dev), w.seq_lens.to(dev)
+    new_lat, new_rope, new_slots = wl.newest_tokens(w, dev)
+    splits, ws_bytes = kv.decode_plan(w.B, w.Sq, w.H, w.K)
+    out = torch.empty((w.B, w.Sq, w.H, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((w.B, w.Sq, w.H), dtype=torch.float32, device=dev)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        kv.quantize_write(new_lat, new_rope, new_slots, pool, err)
+        kv.sparse_mla_decode(q, pool, pt, topk, lens, w.sm_scale, out=out, lse=lse, workspace=ws,
+                             dev_err=err)
+
+    valid = valid_key_count(w)
+    kv_bytes = valid * 352
+    alg_bytes = algorithmic_bytes(w, valid)
+    flops = 2.0 * w.H * valid * (576 + 512)
+    launches_per_step = 2 + (1 if splits > 1 else 0)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    assert int(err.item()) == 0, f"device error flags {int(err.item())}"
+
+    e0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    e1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    d0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    d1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    wall0 = time.perf_counter()
+    with ClockSampler(local) as clocks:
+        for i in range(args.steps):
+            flush.zero_()
+            e0[i].record(stream)
+            kv.quantize_write(new_lat, new_rope, new_slots, pool, err)
+            d0[i].record(stream)
+            kv.set_timing_event(d1[i])
+            kv.sparse_mla_decode(q, pool, pt, topk, lens, w.sm_scale, out=out, lse=lse,
+                                 workspace=ws, dev_err=err)
+            e1[i].record(stream)
+        kv.set_timing_event(None)
+        torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - wall0
+    if world > 1:
+        torch.distributed.barrier()
+    step_ms = [a.elapsed_time(b) for a, b in zip(e0, e1)]
+    dec_ms = [a.elapsed_time(b) for a, b in zip(d0, d1)]
+    t_ms = sum(step_ms) / len(step_ms)
+    dec_ms_avg = sum(dec_ms) / len(dec_ms)
+    assert int(err.item()) == 0, f"device error flags {int(err.item())}"
+
+    max_ms, tot_bytes = reduce_over_ranks(t_ms, kv_bytes, dev if world > 1 else None)
+    value = tot_bytes / (max_ms * 1e-3) / 1e9
+
+    # end to end through the public API, host buffers in and out
+    e2e = run_e2e(kv, w, dev, pool, pt, lens, flush, args)
+
+    peak_gbs, peak_tflops, peak_kind = measured_peaks()
+    achieved = alg_bytes / (dec_ms_avg * 1e-3) / 1e9
+    cpu = None
+    if rank == 0 and not args.skip_cpu:
+        reqs = list(range(min(w.B, args.cpu_sessions)))
+        dt, gathered = oracle_sample(w, reqs)
+        cpu = {"value": gathered / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": f"{len(reqs)} of {w.B} sessions: new-token cache write + decode, "
+                         f"{dt:.2f} s", "cpu": cpu_model()}
+    if world > 1:
+        torch.distributed.barrier()
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": max_ms,
+            "us_per_step": max_ms * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": WORKLOAD_DESC, "B": w.B, "Sq": w.Sq, "H": w.H, "K": w.K,
+                       "seq_len": int(w.seq_lens[0]), "pool_bytes": w.num_slots * 352,
+                       "splits": splits, "l2": "flushed between timed steps (256 MiB write)",
+                       "parallelism": f"{world} independent ranks (sessions sharded)"},
+            "kv_bytes_per_step": kv_bytes * world, "algorithmic_bytes_per_step": alg_bytes * world,
+            "decode_kernel_us": dec_ms_avg * 1e3,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak_gbs, "unit": "GB/s",
+                         "frac": achieved / peak_gbs, "traffic": ncu_traffic_bytes(),
+                         "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
+                         if peak_kind == "measured" else "fallback 6800 GB/s",
+                         "kernel": "decode_kernel<64> (merge excluded)",
+                         "tensor_tflops": flops / (dec_ms_avg * 1e-3) / 1e12,
+                         "tensor_frac_of_bf16_peak": flops / (dec_ms_avg * 1e-3) / 1e12 /
+                         peak_tflops},
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clocks.summary(),
+            "wall_s_timed_loop": wall,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def run_e2e(kv, w, dev, pool, pt, lens, flush, args):
+    """Same step through the public API with pinned host inputs and outputs."""
+    q_h = wl.queries(w).pin_memory()
+    topk_h = w.topk.pin_memory()
+    nl, nr, ns = wl.newest_tokens(w)
+    nl_h, nr_h, ns_h = nl.pin_memory(), nr.pin_memory(), ns.pin_memory()
+    out_h = torch.empty((w.B, w.Sq, w.H, 512), dtype=torch.bfloat16).pin_memory()
+    lse_h = torch.empty((w.B, w.Sq, w.H), dtype=torch.float32).pin_memory()
+    q_d = torch.empty_like(q_h, device=dev)
+    topk_d = torch.empty_like(topk_h, device=dev)
+    nl_d, nr_d, ns_d = (torch.empty_like(nl_h, device=dev), torch.empty_like(nr_h, device=dev),
+                        torch.empty_like(ns_h, device=dev))
+    stream = torch.cuda.current_stream(dev)
+    h2d = sum(t.numel() * t.element_size() for t in (q_h, topk_h, nl_h, nr_h, ns_h))
+    d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
+
+    def step():
+        q_d.copy_(q_h, non_blocking=True)
+        topk_d.copy_(topk_h, non_blocking=True)
+        nl_d.copy_(nl_h, non_blocking=True)
+        nr_d.copy_(nr_h, non_blocking=True)
+        ns_d.copy_(ns_h, non_blocking=True)
+        kv.quantize_write(nl_d, nr_d, ns_d, pool)
+        out, lse = kv.sparse_mla_decode(q_d, pool, pt, topk_d, lens, w.sm_scale)
+        out_h.copy_(out, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    times = []
+    for _ in range(args.steps):
+        flush.zero_()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        step()
+        b.record(stream)
+        b.synchronize()
+        times.append(a.elapsed_time(b))
+    t = sum(times) / len(times)
+    valid = valid_key_count(w)
+    return {"value": valid * 352 / (t * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": t,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+def main(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--cpu-sessions", type=int, default=64)
+    p.add_argument("--skip-cpu", action="store_true")
+    args = p.parse_args(argv)
+    if args.warmup < 3:
+        p.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,212 @@
+"""NVFP4 latent-KV cache write and sparse MLA decode for GB300 (sm_103a).
+
+A thin Python binding over ``libkv4mla.so`` (C ABI in ``include/kv4mla.h``).
+Every step of the computation runs in the library's CUDA kernels; this
+module only checks tensors, passes device pointers and the current CUDA
+stream, allocates outputs and the split-K workspace with PyTorch, and turns
+status codes into exceptions.  There is no CPU fallback: if the library
+cannot be loaded, importing the functions raises.
+
+Row format and method: numinousmuses "inference-optimizations" README,
+sections "4-bit KV cache" (352-byte NVFP4 row, kv4mla decode) and
+"Attention kernels" (split-K sparse decode).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+__all__ = [
+    "Kv4Error", "library_path", "load_library", "quantize_write", "decode_plan",
+    "sparse_mla_decode", "debug_gather_dequant", "set_wait_limit", "set_timing_event",
+    "ROW_BYTES", "LATENT", "ROPE", "QK_DIM", "PAGE", "DEV_BAD_SLOT", "DEV_BAD_PAGE",
+    "DEV_TIMEOUT",
+]
+
+ROW_BYTES, LATENT, ROPE, QK_DIM, PAGE, TILE_KEYS = 352, 512, 64, 576, 64, 128
+DEV_BAD_SLOT, DEV_BAD_PAGE, DEV_TIMEOUT = 1, 2, 4
+_STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported shape or page size",
+           3: "device is not compute capability 10.3", 4: "kernel launch failed",
+           5: "workspace missing or too small"}
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_lock = threading.Lock()
+_lib = None
+_workspaces: dict = {}
+
+
+class Kv4Error(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn}: {_STATUS.get(status, 'unknown status')} (status {status})")
+        self.status = status
+
+
+def library_path() -> str:
+    return os.path.join(_HERE, "libkv4mla.so")
+
+
+def load_library():
+    """Load libkv4mla.so (building it first if the sources are newer)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        from . import build as _build
+        path = _build.build()
+        lib = ctypes.CDLL(path)
+        P, i32, i64, f32, sz = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64,
+                                ctypes.c_float, ctypes.c_size_t)
+        lib.kv4_quantize_write.argtypes = [P, i64, P, i64, P, i64, P, i64, P, P]
+        lib.kv4_quantize_write.restype = i32
+        lib.kv4_decode_plan.argtypes = [i32, i32, i32, i32, i32, ctypes.POINTER(i32),
+                                        ctypes.POINTER(sz)]
+        lib.kv4_decode_plan.restype = i32
+        lib.kv4_sparse_mla_decode.argtypes = [P, P, i64, P, i64, i32, P, i32, P, i32, i32, i32,
+                                              f32, P, P, P, sz, i32, P, P]
+        lib.kv4_sparse_mla_decode.restype = i32
+        lib.kv4_debug_gather_dequant.argtypes = [P, i64, P, i64, i32, P, i32, P, i32, i32, P, P,
+                                                 P]
+        lib.kv4_debug_gather_dequant.restype = i32
+        lib.kv4_set_wait_limit.argtypes = [i64, i32]
+        lib.kv4_set_wait_limit.restype = i32
+        lib.kv4_set_timing_event.argtypes = [P]
+        lib.kv4_set_timing_event.restype = i32
+        lib.kv4_status_str.argtypes = [i32]
+        lib.kv4_status_str.restype = ctypes.c_char_p
+        lib.kv4_version.argtypes = []
+        lib.kv4_version.restype = i32
+        _lib = lib
+        return lib
+
+
+def _check(fn: str, status: int):
+    if status != 0:
+        raise Kv4Error(fn, status)
+
+
+def _dev(t: torch.Tensor, name: str, dtype: torch.dtype, contiguous: bool = True):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if contiguous and not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _err_ptr(dev_err):
+    if dev_err is None:
+        return None
+    return _dev(dev_err, "dev_err", torch.int32)
+
+
+def quantize_write(latent: torch.Tensor, rope: torch.Tensor, slot_mapping: torch.Tensor,
+                   pool: torch.Tensor, dev_err: torch.Tensor | None = None) -> None:
+    """Quantize latent bf16 [N,512] and rope bf16 [N,64] into pool uint8
+    [num_slots,352] at slot_mapping int64 [N] (negative = skip)."""
+    lib = load_library()
+    n = slot_mapping.shape[0]
+    if latent.dim() != 2 or rope.dim() != 2 or latent.shape[0] != n or rope.shape[0] != n:
+        raise ValueError("latent [N,512], rope [N,64] and slot_mapping [N] must agree")
+    if latent.stride(1) != 1 or rope.stride(1) != 1:
+        raise ValueError("latent and rope rows must be contiguous")
+    _check("kv4_quantize_write", lib.kv4_quantize_write(
+        _dev(latent, "latent", torch.bfloat16, False), latent.stride(0),
+        _dev(rope, "rope", torch.bfloat16, False), rope.stride(0),
+        _dev(slot_mapping, "slot_mapping", torch.int64), n,
+        _dev(pool, "pool", torch.uint8), pool.shape[0], _err_ptr(dev_err),
+        _stream(pool.device)))
+
+
+def decode_plan(B: int, Sq: int, H: int, K: int, force_splits: int = 0):
+    """(splits, workspace_bytes) the decode will use on the current device."""
+    lib = load_library()
+    s = ctypes.c_int(0)
+    ws = ctypes.c_size_t(0)
+    _check("kv4_decode_plan", lib.kv4_decode_plan(B, Sq, H, K, force_splits, ctypes.byref(s),
+                                                  ctypes.byref(ws)))
+    return s.value, ws.value
+
+
+def _workspace(device, nbytes: int):
+    if nbytes == 0:
+        return None
+    key = (str(device), torch.cuda.current_stream(device).cuda_stream)
+    buf = _workspaces.get(key)
+    if buf is None or buf.numel() < nbytes:
+        buf = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        _workspaces[key] = buf
+    return buf
+
+
+def sparse_mla_decode(q: torch.Tensor, pool: torch.Tensor, page_table: torch.Tensor,
+                      topk_idx: torch.Tensor, seq_lens: torch.Tensor, sm_scale: float,
+                      out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
+                      workspace: torch.Tensor | None = None, force_splits: int = 0,
+                      dev_err: torch.Tensor | None = None):
+    """Sparse MLA decode over the NVFP4 pool.
+
+    q bf16 [B,Sq,H,576]; pool uint8 [num_slots,352]; page_table int32
+    [B,pt_stride]; topk_idx int32 [B,Sq,K] (logical positions, -1 = pad);
+    seq_lens int32 [B].  Returns (out bf16 [B,Sq,H,512], lse fp32 [B,Sq,H]).
+    """
+    lib = load_library()
+    B, Sq, H, D = q.shape
+    if D != QK_DIM:
+        raise ValueError("q must be [B, Sq, H, 576]")
+    K = topk_idx.shape[2]
+    if tuple(topk_idx.shape[:2]) != (B, Sq) or seq_lens.shape[0] != B or page_table.shape[0] != B:
+        raise ValueError("topk_idx [B,Sq,K], seq_lens [B] and page_table [B,*] must agree with q")
+    dev = q.device
+    if out is None:
+        out = torch.empty((B, Sq, H, LATENT), dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((B, Sq, H), dtype=torch.float32, device=dev)
+    splits, ws_bytes = decode_plan(B, Sq, H, K, force_splits)
+    if workspace is None:
+        workspace = _workspace(dev, ws_bytes)
+    ws_ptr = None if workspace is None else _dev(workspace, "workspace", workspace.dtype)
+    ws_len = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("kv4_sparse_mla_decode", lib.kv4_sparse_mla_decode(
+        _dev(q, "q", torch.bfloat16), _dev(pool, "pool", torch.uint8), pool.shape[0],
+        _dev(page_table, "page_table", torch.int32), page_table.shape[1], PAGE,
+        _dev(topk_idx, "topk_idx", torch.int32), K, _dev(seq_lens, "seq_lens", torch.int32),
+        B, Sq, H, float(sm_scale), _dev(out, "out", torch.bfloat16),
+        _dev(lse, "lse", torch.float32), ws_ptr, ws_len, force_splits, _err_ptr(dev_err),
+        _stream(dev)))
+    return out, lse
+
+
+def debug_gather_dequant(pool: torch.Tensor, page_table: torch.Tensor, topk_idx: torch.Tensor,
+                         seq_lens: torch.Tensor, dev_err: torch.Tensor | None = None):
+    """The decode's gather + dequantization: bf16 [B,Sq,K,576] (masked rows 0)."""
+    lib = load_library()
+    B, Sq, K = topk_idx.shape
+    rows = torch.empty((B, Sq, K, QK_DIM), dtype=torch.bfloat16, device=pool.device)
+    _check("kv4_debug_gather_dequant", lib.kv4_debug_gather_dequant(
+        _dev(pool, "pool", torch.uint8), pool.shape[0],
+        _dev(page_table, "page_table", torch.int32), page_table.shape[1], PAGE,
+        _dev(topk_idx, "topk_idx", torch.int32), K, _dev(seq_lens, "seq_lens", torch.int32),
+        B, Sq, _dev(rows, "rows", torch.bfloat16), _err_ptr(dev_err), _stream(pool.device)))
+    return rows
+
+
+def set_timing_event(event: "torch.cuda.Event | None") -> None:
+    """Measurement hook: record ``event`` between the decode and merge kernels
+    of every later sparse_mla_decode call (None turns it off)."""
+    handle = None if event is None else ctypes.c_void_p(event.cuda_event)
+    _check("kv4_set_timing_event", load_library().kv4_set_timing_event(handle))
+
+
+def set_wait_limit(timeout_ns: int = 0, fault_site: int = 0) -> None:
+    """Test hook: bounded-wait limit for the next launches and an optional
+    injected wait on a barrier nothing arrives on (fault_site=1)."""
+    _check("kv4_set_wait_limit", load_library().kv4_set_wait_limit(int(timeout_ns),
+                                                                   int(fault_site)))

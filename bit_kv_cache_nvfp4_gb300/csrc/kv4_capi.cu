@@ -1,0 +1,244 @@
+// kv4_capi.cu -- the extern "C" entry points of libkv4mla.so declared in
+// include/kv4mla.h: argument validation, the split-K planner and the
+// stream-ordered launches.  The library never allocates device memory and
+// never synchronizes.
+#include "kv4mla.h"
+#include "kv4_launch.h"
+
+#include <atomic>
+#include <cstdint>
+#include <cstdlib>
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_sms[kMaxDevices];          // 0 = not queried yet
+std::atomic<int> g_cc[kMaxDevices];           // major*10 + minor
+std::atomic<int64_t> g_timeout_ns{1000000000};  // bounded-wait limit: 1 s
+std::atomic<int> g_fault_site{0};
+std::atomic<void*> g_timing_event{nullptr};
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// SM count and compute capability of the current device (cached).
+kv4_status device_info(int* sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+    return KV4_ERR_LAUNCH;
+  int n = g_sms[dev].load(std::memory_order_relaxed);
+  int cc = g_cc[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return KV4_ERR_LAUNCH;
+    cc = major * 10 + minor;
+    g_cc[dev].store(cc, std::memory_order_relaxed);
+    g_sms[dev].store(n, std::memory_order_relaxed);
+  }
+  if (cc != 103) return KV4_ERR_ARCH;           // built for sm_103a only
+  *sms = n;
+  return KV4_OK;
+}
+
+int heads_per_block(int H) {
+  if (H == 16 || H == 32 || H == 64) return H;
+  if (H > 64 && H <= 256 && H % 64 == 0) return 64;
+  return 0;
+}
+
+struct Plan {
+  int HG, units, tiles, splits, tiles_per_split;
+  size_t ws_bytes;
+};
+
+// Split-K planner: pick the number of partitions S of each query's tiles
+// that minimizes (waves of thread blocks) x (tiles per partition), plus a
+// half-tile charge for the merge when S > 1; ties go to the smaller S.
+Plan make_plan(int B, int Sq, int H, int K, int force_splits, int sms) {
+  Plan p{};
+  p.HG = heads_per_block(H);
+  p.units = B * Sq * (H / p.HG);
+  p.tiles = (K + KV4_TILE_KEYS - 1) / KV4_TILE_KEYS;
+  int S = 1;
+  if (p.tiles > 1) {
+    if (force_splits > 0) {
+      S = force_splits < p.tiles ? force_splits : p.tiles;
+    } else {
+      double best = 1e300;
+      for (int c = 1; c <= p.tiles; ++c) {
+        const long long waves = (static_cast<long long>(p.units) * c + sms - 1) / sms;
+        const int per = (p.tiles + c - 1) / c;
+        const double cost = static_cast<double>(waves) * per + (c > 1 ? 0.5 : 0.0);
+        if (cost < best - 1e-9) { best = cost; S = c; }
+      }
+    }
+  }
+  p.tiles_per_split = p.tiles > 0 ? (p.tiles + S - 1) / S : 0;
+  p.splits = p.tiles_per_split > 0 ? (p.tiles + p.tiles_per_split - 1) / p.tiles_per_split : 1;
+  p.ws_bytes = p.splits > 1 ? static_cast<size_t>(p.units) * p.splits * p.HG *
+                                  (KV4_LATENT + 1) * sizeof(float)
+                            : 0;
+  return p;
+}
+
+kv4_status check_decode_shape(int B, int Sq, int H, int K) {
+  if (B < 0 || Sq < 1 || K < 0) return KV4_ERR_INVALID_ARG;
+  if (heads_per_block(H) == 0) return KV4_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * Sq * H > (1LL << 30)) return KV4_ERR_INVALID_ARG;
+  return KV4_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+kv4_status kv4_quantize_write(const void* latent_dev, int64_t latent_row_stride,
+                              const void* rope_dev, int64_t rope_row_stride,
+                              const int64_t* slot_mapping_dev, int64_t n_tokens,
+                              uint8_t* pool_dev, int64_t num_slots, int32_t* dev_err,
+                              kv4_stream_t stream) {
+  if (n_tokens < 0 || num_slots < 0) return KV4_ERR_INVALID_ARG;
+  if (n_tokens == 0) return KV4_OK;
+  if (!latent_dev || !rope_dev || !slot_mapping_dev || !pool_dev) return KV4_ERR_INVALID_ARG;
+  if (latent_row_stride < KV4_LATENT || latent_row_stride % 8 != 0 ||
+      rope_row_stride < KV4_ROPE || rope_row_stride % 8 != 0)
+    return KV4_ERR_INVALID_ARG;
+  if (!aligned16(latent_dev) || !aligned16(rope_dev) || !aligned16(pool_dev) ||
+      (reinterpret_cast<uintptr_t>(slot_mapping_dev) & 7u) != 0)
+    return KV4_ERR_INVALID_ARG;
+  if (num_slots > INT64_MAX / KV4_ROW_BYTES) return KV4_ERR_INVALID_ARG;
+  int sms = 0;
+  const kv4_status st = device_info(&sms);
+  if (st != KV4_OK) return st;
+  kv4::QuantizeArgs a{latent_dev, latent_row_stride, rope_dev,  rope_row_stride, slot_mapping_dev,
+                      n_tokens,   pool_dev,          num_slots, dev_err};
+  return kv4::launch_quantize_write(a, sms, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? KV4_OK
+             : KV4_ERR_LAUNCH;
+}
+
+kv4_status kv4_decode_plan(int B, int Sq, int H, int K, int force_splits, int* splits,
+                           size_t* workspace_bytes) {
+  const kv4_status shape = check_decode_shape(B, Sq, H, K);
+  if (shape != KV4_OK) return shape;
+  int sms = 0;
+  const kv4_status st = device_info(&sms);
+  if (st != KV4_OK) return st;
+  const Plan p = make_plan(B, Sq, H, K, force_splits, sms);
+  if (splits) *splits = p.splits;
+  if (workspace_bytes) *workspace_bytes = p.ws_bytes;
+  return KV4_OK;
+}
+
+kv4_status kv4_sparse_mla_decode(const void* q_dev, const uint8_t* pool_dev, int64_t num_slots,
+                                 const int32_t* page_table_dev, int64_t pt_stride, int page_size,
+                                 const int32_t* topk_idx_dev, int K, const int32_t* seq_lens_dev,
+                                 int B, int Sq, int H, float sm_scale, void* out_dev,
+                                 float* lse_dev, void* workspace_dev, size_t workspace_bytes,
+                                 int force_splits, int32_t* dev_err, kv4_stream_t stream) {
+  const kv4_status shape = check_decode_shape(B, Sq, H, K);
+  if (shape != KV4_OK) return shape;
+  if (page_size != KV4_PAGE) return KV4_ERR_UNSUPPORTED;
+  if (B == 0) return KV4_OK;
+  if (!q_dev || !pool_dev || !page_table_dev || !topk_idx_dev || !seq_lens_dev || !out_dev ||
+      !lse_dev)
+    return KV4_ERR_INVALID_ARG;
+  if (num_slots < 0 || num_slots > INT32_MAX || pt_stride < 1 || pt_stride > INT32_MAX)
+    return KV4_ERR_INVALID_ARG;
+  if (!aligned16(q_dev) || !aligned16(pool_dev) || !aligned16(out_dev) ||
+      (reinterpret_cast<uintptr_t>(lse_dev) & 3u) != 0 ||
+      (reinterpret_cast<uintptr_t>(page_table_dev) & 3u) != 0 ||
+      (reinterpret_cast<uintptr_t>(topk_idx_dev) & 3u) != 0 ||
+      (reinterpret_cast<uintptr_t>(seq_lens_dev) & 3u) != 0)
+    return KV4_ERR_INVALID_ARG;
+  int sms = 0;
+  const kv4_status st = device_info(&sms);
+  if (st != KV4_OK) return st;
+  const Plan p = make_plan(B, Sq, H, K, force_splits, sms);
+  if (p.ws_bytes > 0 &&
+      (workspace_dev == nullptr || workspace_bytes < p.ws_bytes || !aligned16(workspace_dev)))
+    return KV4_ERR_WORKSPACE;
+
+  kv4::DecodeArgs a{};
+  a.q = q_dev;
+  a.pool = pool_dev;
+  a.num_slots = num_slots;
+  a.page_table = page_table_dev;
+  a.pt_stride = pt_stride;
+  a.topk = topk_idx_dev;
+  a.K = K;
+  a.seq_lens = seq_lens_dev;
+  a.B = B;
+  a.Sq = Sq;
+  a.H = H;
+  a.HG = p.HG;
+  a.splits = p.splits;
+  a.tiles_per_split = p.tiles_per_split;
+  a.sm_scale = sm_scale;
+  a.out = out_dev;
+  a.lse = lse_dev;
+  if (p.splits > 1) {
+    a.ws_o = static_cast<float*>(workspace_dev);
+    a.ws_lse = a.ws_o + static_cast<size_t>(p.units) * p.splits * p.HG * KV4_LATENT;
+  }
+  a.dev_err = dev_err;
+  a.timeout_ns = static_cast<uint64_t>(g_timeout_ns.load());
+  a.fault_site = g_fault_site.load();
+  a.after_decode = static_cast<cudaEvent_t>(g_timing_event.load());
+  return kv4::launch_decode(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? KV4_OK
+             : KV4_ERR_LAUNCH;
+}
+
+kv4_status kv4_debug_gather_dequant(const uint8_t* pool_dev, int64_t num_slots,
+                                    const int32_t* page_table_dev, int64_t pt_stride,
+                                    int page_size, const int32_t* topk_idx_dev, int K,
+                                    const int32_t* seq_lens_dev, int B, int Sq, void* rows_dev,
+                                    int32_t* dev_err, kv4_stream_t stream) {
+  if (B < 0 || Sq < 1 || K < 0) return KV4_ERR_INVALID_ARG;
+  if (page_size != KV4_PAGE) return KV4_ERR_UNSUPPORTED;
+  if (B == 0 || K == 0) return KV4_OK;
+  if (!pool_dev || !page_table_dev || !topk_idx_dev || !seq_lens_dev || !rows_dev)
+    return KV4_ERR_INVALID_ARG;
+  if (num_slots < 0 || num_slots > INT32_MAX || pt_stride < 1 || pt_stride > INT32_MAX)
+    return KV4_ERR_INVALID_ARG;
+  if (!aligned16(pool_dev) || !aligned16(rows_dev)) return KV4_ERR_INVALID_ARG;
+  int sms = 0;
+  const kv4_status st = device_info(&sms);
+  if (st != KV4_OK) return st;
+  kv4::GatherArgs a{pool_dev, num_slots, page_table_dev, pt_stride, topk_idx_dev,
+                    K,        seq_lens_dev, B,          Sq,        rows_dev, dev_err};
+  return kv4::launch_debug_gather(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? KV4_OK
+             : KV4_ERR_LAUNCH;
+}
+
+kv4_status kv4_set_wait_limit(int64_t timeout_ns, int fault_site) {
+  if (timeout_ns < 0 || fault_site < 0 || fault_site > 1) return KV4_ERR_INVALID_ARG;
+  g_timeout_ns.store(timeout_ns > 0 ? timeout_ns : 1000000000);
+  g_fault_site.store(fault_site);
+  return KV4_OK;
+}
+
+kv4_status kv4_set_timing_event(void* cuda_event) {
+  g_timing_event.store(cuda_event);
+  return KV4_OK;
+}
+
+const char* kv4_status_str(kv4_status status) {
+  switch (status) {
+    case KV4_OK: return "ok";
+    case KV4_ERR_INVALID_ARG: return "invalid argument";
+    case KV4_ERR_UNSUPPORTED: return "unsupported shape or page size";
+    case KV4_ERR_ARCH: return "current device is not compute capability 10.3";
+    case KV4_ERR_LAUNCH: return "kernel launch failed";
+    case KV4_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+  }
+  return "unknown status";
+}
+
+int kv4_version(void) { return 1; }
+
+}  // extern "C"

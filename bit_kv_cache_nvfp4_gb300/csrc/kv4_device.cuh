@@ -1,0 +1,383 @@
+// kv4_device.cuh -- device helpers shared by the kernels of libkv4mla.so:
+// inline PTX for mbarriers and the 5th-generation tensor core (tcgen05 MMA,
+// tensor memory), shared-memory matrix descriptors, the NVFP4 row
+// dequantization and the top-k index resolution.
+//
+// Row format (numinousmuses "inference-optimizations" README, "4-bit KV
+// cache"): 352 bytes = 256 bytes of E2M1 latent codes (byte j holds elements
+// 2j in its low nibble and 2j+1 in its high nibble) + 32 E4M3 scales (one
+// per 16 latent elements) + 64 E4M3 rope values.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace kv4 {
+
+constexpr int kRowBytes = 352;
+constexpr int kLatent = 512;
+constexpr int kRope = 64;
+constexpr int kQk = 576;
+constexpr int kPage = 64;
+constexpr int kTileKeys = 128;          // keys per MMA tile (the MMA's M)
+constexpr int kChunkBytes = kTileKeys * 128;   // one 64-column slab of a tile
+
+constexpr int kDevBadSlot = 1;
+constexpr int kDevBadPage = 2;
+constexpr int kDevTimeout = 4;
+
+// ---------------------------------------------------------------------------
+// small utilities
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void flag_error(int32_t* dev_err, int flag) {
+  if (dev_err != nullptr) atomicOr(dev_err, flag);
+}
+
+// Byte offset inside a swizzled operand region (base 1024-byte aligned):
+// the hardware XORs address bits [4, 4+B) with bits [7, 7+B), B = 3 for the
+// 128-byte swizzle, 2 for 64-byte, 1 for 32-byte.
+template <int B>
+__device__ __forceinline__ uint32_t swizzle(uint32_t off) {
+  return off ^ (((off >> 7) & ((1u << B) - 1u)) << 4);
+}
+
+// ---------------------------------------------------------------------------
+// mbarrier
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for the phase with the given parity; gives up after timeout_ns.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
+                                                  uint64_t timeout_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (global_timer_ns() - t0 > timeout_ns) return false;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// proxy / tensor-core fences
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void fence_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_before_sync() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after_sync() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Named barrier among `count` threads (a multiple of 32).
+__device__ __forceinline__ void named_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+// Named barrier that also returns whether any participant passed true.
+__device__ __forceinline__ bool named_sync_or(int id, int count, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+      "barrier.cta.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(count)
+      : "memory");
+  return r != 0;
+}
+
+// ---------------------------------------------------------------------------
+// tensor memory
+// ---------------------------------------------------------------------------
+// Allocate ncols (power of two >= 32) TMEM columns; the base address is
+// written to shared memory at dst.  Whole warp.
+__device__ __forceinline__ void tmem_alloc(uint32_t dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+
+// 32 lanes x 32 bits, 16 consecutive columns: thread i of the warp receives
+// lane (quarter*32 + i); taddr carries the lane quarter in bits [16, 32).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                 "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+               ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]),
+               "r"(r[6]), "r"(r[7])
+               : "memory");
+}
+
+// Load then wait, with the destination registers tied to the wait so that
+// no use of them can be scheduled before the data has arrived.
+__device__ __forceinline__ void tmem_ld16_sync(uint32_t taddr, uint32_t (&r)[16]) {
+  tmem_ld16(taddr, r);
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                 "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                 "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
+               :
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld8_sync(uint32_t taddr, uint32_t (&r)[8]) {
+  tmem_ld8(taddr, r);
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                 "+r"(r[6]), "+r"(r[7])
+               :
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld_wait() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
+// tcgen05 MMA (kind::f16, bf16 inputs, fp32 accumulator in TMEM)
+// ---------------------------------------------------------------------------
+enum : uint32_t {
+  kSwizzleNone = 0,
+  kSwizzle128 = 2,
+  kSwizzle64 = 4,
+  kSwizzle32 = 6,
+};
+
+// Shared-memory matrix descriptor: start address, leading- and stride-
+// dimension byte offsets (16-byte units), descriptor version 1, swizzle.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes,
+                                              uint32_t sbo_bytes, uint32_t swizzle_mode) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(swizzle_mode & 7u) << 61;
+  return d;
+}
+
+// Instruction descriptor: D fp32, A and B bf16, dense, no negation.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major,
+                                                  bool b_mn_major) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn_major ? 1u : 0u) << 15) |
+         ((b_mn_major ? 1u : 0u) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive on an mbarrier once every MMA issued so far by this thread is done.
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// minifloat conversions (exact)
+// ---------------------------------------------------------------------------
+// Four E2M1 byte pairs (8 codes) -> four f16x2 (low nibble -> low half).
+__device__ __forceinline__ void e2m1x8_to_f16x8(uint32_t w, uint32_t (&h)[4]) {
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+      : "r"(w));
+}
+
+// Two E4M3 bytes (low byte -> low half) -> f16x2.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_bytes) {
+  uint32_t h;
+  const uint16_t v = static_cast<uint16_t>(two_bytes);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(v));
+  return h;
+}
+
+// One E4M3 byte -> float (exact).
+__device__ __forceinline__ float e4m3_to_float(uint32_t byte) {
+  uint32_t h = e4m3x2_to_f16x2(byte & 0xFFu);
+  return __half2float(__low2half(*reinterpret_cast<const __half2*>(&h)));
+}
+
+// f16x2 holding values whose f16 mantissa has at most 3 significant bits
+// (every E2M1 and E4M3 value) -> bf16x2 holding value * 2^-112.  Exact:
+// shifting the f16 exponent/mantissa field right by 3 re-biases the
+// exponent from 15 to 127 - 112, and zero stays zero.
+__device__ __forceinline__ uint32_t f16x2_to_bf16x2_scaled_down(uint32_t h) {
+  return ((h >> 3) & 0x0FFF0FFFu) | (h & 0x80008000u);
+}
+
+__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
+  __nv_bfloat162 x = *reinterpret_cast<__nv_bfloat162*>(&a);
+  __nv_bfloat162 y = *reinterpret_cast<__nv_bfloat162*>(&b);
+  __nv_bfloat162 z = __hmul2(x, y);
+  return *reinterpret_cast<uint32_t*>(&z);
+}
+
+// bf16x2 {s * 2^112, s * 2^112} for an E4M3 scale s given as f16 (exact:
+// s has at most 4 significant bits and s * 2^112 < 2^121).
+__device__ __forceinline__ uint32_t scale_multiplier(__half s) {
+  const float f = __half2float(s) * 0x1p112f;
+  const __nv_bfloat16 b = __float2bfloat16_rn(f);
+  const uint32_t u = static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(&b));
+  return u | (u << 16);
+}
+
+// ---------------------------------------------------------------------------
+// row dequantization
+// ---------------------------------------------------------------------------
+// A warp dequantizes one 352-byte row held as 32-bit words: lane l holds
+// w_lo = word l (latent elements 8l..8l+7), w_hi = word l+32 (latent
+// 256+8l..), w_ex = word l+64 for l < 24 (lanes 0..7: scale bytes 4l..4l+3,
+// lanes 8..23: rope bytes 4(l-8)..4(l-8)+3).  Outputs, as bf16:
+//   lat_lo: latent 8l..8l+7, lat_hi: latent 256+8l..256+8l+7,
+//   rope:   rope 4(l-8)..4(l-8)+3 (lanes 8..23 only).
+// Every lane of the warp must call this (it shuffles).
+struct DequantRow {
+  uint4 lat_lo, lat_hi;
+  uint2 rope;
+};
+
+__device__ __forceinline__ DequantRow dequant_row_words(uint32_t w_lo, uint32_t w_hi,
+                                                        uint32_t w_ex, int lane) {
+  // scale byte of latent block lane/2 lives in word lane/8 (lane lane/8), and
+  // that of block 16 + lane/2 in word 4 + lane/8.
+  const uint32_t sw_lo = __shfl_sync(0xFFFFFFFFu, w_ex, lane >> 3);
+  const uint32_t sw_hi = __shfl_sync(0xFFFFFFFFu, w_ex, 4 + (lane >> 3));
+  const uint32_t sh = ((lane >> 1) & 3) * 8;
+  const uint32_t s_pair = ((sw_lo >> sh) & 0xFFu) | (((sw_hi >> sh) & 0xFFu) << 8);
+  uint32_t s_f16x2 = e4m3x2_to_f16x2(s_pair);
+  const __half2 s_h = *reinterpret_cast<const __half2*>(&s_f16x2);
+  const uint32_t m_lo = scale_multiplier(__low2half(s_h));
+  const uint32_t m_hi = scale_multiplier(__high2half(s_h));
+
+  DequantRow r;
+  uint32_t h[4];
+  e2m1x8_to_f16x8(w_lo, h);
+  r.lat_lo.x = bf16x2_mul(f16x2_to_bf16x2_scaled_down(h[0]), m_lo);
+  r.lat_lo.y = bf16x2_mul(f16x2_to_bf16x2_scaled_down(h[1]), m_lo);
+  r.lat_lo.z = bf16x2_mul(f16x2_to_bf16x2_scaled_down(h[2]), m_lo);
+  r.lat_lo.w = bf16x2_mul(f16x2_to_bf16x2_scaled_down(h[3]), m_lo);
+  e2m1x8_to_f16x8(w_hi, h);
+  r.lat_hi.x = bf16x2_mul(f16x2_to_bf16x2_scaled_down(h[0]), m_hi);
+  r.lat_hi.y = bf16x2_mul(f16x2_to_bf16x2_scaled_down(h[1]), m_hi);
+  r.lat_hi.z = bf16x2_mul(f16x2_to_bf16x2_scaled_down(h[2]), m_hi);
+  r.lat_hi.w = bf16x2_mul(f16x2_to_bf16x2_scaled_down(h[3]), m_hi);
+
+  const uint32_t two112 = 0x77807780u;   // bf16x2 {2^112, 2^112}
+  r.rope.x = bf16x2_mul(f16x2_to_bf16x2_scaled_down(e4m3x2_to_f16x2(w_ex & 0xFFFFu)), two112);
+  r.rope.y = bf16x2_mul(f16x2_to_bf16x2_scaled_down(e4m3x2_to_f16x2(w_ex >> 16)), two112);
+  return r;
+}
+
+// ---------------------------------------------------------------------------
+// top-k index -> pool slot (a2)
+// ---------------------------------------------------------------------------
+// Returns the slot of key k of one query, or -1 when masked.  A position
+// outside [0, l_eff) is padding (masked, no error); a page index past the
+// table, a negative page entry or a slot past the pool are masked and
+// flagged.
+__device__ __forceinline__ int32_t resolve_slot(const int32_t* __restrict__ topk_row, int k,
+                                                int K, int64_t l_eff,
+                                                const int32_t* __restrict__ pt_row,
+                                                int64_t pt_stride, int64_t num_slots,
+                                                int32_t* dev_err) {
+  if (k >= K) return -1;
+  const int32_t idx = __ldg(topk_row + k);
+  if (idx < 0 || static_cast<int64_t>(idx) >= l_eff) return -1;
+  const int32_t pi = idx >> 6;
+  if (pi >= pt_stride) {
+    flag_error(dev_err, kDevBadPage);
+    return -1;
+  }
+  const int32_t page = __ldg(pt_row + pi);
+  const int64_t slot = static_cast<int64_t>(page) * kPage + (idx & (kPage - 1));
+  if (page < 0 || slot >= num_slots) {
+    flag_error(dev_err, kDevBadPage);
+    return -1;
+  }
+  return static_cast<int32_t>(slot);
+}
+
+}  // namespace kv4

@@ -1,0 +1,65 @@
+// kv4_launch.h -- internal launch interface between the C ABI (kv4_capi.cu)
+// and the kernels.  Not installed; the public interface is include/kv4mla.h.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace kv4 {
+
+struct QuantizeArgs {
+  const void* latent;
+  int64_t latent_stride;
+  const void* rope;
+  int64_t rope_stride;
+  const int64_t* slots;
+  int64_t n_tokens;
+  uint8_t* pool;
+  int64_t num_slots;
+  int32_t* dev_err;
+};
+
+struct DecodeArgs {
+  const void* q;               // bf16 [B, Sq, H, 576]
+  const uint8_t* pool;
+  int64_t num_slots;
+  const int32_t* page_table;
+  int64_t pt_stride;
+  const int32_t* topk;         // int32 [B, Sq, K]
+  int K;
+  const int32_t* seq_lens;
+  int B, Sq, H;
+  int HG;                      // heads per thread block: 16, 32 or 64
+  int splits;                  // split-K partitions (>= 1)
+  int tiles_per_split;
+  float sm_scale;
+  void* out;                   // bf16 [B, Sq, H, 512]
+  float* lse;                  // fp32 [B, Sq, H]
+  float* ws_o;                 // fp32 [units, splits, HG, 512] when splits > 1
+  float* ws_lse;               // fp32 [units, splits, HG]
+  int32_t* dev_err;
+  uint64_t timeout_ns;
+  int fault_site;
+  cudaEvent_t after_decode;    // recorded between the decode and merge kernels (may be null)
+};
+
+struct GatherArgs {
+  const uint8_t* pool;
+  int64_t num_slots;
+  const int32_t* page_table;
+  int64_t pt_stride;
+  const int32_t* topk;
+  int K;
+  const int32_t* seq_lens;
+  int B, Sq;
+  void* rows;                  // bf16 [B, Sq, K, 576]
+  int32_t* dev_err;
+};
+
+cudaError_t launch_quantize_write(const QuantizeArgs& a, int num_sms, cudaStream_t stream);
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
+cudaError_t launch_debug_gather(const GatherArgs& a, cudaStream_t stream);
+size_t decode_smem_bytes(int HG);
+
+}  // namespace kv4

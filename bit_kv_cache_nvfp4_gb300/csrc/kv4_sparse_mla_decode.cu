@@ -1,0 +1,605 @@
+// kv4_sparse_mla_decode.cu -- sparse MLA decode over the NVFP4 latent KV
+// pool on the 5th-generation tensor core (numinousmuses
+// "inference-optimizations" README: "4-bit KV cache" kv4mla bullet -- the
+// 4-bit rows are dequantized in shared memory instead of an FP8 scratch copy
+// in HBM; "Attention kernels" split-K sparse decode bullet; "Parallelism and
+// disaggregation" (o, lse) merge).
+//
+// Work unit: one thread block per (request b, draft token s, head group g,
+// split).  A head group holds HG = min(H, 64) query heads, which all share
+// every gathered row.  The block walks its share of the top-k list in tiles
+// of 128 keys:
+//   a2/a3  warp 8 resolves the next tile's slots (top-k -> page table);
+//          warps 0..7 gather the 352-byte rows (coalesced 4-byte loads,
+//          16 rows in flight per warp)
+//   a4     and dequantize them straight into the 128-byte-swizzled bf16
+//          operand tile in shared memory (576 columns per key; E2M1 x E4M3
+//          and E4M3 values are exact in bf16)
+//   a5     one thread issues S^T[128 x HG] = K_tile . Q^T on tcgen05
+//          (M = 128 keys, N = HG, K = 576; fp32 accumulator in TMEM)
+//   a6     warps 0..7 read S from TMEM (one key per thread; warps 0..3 take
+//          the first half of the heads, warps 4..7 the second half) and run
+//          the online softmax in base 2; the running maximum is only raised when
+//          a score exceeds it by more than 8 (so most tiles need no cross-
+//          thread reduction and no rescale), p is rounded to bf16 and
+//          written as the PV operand over the tile's rope columns, which
+//          QK^T no longer needs
+//   a7     one thread issues O^T[512 x HG] += V^T . P^T (four M = 128 slabs
+//          of latent columns; V^T is the same shared-memory tile read as an
+//          MN-major operand)
+//   a8     epilogue: O / sum(p) -> bf16 out, lse = ln 2 * (m + log2 sum(p));
+//          with several splits the normalized partial (o, lse) goes to the
+//          workspace and
+//   a9     merge_kernel combines the partials by log-sum-exp.
+// Every mbarrier wait is bounded (KV4_DEV_TIMEOUT on expiry).
+#include "kv4_device.cuh"
+#include "kv4_launch.h"
+
+#include <math.h>
+
+namespace kv4 {
+namespace {
+
+constexpr int kThreads = 288;            // 8 gather/softmax warps + 1 MMA warp
+constexpr int kMmaWarp = 8;
+constexpr float kRaiseThreshold = 8.0f;  // log2 units: p <= 256 between raises
+
+template <int HG>
+struct Layout {
+  static constexpr int HPT = HG / 2;                                  // heads per softmax group
+  static constexpr uint32_t q_bytes = 9u * HG * 128u;                 // Q, 9 slabs
+  static constexpr uint32_t kv_off = (q_bytes + 1023u) & ~1023u;
+  static constexpr uint32_t kv_bytes = 9u * kChunkBytes;              // K/V tile
+  static constexpr uint32_t ctl_off = kv_off + kv_bytes;
+  // control block
+  static constexpr uint32_t bar_off = ctl_off;                        // uint64 x 2
+  static constexpr uint32_t tmem_off = ctl_off + 16;                  // uint32
+  static constexpr uint32_t slot_off = ctl_off + 32;                  // int32 [2][128]
+  static constexpr uint32_t mref_off = slot_off + 2 * 128 * 4;        // float [HG]
+  static constexpr uint32_t alpha_off = mref_off + HG * 4;            // float [HG]
+  static constexpr uint32_t red_off = alpha_off + HG * 4;             // float [2][4][HPT]
+  static constexpr uint32_t lsum_off = red_off + 4 * HG * 4;          // float [2][HG]
+  static constexpr uint32_t end = lsum_off + 2 * HG * 4;
+  static constexpr uint32_t smem_bytes = end + 1024;                  // + alignment slack
+  // tensor memory: O^T slabs at columns [0, 4HG), S^T at [4HG, 5HG)
+  static constexpr uint32_t tmem_cols = (5 * HG <= 128) ? 128 : (5 * HG <= 256 ? 256 : 512);
+  static constexpr uint32_t col_o = 0;
+  static constexpr uint32_t col_s = 4 * HG;
+  // P^T operand (MN-major, N = HG): one swizzle atom per 8 keys
+  static constexpr uint32_t p_row_bytes = 2 * HG;
+  static constexpr uint32_t p_atom_bytes = 8 * p_row_bytes;
+  static constexpr uint32_t p_swizzle_mode =
+      HG == 64 ? kSwizzle128 : (HG == 32 ? kSwizzle64 : kSwizzle32);
+  static constexpr int p_swizzle_bits = HG == 64 ? 3 : (HG == 32 ? 2 : 1);
+};
+
+// Reduce N values per lane across the 32 lanes of a warp by halving: after
+// the call lane l holds max(N/32, 1) results, for heads reduced_head(l, j).
+template <int N, bool IS_MAX>
+__device__ __forceinline__ void warp_transpose_reduce(float (&v)[N], int lane) {
+  int n = N;
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) {
+    if (n > 1) {
+      const int half = n / 2;
+      const bool upper = (lane & off) != 0;
+#pragma unroll
+      for (int i = 0; i < N / 2; ++i) {
+        if (i < half) {
+          const float keep = upper ? v[half + i] : v[i];
+          const float send = upper ? v[i] : v[half + i];
+          const float got = __shfl_xor_sync(0xFFFFFFFFu, send, off);
+          v[i] = IS_MAX ? fmaxf(keep, got) : keep + got;
+        }
+      }
+      n = half;
+    } else {
+      const float got = __shfl_xor_sync(0xFFFFFFFFu, v[0], off);
+      v[0] = IS_MAX ? fmaxf(v[0], got) : v[0] + got;
+    }
+  }
+}
+
+template <int N>
+__device__ __forceinline__ int reduced_head(int lane, int j) {
+  int head = 0, n = N;
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) {
+    if (n > 1) {
+      n /= 2;
+      if (lane & off) head += n;
+    }
+  }
+  return head + j;
+}
+
+// Reduction of N per-thread values over the 128 threads of one softmax
+// group (4 warps, named barrier bar_id); totals land in dst[N] (shared).
+// v is destroyed.
+template <int N, bool IS_MAX>
+__device__ __forceinline__ void group_reduce(float (&v)[N], int quarter, int lane, float* red,
+                                             float* dst, int bar_id) {
+  warp_transpose_reduce<N, IS_MAX>(v, lane);
+  constexpr int kPerLane = N >= 32 ? N / 32 : 1;
+#pragma unroll
+  for (int j = 0; j < kPerLane; ++j) red[quarter * N + reduced_head<N>(lane, j)] = v[j];
+  named_sync(bar_id, 128);
+  const int r = quarter * 32 + lane;
+  if (r < N) {
+    float acc = red[r];
+#pragma unroll
+    for (int w = 1; w < 4; ++w) acc = IS_MAX ? fmaxf(acc, red[w * N + r]) : acc + red[w * N + r];
+    dst[r] = acc;
+  }
+  named_sync(bar_id, 128);
+}
+
+// N consecutive fp32 TMEM columns of this thread's lane.
+template <int N>
+__device__ __forceinline__ void tmem_load_cols(uint32_t taddr, float (&x)[N]) {
+  __syncwarp();                        // tcgen05.ld is warp-collective (.sync.aligned)
+  if constexpr (N == 8) {
+    uint32_t v[8];
+    tmem_ld8_sync(taddr, v);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) x[j] = __uint_as_float(v[j]);
+  } else {
+#pragma unroll
+    for (int c = 0; c < N / 16; ++c) {
+      uint32_t v[16];
+      tmem_ld16_sync(taddr + 16 * c, v);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) x[16 * c + j] = __uint_as_float(v[j]);
+    }
+  }
+}
+
+template <int N>
+__device__ __forceinline__ void tmem_scale_cols(uint32_t taddr, const float* alpha) {
+  __syncwarp();
+  if constexpr (N == 8) {
+    uint32_t v[8];
+    tmem_ld8_sync(taddr, v);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * alpha[j]);
+    tmem_st8(taddr, v);
+  } else {
+#pragma unroll
+    for (int c = 0; c < N / 16; ++c) {
+      uint32_t v[16];
+      tmem_ld16_sync(taddr + 16 * c, v);
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        v[j] = __float_as_uint(__uint_as_float(v[j]) * alpha[16 * c + j]);
+      tmem_st16(taddr + 16 * c, v);
+    }
+  }
+}
+
+template <int HG>
+__global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
+  using L = Layout<HG>;
+  constexpr int HPT = L::HPT;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023u) & ~static_cast<uintptr_t>(1023u));
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int NG = a.H / HG;
+  const int split = blockIdx.x % a.splits;
+  const int unit = blockIdx.x / a.splits;          // (b, s, g)
+  const int g = unit % NG;
+  const int bs = unit / NG;                        // b * Sq + s
+  const int b = bs / a.Sq;
+  const int s = bs % a.Sq;
+  const int64_t l_eff = static_cast<int64_t>(__ldg(a.seq_lens + b)) - (a.Sq - 1 - s);
+  const int32_t* topk_row = a.topk + static_cast<int64_t>(bs) * a.K;
+  const int32_t* pt_row = a.page_table + static_cast<int64_t>(b) * a.pt_stride;
+  const int num_tiles = (a.K + kTileKeys - 1) / kTileKeys;
+  const int tile_begin = split * a.tiles_per_split;
+  const int tile_end = min(num_tiles, tile_begin + a.tiles_per_split);
+  const int my_tiles = max(0, tile_end - tile_begin);
+
+  uint8_t* q_s = smem;
+  uint8_t* kv_s = smem + L::kv_off;
+  const uint32_t bar_mma = smem_addr(smem + L::bar_off);
+  const uint32_t bar_fault = smem_addr(smem + L::bar_off + 8);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::tmem_off);
+  int32_t* slot_s = reinterpret_cast<int32_t*>(smem + L::slot_off);
+  float* m_ref = reinterpret_cast<float*>(smem + L::mref_off);
+  float* alpha_s = reinterpret_cast<float*>(smem + L::alpha_off);
+  float* red_all = reinterpret_cast<float*>(smem + L::red_off);
+  float* lsum = reinterpret_cast<float*>(smem + L::lsum_off);
+
+  // ---- prologue ------------------------------------------------------------
+  if (warp == kMmaWarp) tmem_alloc(smem_addr(tmem_slot), L::tmem_cols);
+  if (tid == 0) {
+    mbar_init(bar_mma, 1);
+    mbar_init(bar_fault, 1);
+    fence_mbar_init();
+  }
+  if (tid < HG) m_ref[tid] = -INFINITY;
+  // Q rows of this head group -> 128-byte-swizzled K-major operand
+  {
+    const uint4* qsrc = reinterpret_cast<const uint4*>(
+        static_cast<const __nv_bfloat16*>(a.q) + (static_cast<int64_t>(bs) * a.H + g * HG) * kQk);
+    for (int i = tid; i < HG * 72; i += kThreads) {
+      const int h = i / 72, gu = i % 72;          // 16-byte unit gu of head h
+      const uint32_t off = (gu >> 3) * (HG * 128) + (h >> 3) * 1024 + (h & 7) * 128 + (gu & 7) * 16;
+      *reinterpret_cast<uint4*>(q_s + swizzle<3>(off)) = __ldg(qsrc + h * 72 + gu);
+    }
+  }
+  // slots of the first tile
+  if (warp == kMmaWarp && my_tiles > 0) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int r = lane + 32 * i;
+      slot_s[r] = resolve_slot(topk_row, tile_begin * kTileKeys + r, a.K, l_eff, pt_row,
+                               a.pt_stride, a.num_slots, a.dev_err);
+    }
+  }
+  fence_async_smem();
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  if (a.fault_site == 1 && warp == kMmaWarp) {
+    // test hook: the MMA warp waits on a barrier that nothing arrives on
+    const bool ok = mbar_wait_bounded(bar_fault, 0, a.timeout_ns);
+    __syncwarp();
+    if (!ok && lane == 0) flag_error(a.dev_err, kDevTimeout);
+  }
+
+  // softmax roles (warps 0..7): group G owns heads [G*HPT, G*HPT + HPT);
+  // thread (quarter, lane) owns key row r = quarter*32 + lane of each tile,
+  // which is TMEM lane r.
+  const int G = warp >> 2;
+  const int quarter = warp & 3;
+  const int r_key = quarter * 32 + lane;
+  const int h0 = G * HPT;
+  const int bar_group = 1 + G;
+  float* red = red_all + G * 4 * HPT;
+  const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+  const float scale = a.sm_scale * 1.4426950408889634f;   // base-2 exponent
+
+  float l_true[HPT], l_bf16[HPT];
+#pragma unroll
+  for (int h = 0; h < HPT; ++h) { l_true[h] = 0.0f; l_bf16[h] = 0.0f; }
+  uint32_t mma_phase = 0;
+  bool timed_out = false;
+
+  const uint32_t kv_addr = smem_addr(kv_s);
+  const uint32_t q_addr = smem_addr(q_s);
+  const uint32_t p_addr = kv_addr + 8 * kChunkBytes;   // over the rope slab
+
+  for (int it = 0; it < my_tiles; ++it) {
+    const int tile = tile_begin + it;
+    const int buf = it & 1;
+    // ---- a3/a4: gather + dequantize the tile into shared memory (warps 0..7)
+    if (warp < 8) {
+      const int32_t* slots = slot_s + buf * 128;
+      uint32_t wlo[16], whi[16], wex[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int32_t sl = slots[warp * 16 + i];
+        if (sl >= 0) {
+          const uint32_t* row =
+              reinterpret_cast<const uint32_t*>(a.pool + static_cast<int64_t>(sl) * kRowBytes);
+          wlo[i] = __ldg(row + lane);
+          whi[i] = __ldg(row + 32 + lane);
+          wex[i] = lane < 24 ? __ldg(row + 64 + lane) : 0u;
+        } else {
+          wlo[i] = whi[i] = wex[i] = 0u;                 // masked key: zero row
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int r = warp * 16 + i;
+        const DequantRow d = dequant_row_words(wlo[i], whi[i], wex[i], lane);
+        const uint32_t rowoff = (r >> 3) * 1024 + (r & 7) * 128;
+        const uint32_t u = (lane & 7) * 16;
+        *reinterpret_cast<uint4*>(kv_s + swizzle<3>((lane >> 3) * kChunkBytes + rowoff + u)) =
+            d.lat_lo;
+        *reinterpret_cast<uint4*>(kv_s + swizzle<3>((4 + (lane >> 3)) * kChunkBytes + rowoff + u)) =
+            d.lat_hi;
+        if (lane >= 8 && lane < 24) {
+          const uint32_t lr = lane - 8;
+          *reinterpret_cast<uint2*>(kv_s + swizzle<3>(8 * kChunkBytes + rowoff + lr * 8)) = d.rope;
+        }
+      }
+    } else if (it + 1 < my_tiles) {
+      // ---- a2: next tile's slots (warp 8) ----
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int r = lane + 32 * i;
+        slot_s[(buf ^ 1) * 128 + r] =
+            resolve_slot(topk_row, (tile + 1) * kTileKeys + r, a.K, l_eff, pt_row, a.pt_stride,
+                         a.num_slots, a.dev_err);
+      }
+    }
+    fence_async_smem();
+    __syncthreads();
+
+    // ---- a5: S^T = K_tile . Q^T ----
+    if (warp == kMmaWarp && lane == 0) {
+      tc_fence_after_sync();
+      constexpr uint32_t idesc = idesc_bf16(128, HG, false, false);
+#pragma unroll
+      for (int kk = 0; kk < 36; ++kk) {
+        const uint32_t c = kk >> 2, sub = kk & 3;
+        const uint64_t ad = smem_desc(kv_addr + c * kChunkBytes + sub * 32, 16, 1024, kSwizzle128);
+        const uint64_t bd = smem_desc(q_addr + c * (HG * 128) + sub * 32, 16, 1024, kSwizzle128);
+        mma_bf16(tmem + L::col_s, ad, bd, idesc, kk > 0 ? 1u : 0u);
+      }
+      mma_commit(bar_mma);
+    }
+
+    // ---- a6: online softmax (warps 0..7, two head groups) ----
+    if (warp < 8) {
+      if (!mbar_wait_bounded(bar_mma, mma_phase, a.timeout_ns)) timed_out = true;
+      __syncwarp();                    // lanes may leave the wait at different times
+      tc_fence_after_sync();
+      const bool valid = slot_s[buf * 128 + r_key] >= 0;
+      float x[HPT];
+      tmem_load_cols<HPT>(lane_base + L::col_s + h0, x);
+      bool need = false;
+#pragma unroll
+      for (int h = 0; h < HPT; ++h) {
+        x[h] = valid ? x[h] * scale : -INFINITY;
+        need |= x[h] > m_ref[h0 + h] + kRaiseThreshold;
+      }
+      need = named_sync_or(bar_group, 128, need);
+      if (need) {
+        // raise the reference maximum to the tile maximum
+        group_reduce<HPT, true>(x, quarter, lane, red, alpha_s + h0, bar_group);
+        if (r_key < HPT) {
+          const float mo = m_ref[h0 + r_key];
+          const float mn = fmaxf(mo, alpha_s[h0 + r_key]);
+          alpha_s[h0 + r_key] = (mo == mn) ? 1.0f : exp2f(mo - mn);
+          m_ref[h0 + r_key] = mn;
+        }
+        named_sync(bar_group, 128);
+#pragma unroll
+        for (int h = 0; h < HPT; ++h) {
+          l_true[h] *= alpha_s[h0 + h];
+          l_bf16[h] *= alpha_s[h0 + h];
+        }
+        if (it > 0) {
+#pragma unroll
+          for (int mb = 0; mb < 4; ++mb)
+            tmem_scale_cols<HPT>(lane_base + L::col_o + mb * HG + h0, alpha_s + h0);
+          tmem_st_wait();
+        }
+        tmem_load_cols<HPT>(lane_base + L::col_s + h0, x);   // scores again
+#pragma unroll
+        for (int h = 0; h < HPT; ++h) x[h] = valid ? x[h] * scale : -INFINITY;
+      }
+      // probabilities -> bf16 P^T row r_key, heads [h0, h0 + HPT)
+      uint32_t packed[HPT / 2];
+#pragma unroll
+      for (int h = 0; h < HPT; h += 2) {
+        const float p0 = valid ? exp2f(x[h] - m_ref[h0 + h]) : 0.0f;
+        const float p1 = valid ? exp2f(x[h + 1] - m_ref[h0 + h + 1]) : 0.0f;
+        const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
+        l_true[h] += p0;
+        l_true[h + 1] += p1;
+        l_bf16[h] += __low2float(pb);
+        l_bf16[h + 1] += __high2float(pb);
+        packed[h / 2] = *reinterpret_cast<const uint32_t*>(&pb);
+      }
+      uint8_t* p_s = kv_s + 8 * kChunkBytes;
+#pragma unroll
+      for (int u = 0; u < HPT / 8; ++u) {
+        const uint32_t off = (r_key >> 3) * L::p_atom_bytes + (r_key & 7) * L::p_row_bytes +
+                             (h0 * 2) + u * 16;
+        *reinterpret_cast<uint4*>(p_s + swizzle<L::p_swizzle_bits>(off)) =
+            make_uint4(packed[4 * u], packed[4 * u + 1], packed[4 * u + 2], packed[4 * u + 3]);
+      }
+      fence_async_smem();
+      tc_fence_before_sync();
+    }
+    mma_phase ^= 1;
+    __syncthreads();
+
+    // ---- a7: O^T += V^T . P^T ----
+    if (warp == kMmaWarp && lane == 0) {
+      tc_fence_after_sync();
+      constexpr uint32_t idesc = idesc_bf16(128, HG, true, true);
+#pragma unroll
+      for (int mb = 0; mb < 4; ++mb) {
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint64_t ad = smem_desc(kv_addr + (2 * mb) * kChunkBytes + (2 * ks) * 1024,
+                                        kChunkBytes, 1024, kSwizzle128);
+          const uint64_t bd = smem_desc(p_addr + (2 * ks) * L::p_atom_bytes, 8192,
+                                        L::p_atom_bytes, L::p_swizzle_mode);
+          mma_bf16(tmem + L::col_o + mb * HG, ad, bd, idesc, (it > 0 || ks > 0) ? 1u : 0u);
+        }
+      }
+      mma_commit(bar_mma);
+    }
+    // the tile buffer is reused next iteration: wait for PV to finish
+    if (!mbar_wait_bounded(bar_mma, mma_phase, a.timeout_ns)) timed_out = true;
+    __syncwarp();
+    mma_phase ^= 1;
+    tc_fence_after_sync();
+  }
+
+  // ---- a8: epilogue (warps 0..7) ----
+  const bool partial = a.splits > 1;
+  const int64_t out_head0 = static_cast<int64_t>(bs) * a.H + g * HG;   // first head row
+  const int64_t part = static_cast<int64_t>(unit) * a.splits + split;
+  if (warp < 8) {
+    group_reduce<HPT, false>(l_true, quarter, lane, red, lsum + h0, bar_group);
+    group_reduce<HPT, false>(l_bf16, quarter, lane, red, lsum + HG + h0, bar_group);
+    if (r_key < HPT) {
+      const int h = h0 + r_key;
+      const float lt = lsum[h];
+      const float lse = (lt > 0.0f) ? (m_ref[h] + log2f(lt)) * 0.69314718055994531f : -INFINITY;
+      if (partial) a.ws_lse[part * HG + h] = lse;
+      else a.lse[out_head0 + h] = lse;
+    }
+#pragma unroll
+    for (int mb = 0; mb < 4; ++mb) {
+      const int d = mb * 128 + r_key;
+      float o[HPT];
+      if (my_tiles > 0) {
+        tmem_load_cols<HPT>(lane_base + L::col_o + mb * HG + h0, o);
+      } else {
+#pragma unroll
+        for (int j = 0; j < HPT; ++j) o[j] = 0.0f;
+      }
+#pragma unroll
+      for (int j = 0; j < HPT; ++j) {
+        const int h = h0 + j;
+        const float den = lsum[HG + h];
+        const float v = den > 0.0f ? o[j] / den : 0.0f;
+        if (partial) a.ws_o[(part * HG + h) * kLatent + d] = v;
+        else static_cast<__nv_bfloat16*>(a.out)[(out_head0 + h) * kLatent + d] = __float2bfloat16_rn(v);
+      }
+    }
+  }
+  if (timed_out) flag_error(a.dev_err, kDevTimeout);
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    __syncwarp();
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, L::tmem_cols);
+  }
+}
+
+// a9: out = sum_i exp(lse_i - lse) o_i, lse = log sum_i exp(lse_i).
+// One warp per (unit, head); lane l covers columns 4l..4l+3 of each 128.
+__global__ void __launch_bounds__(256) merge_kernel(DecodeArgs a, int n_units) {
+  const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  const int HG = a.HG;
+  if (gw >= n_units * HG) return;
+  const int unit = gw / HG, h = gw % HG;
+  const int NG = a.H / HG;
+  const int g = unit % NG, bs = unit / NG;
+  const float* lse_p = a.ws_lse + static_cast<int64_t>(unit) * a.splits * HG + h;
+  float m = -INFINITY;
+  for (int i = 0; i < a.splits; ++i) m = fmaxf(m, lse_p[i * HG]);
+  float4 acc[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+  float wsum = 0.0f;
+  if (m != -INFINITY) {
+    for (int i = 0; i < a.splits; ++i) {
+      const float li = lse_p[i * HG];
+      if (li == -INFINITY) continue;
+      const float w = expf(li - m);
+      wsum += w;
+      const float4* o = reinterpret_cast<const float4*>(
+          a.ws_o + ((static_cast<int64_t>(unit) * a.splits + i) * HG + h) * kLatent);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float4 v = o[j * 32 + lane];
+        acc[j].x += w * v.x; acc[j].y += w * v.y; acc[j].z += w * v.z; acc[j].w += w * v.w;
+      }
+    }
+  }
+  const int64_t row = static_cast<int64_t>(bs) * a.H + g * HG + h;
+  __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + row * kLatent;
+  const float inv = wsum > 0.0f ? 1.0f / wsum : 0.0f;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(acc[j].x * inv, acc[j].y * inv);
+    const __nv_bfloat162 hi = __floats2bfloat162_rn(acc[j].z * inv, acc[j].w * inv);
+    uint2 pk;
+    pk.x = *reinterpret_cast<const uint32_t*>(&lo);
+    pk.y = *reinterpret_cast<const uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(out + j * 128 + lane * 4) = pk;
+  }
+  if (lane == 0) a.lse[row] = (wsum > 0.0f) ? m + logf(wsum) : -INFINITY;
+}
+
+// Debug: the decode's index resolution and dequantization written to HBM.
+// One warp per (b, s, k) row.
+__global__ void __launch_bounds__(256) debug_gather_kernel(GatherArgs a) {
+  const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  const int64_t n = static_cast<int64_t>(a.B) * a.Sq * a.K;
+  if (gw >= n) return;
+  const int k = static_cast<int>(gw % a.K);
+  const int64_t bs = gw / a.K;
+  const int b = static_cast<int>(bs / a.Sq), s = static_cast<int>(bs % a.Sq);
+  const int64_t l_eff = static_cast<int64_t>(__ldg(a.seq_lens + b)) - (a.Sq - 1 - s);
+  int32_t slot = 0;
+  if (lane == 0)
+    slot = resolve_slot(a.topk + bs * a.K, k, a.K, l_eff, a.page_table + static_cast<int64_t>(b) * a.pt_stride,
+                        a.pt_stride, a.num_slots, a.dev_err);
+  slot = __shfl_sync(0xFFFFFFFFu, slot, 0);
+  uint32_t wlo = 0, whi = 0, wex = 0;
+  if (slot >= 0) {
+    const uint32_t* row = reinterpret_cast<const uint32_t*>(a.pool + static_cast<int64_t>(slot) * kRowBytes);
+    wlo = __ldg(row + lane);
+    whi = __ldg(row + 32 + lane);
+    wex = lane < 24 ? __ldg(row + 64 + lane) : 0u;
+  }
+  DequantRow d = dequant_row_words(wlo, whi, wex, lane);
+  if (slot < 0) {
+    d.lat_lo = d.lat_hi = make_uint4(0, 0, 0, 0);
+    d.rope = make_uint2(0, 0);
+  }
+  __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.rows) + gw * kQk;
+  *reinterpret_cast<uint4*>(out + 8 * lane) = d.lat_lo;
+  *reinterpret_cast<uint4*>(out + 256 + 8 * lane) = d.lat_hi;
+  if (lane >= 8 && lane < 24) *reinterpret_cast<uint2*>(out + 512 + 4 * (lane - 8)) = d.rope;
+}
+
+template <int HG>
+cudaError_t launch_decode_hg(const DecodeArgs& a, cudaStream_t stream) {
+  const size_t smem = Layout<HG>::smem_bytes;
+  static bool configured = false;   // per process; attribute is per kernel
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(decode_kernel<HG>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  const int units = a.B * a.Sq * (a.H / HG);
+  decode_kernel<HG><<<units * a.splits, kThreads, smem, stream>>>(a);
+  cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess && a.after_decode != nullptr) e = cudaEventRecord(a.after_decode, stream);
+  if (e != cudaSuccess || a.splits == 1) return e;
+  const int warps = units * HG;
+  merge_kernel<<<(warps + 7) / 8, 256, 0, stream>>>(a, units);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t decode_smem_bytes(int HG) {
+  switch (HG) {
+    case 16: return Layout<16>::smem_bytes;
+    case 32: return Layout<32>::smem_bytes;
+    case 64: return Layout<64>::smem_bytes;
+    default: return 0;
+  }
+}
+
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
+  switch (a.HG) {
+    case 16: return launch_decode_hg<16>(a, stream);
+    case 32: return launch_decode_hg<32>(a, stream);
+    case 64: return launch_decode_hg<64>(a, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_debug_gather(const GatherArgs& a, cudaStream_t stream) {
+  const int64_t rows = static_cast<int64_t>(a.B) * a.Sq * a.K;
+  if (rows <= 0) return cudaSuccess;
+  const int64_t blocks = (rows + 7) / 8;
+  debug_gather_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace kv4

@@ -327,14 +327,35 @@ def compact_pool_plan(w: Workload, query_ids):
     return pt_c, pages, len(pages) * PAGE
 
 
-def compact_pool_tokens(w: Workload, pages):
-    """Tokens that fill the compact pool: (global ids int64, compact slots int64)."""
-    ids, slots = [], []
-    for cp, (b, pi) in enumerate(pages):
-        L = int(w.seq_lens[b])
-        pos = torch.arange(pi * PAGE, min(L, (pi + 1) * PAGE), dtype=torch.int64)
-        ids.append(pos + int(w.token_offset[b]))
-        slots.append(cp * PAGE + pos % PAGE)
+def compact_pool_tokens(w: Workload, pages, query_ids=None):
+    """Tokens that fill the compact pool: (global ids int64, compact slots int64).
+
+    With query_ids, only the positions those queries select (in range) are
+    emitted -- the other rows of the compact pages are never read; without,
+    every token of every touched page is emitted.
+    """
+    page_of = {bp: cp for cp, bp in enumerate(pages)}
+    if query_ids is None:
+        ids, slots = [], []
+        for cp, (b, pi) in enumerate(pages):
+            L = int(w.seq_lens[b])
+            pos = torch.arange(pi * PAGE, min(L, (pi + 1) * PAGE), dtype=torch.int64)
+            ids.append(pos + int(w.token_offset[b]))
+            slots.append(cp * PAGE + pos % PAGE)
+    else:
+        per_b = {}
+        for (b, s) in query_ids:
+            L_eff = int(w.seq_lens[b]) - (w.Sq - 1 - s)
+            idx = w.topk[b, s].to(torch.int64)
+            idx = idx[(idx >= 0) & (idx < L_eff) & (idx // PAGE < w.pt_stride)]
+            per_b.setdefault(b, []).append(idx)
+        ids, slots = [], []
+        for b, lst in per_b.items():
+            pos = torch.unique(torch.cat(lst))
+            cps = torch.tensor([page_of[(b, int(pi))] for pi in (pos // PAGE).tolist()],
+                               dtype=torch.int64)
+            ids.append(pos + int(w.token_offset[b]))
+            slots.append(cps * PAGE + pos % PAGE)
     if not ids:
         return torch.zeros(0, dtype=torch.int64), torch.zeros(0, dtype=torch.int64)
     return torch.cat(ids), torch.cat(slots)

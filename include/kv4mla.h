@@ -1,0 +1,168 @@
+/*
+ * kv4mla.h -- C ABI of libkv4mla.so: NVFP4 latent-KV cache write and
+ * sparse MLA (DSA) decode on GB300 (sm_103a).
+ *
+ * The method (numinousmuses "inference-optimizations" README):
+ *  - "4-bit KV cache", GLM-5.3 bullet: each cached token is one 352-byte
+ *    NVFP4 row -- E2M1 values with one E4M3 scale per 16 values -- that
+ *    replaces the 576-byte FP8 row used by DSA sparse attention.  This
+ *    library fixes the byte order of the row:
+ *        bytes [0,256)   512 latent E2M1 codes, byte j = code(2j) | code(2j+1)<<4
+ *        bytes [256,288) 32 E4M3 scales, scale i covers latent 16i..16i+15
+ *        bytes [288,352) 64 rope values as E4M3 (no scale)
+ *    A row lives at pool + slot*352; slot = page*64 + offset (64-token pages,
+ *    the page size of the sgl-amd-mono sparse-attention page table).
+ *  - "4-bit KV cache", kv4mla bullet: the decode reads the 4-bit rows and
+ *    dequantizes them in shared memory (no FP8 scratch copy in HBM).
+ *  - "Attention kernels", split-K sparse decode bullet, and "Parallelism and
+ *    disaggregation", (o, lse) merge bullet: when the batch is too small to
+ *    fill the GPU the selected set is split and the partial (o, lse) are
+ *    merged by log-sum-exp.
+ *
+ * Conventions for every entry point:
+ *  - Pointers named *_dev are DEVICE pointers of the current CUDA device;
+ *    the caller allocates and owns every buffer (including the workspace).
+ *    The library keeps no pointer after a call returns, never allocates
+ *    device memory and never synchronizes.
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream) and runs asynchronously; outputs are valid once the stream has
+ *    reached that point.
+ *  - Host-detectable argument errors return a nonzero kv4_status and launch
+ *    nothing.  Errors only the device can see (an index or page out of range,
+ *    a bounded wait that gave up) OR a KV4_DEV_* flag into *dev_err (when
+ *    non-NULL); the offending row is skipped / the offending key is masked.
+ *    Read *dev_err after synchronizing.  Nothing traps.
+ *  - bf16 tensors are raw IEEE bfloat16; all sizes are in elements unless
+ *    named *_bytes.
+ */
+#ifndef KV4MLA_H
+#define KV4MLA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* kv4_stream_t;   /* same handle as cudaStream_t */
+
+typedef enum {
+  KV4_OK = 0,
+  KV4_ERR_INVALID_ARG = 1,   /* null pointer, bad size, stride or alignment   */
+  KV4_ERR_UNSUPPORTED = 2,   /* H or page size outside the supported set      */
+  KV4_ERR_ARCH = 3,          /* current device is not compute capability 10.3 */
+  KV4_ERR_LAUNCH = 4,        /* a kernel launch failed (cudaGetLastError)     */
+  KV4_ERR_WORKSPACE = 5      /* workspace missing or smaller than required    */
+} kv4_status;
+
+/* Flags OR-ed into *dev_err by the kernels. */
+enum {
+  KV4_DEV_BAD_SLOT = 1,      /* write: slot >= num_slots; that row skipped     */
+  KV4_DEV_BAD_PAGE = 2,      /* decode: page index >= pt_stride, negative page
+                                entry or slot >= num_slots; that key masked    */
+  KV4_DEV_TIMEOUT = 4        /* a bounded on-chip wait gave up; the outputs of
+                                that thread block are not valid               */
+};
+
+enum {
+  KV4_ROW_BYTES = 352, KV4_LATENT = 512, KV4_ROPE = 64, KV4_QK_DIM = 576,
+  KV4_BLOCK = 16, KV4_PAGE = 64, KV4_TILE_KEYS = 128
+};
+
+/* ---------------------------------------------------------------------------
+ * kv4_quantize_write -- quantize N new tokens into their cache rows.
+ * Source: README "4-bit KV cache" (the quantized write of the NVFP4 row).
+ *   latent_dev        bf16 [N, latent_row_stride]; first 512 used
+ *   rope_dev          bf16 [N, rope_row_stride];   first 64 used
+ *                     (both: base 16-byte aligned, stride a multiple of 8)
+ *   slot_mapping_dev  int64 [N]; slot < 0 skips the token
+ *   pool_dev          uint8 [num_slots, 352], base 16-byte aligned
+ * Per 16-element block: scale byte = E4M3(amax/6) (IEEE fp32 division, round
+ * half to even, saturate at 448); s = decoded scale; code = E2M1(x/s) (fp32
+ * division, round half to even, saturate at 6, sign of x kept); s == 0 gives
+ * all-zero codes.  Rope: E4M3(x).  Bit-identical to the CPU oracle.
+ * ------------------------------------------------------------------------- */
+kv4_status kv4_quantize_write(const void* latent_dev, int64_t latent_row_stride,
+                              const void* rope_dev, int64_t rope_row_stride,
+                              const int64_t* slot_mapping_dev, int64_t n_tokens,
+                              uint8_t* pool_dev, int64_t num_slots,
+                              int32_t* dev_err, kv4_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * kv4_decode_plan -- number of split-K partitions and workspace bytes that
+ * kv4_sparse_mla_decode will use for this shape on the current device.
+ * force_splits > 0 requests that many partitions (clamped to the number of
+ * 128-key tiles); 0 lets the planner fill the SMs.
+ * ------------------------------------------------------------------------- */
+kv4_status kv4_decode_plan(int B, int Sq, int H, int K, int force_splits,
+                           int* splits, size_t* workspace_bytes);
+
+/* ---------------------------------------------------------------------------
+ * kv4_sparse_mla_decode -- sparse MLA decode over the NVFP4 pool.
+ * Source: README "4-bit KV cache" (kv4mla) and "Attention kernels"
+ * (split-K); (o, lse) merge from "Parallelism and disaggregation".
+ *   q_dev          bf16 [B, Sq, H, 576] contiguous (512 latent + 64 rope),
+ *                  16-byte aligned
+ *   pool_dev       uint8 [num_slots, 352] (num_slots < 2^31), 16-byte aligned
+ *   page_table_dev int32 [B, pt_stride]: physical page of each 64-token
+ *                  logical page; page_size must be 64
+ *   topk_idx_dev   int32 [B, Sq, K]: logical token positions; a position
+ *                  outside [0, L_eff) is masked (-1 = padding), with
+ *                  L_eff = seq_lens[b] - (Sq-1-s) (causal within the draft)
+ *   seq_lens_dev   int32 [B]: tokens of request b, including its Sq drafts
+ *   H              16, 32, 64, or a multiple of 64 up to 256
+ *   sm_scale       softmax scale applied to q.k
+ *   out_dev        bf16 [B, Sq, H, 512]: softmax-weighted sum of the latent
+ *                  part of the selected rows (0 if no key is valid)
+ *   lse_dev        fp32 [B, Sq, H]: natural-log log-sum-exp of the scaled
+ *                  scores (-inf if no key is valid)
+ *   workspace_dev  device scratch of at least the bytes kv4_decode_plan
+ *                  returns (may be NULL when that is 0), 16-byte aligned
+ * Duplicated positions count once per occurrence.  Scores use all 576 dims;
+ * the weighted sum uses the 512 latent dims of the same rows.
+ * ------------------------------------------------------------------------- */
+kv4_status kv4_sparse_mla_decode(const void* q_dev, const uint8_t* pool_dev,
+                                 int64_t num_slots, const int32_t* page_table_dev,
+                                 int64_t pt_stride, int page_size,
+                                 const int32_t* topk_idx_dev, int K,
+                                 const int32_t* seq_lens_dev, int B, int Sq, int H,
+                                 float sm_scale, void* out_dev, float* lse_dev,
+                                 void* workspace_dev, size_t workspace_bytes,
+                                 int force_splits, int32_t* dev_err,
+                                 kv4_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * kv4_debug_gather_dequant -- the decode's own index resolution and
+ * dequantization, written out: rows_dev bf16 [B, Sq, K, 576] receives the
+ * dequantized selected rows (all zero for a masked key).  Exists so that the
+ * gather indexing can be checked bit for bit; same argument meaning as
+ * kv4_sparse_mla_decode.
+ * ------------------------------------------------------------------------- */
+kv4_status kv4_debug_gather_dequant(const uint8_t* pool_dev, int64_t num_slots,
+                                    const int32_t* page_table_dev, int64_t pt_stride,
+                                    int page_size, const int32_t* topk_idx_dev, int K,
+                                    const int32_t* seq_lens_dev, int B, int Sq,
+                                    void* rows_dev, int32_t* dev_err,
+                                    kv4_stream_t stream);
+
+/* Test hook: the next kernel launches use this bounded-wait limit (ns) and,
+ * when fault_site != 0, skip one internal mbarrier arrive so that the wait
+ * runs out and KV4_DEV_TIMEOUT is reported.  0, 0 restores the defaults. */
+kv4_status kv4_set_wait_limit(int64_t timeout_ns, int fault_site);
+
+/* Measurement hook: when `cuda_event` (a cudaEvent_t) is non-NULL, every
+ * later kv4_sparse_mla_decode call records it on its stream right after the
+ * decode kernel and before the split-K merge kernel, so that a caller can
+ * time the decode kernel alone with events on the same stream.  NULL turns
+ * it off.  The event must outlive its use. */
+kv4_status kv4_set_timing_event(void* cuda_event);
+
+const char* kv4_status_str(kv4_status status);
+int kv4_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KV4MLA_H */

@@ -1,0 +1,94 @@
+"""Helpers shared by the GPU parity tests: pools built on the device by the
+library, and oracle results for the same seeded inputs on the host."""
+from __future__ import annotations
+
+import functools
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from bit_kv_cache_nvfp4_gb300 import workloads as wl
+
+OUT_ATOL = 2e-2      # max |out_gpu (bf16) - out_oracle (fp32)|
+LSE_ATOL = 1e-3      # max |lse_gpu - lse_oracle|
+
+
+def need_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+
+
+def bits(t: torch.Tensor) -> np.ndarray:
+    """bf16 tensor -> uint16 numpy of its bit patterns (host)."""
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+@functools.lru_cache(maxsize=2)
+def workload(name: str, seed: int = 0) -> wl.Workload:
+    return wl.make_workload(name, seed)
+
+
+_POOLS: dict = {}
+
+
+def gpu_pool(w: wl.Workload) -> torch.Tensor:
+    """The workload's NVFP4 pool, written on the GPU by kv4_quantize_write."""
+    import bit_kv_cache_nvfp4_gb300 as kv
+    key = (w.name, w.seed)
+    if key not in _POOLS:
+        _POOLS.clear()                       # keep one large pool at a time
+        torch.cuda.empty_cache()
+        dev = torch.device("cuda")
+        pool = torch.zeros((w.num_slots, 352), dtype=torch.uint8, device=dev)
+        for lat, rope, slots in wl.iter_pool_chunks(w, chunk=1 << 18, device=dev):
+            kv.quantize_write(lat, rope, slots, pool)
+        torch.cuda.synchronize()
+        _POOLS[key] = pool
+    return _POOLS[key]
+
+
+def device_inputs(w: wl.Workload):
+    dev = torch.device("cuda")
+    q = wl.queries(w, dev)
+    return (q, w.page_table.to(dev), w.topk.to(dev), w.seq_lens.to(dev))
+
+
+def oracle_decode(w: wl.Workload, requests, splits: int = 1):
+    """Oracle (out fp32 [n,Sq,H,512], lse [n,Sq,H]) for the listed requests,
+    computed on a compact pool holding only the rows those requests select."""
+    qids = [(b, s) for b in requests for s in range(w.Sq)]
+    pt_c, pages, ns = wl.compact_pool_plan(w, qids)
+    ids, cslots = wl.compact_pool_tokens(w, pages, qids)
+    pool = np.zeros((max(ns, 64), 352), dtype=np.uint8)
+    if ids.numel():
+        lat, rope = wl.token_rows(w, ids)
+        assert oracle.quantize_write(bits(lat), bits(rope), cslots.numpy(), pool) == oracle.OK
+    q = bits(wl.queries(w))
+    outs, lses = [], []
+    for b in requests:
+        st, out, lse = oracle.sparse_mla_decode(
+            np.ascontiguousarray(q[b:b + 1]), pool, np.ascontiguousarray(pt_c[b:b + 1].numpy()),
+            np.ascontiguousarray(w.topk[b:b + 1].numpy()),
+            np.ascontiguousarray(w.seq_lens[b:b + 1].numpy()), w.sm_scale, splits=splits)
+        assert st == oracle.OK
+        outs.append(out[0])
+        lses.append(lse[0])
+    return np.stack(outs), np.stack(lses)
+
+
+def assert_close(out_gpu: torch.Tensor, lse_gpu: torch.Tensor, out_ref: np.ndarray,
+                 lse_ref: np.ndarray, what: str = ""):
+    o = out_gpu.float().cpu().numpy()
+    l = lse_gpu.float().cpu().numpy()
+    assert o.shape == out_ref.shape and l.shape == lse_ref.shape
+    both_inf = np.isneginf(l) & np.isneginf(lse_ref)
+    assert np.array_equal(np.isneginf(l), np.isneginf(lse_ref)), f"{what}: -inf lse pattern differs"
+    err_o = np.abs(o - out_ref)
+    err_l = np.where(both_inf, 0.0, np.abs(l - lse_ref))
+    assert np.isfinite(o).all(), f"{what}: non-finite output"
+    mo, ml = float(err_o.max()), float(err_l.max())
+    assert mo <= OUT_ATOL, f"{what}: max |out err| {mo:.4g} > {OUT_ATOL}"
+    assert ml <= LSE_ATOL, f"{what}: max |lse err| {ml:.4g} > {LSE_ATOL}"
+    return mo, ml

@@ -1,0 +1,80 @@
+"""The C-ABI library without a GPU: it loads, exports every function that
+include/kv4mla.h declares, and rejects bad arguments on the host before any
+device call.  Also checks the oracle library's exports."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared(header):
+    text = open(header).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kv4(?:ref)?_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from bit_kv_cache_nvfp4_gb300 import build
+    return ctypes.CDLL(build.build())
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared(os.path.join(ROOT, "include", "kv4mla.h"))
+    assert "kv4_sparse_mla_decode" in names and "kv4_quantize_write" in names
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_oracle_exports_every_declared_symbol():
+    import oracle
+    olib = ctypes.CDLL(oracle.build())
+    names = declared(os.path.join(ROOT, "oracle", "kv4ref.h"))
+    assert not [n for n in names if not hasattr(olib, n)]
+
+
+def test_status_strings_and_version(lib):
+    lib.kv4_status_str.restype = ctypes.c_char_p
+    assert lib.kv4_status_str(0) == b"ok"
+    assert b"workspace" in lib.kv4_status_str(5)
+    assert lib.kv4_version() >= 1
+
+
+def test_host_side_validation_needs_no_device(lib):
+    P, i64 = ctypes.c_void_p, ctypes.c_int64
+    lib.kv4_quantize_write.argtypes = [P, i64, P, i64, P, i64, P, i64, P, P]
+    assert lib.kv4_quantize_write(None, 512, None, 64, None, -1, None, 10, None, None) == 1
+    assert lib.kv4_quantize_write(None, 512, None, 64, None, 0, None, 10, None, None) == 0
+    # 16 tokens with null pointers
+    assert lib.kv4_quantize_write(None, 512, None, 64, None, 16, None, 10, None, None) == 1
+    s, ws = ctypes.c_int(), ctypes.c_size_t()
+    lib.kv4_decode_plan.argtypes = [ctypes.c_int] * 5 + [ctypes.POINTER(ctypes.c_int),
+                                                         ctypes.POINTER(ctypes.c_size_t)]
+    assert lib.kv4_decode_plan(1, 1, 48, 128, 0, ctypes.byref(s), ctypes.byref(ws)) == 2
+    assert lib.kv4_decode_plan(1, 0, 64, 128, 0, ctypes.byref(s), ctypes.byref(ws)) == 1
+    lib.kv4_set_wait_limit.argtypes = [i64, ctypes.c_int]
+    assert lib.kv4_set_wait_limit(-1, 0) == 1
+    assert lib.kv4_set_wait_limit(0, 5) == 1
+    assert lib.kv4_set_wait_limit(0, 0) == 0
+    f = ctypes.c_float
+    lib.kv4_sparse_mla_decode.argtypes = [P, P, i64, P, i64, ctypes.c_int, P, ctypes.c_int, P,
+                                          ctypes.c_int, ctypes.c_int, ctypes.c_int, f, P, P, P,
+                                          ctypes.c_size_t, ctypes.c_int, P, P]
+    # page size other than 64
+    assert lib.kv4_sparse_mla_decode(None, None, 64, None, 1, 32, None, 8, None, 1, 1, 16, 0.1,
+                                     None, None, None, 0, 0, None, None) == 2
+    # empty batch is a no-op
+    assert lib.kv4_sparse_mla_decode(None, None, 64, None, 1, 64, None, 8, None, 0, 1, 16, 0.1,
+                                     None, None, None, 0, 0, None, None) == 0
+
+
+def test_binding_fails_loudly_without_cuda_tensors():
+    import torch
+    import bit_kv_cache_nvfp4_gb300 as kv
+    with pytest.raises(TypeError):
+        kv.quantize_write(torch.zeros(1, 512, dtype=torch.bfloat16),
+                          torch.zeros(1, 64, dtype=torch.bfloat16),
+                          torch.zeros(1, dtype=torch.int64), torch.zeros(64, 352, dtype=torch.uint8))

@@ -243,3 +243,12 @@ def test_compact_pool_equals_full_pool():
     st, out_c, lse_c = oracle.sparse_mla_decode(q, pool_c, pt_c.numpy(), w.topk.numpy(),
                                                 w.seq_lens.numpy(), w.sm_scale)
     assert np.array_equal(out_full, out_c) and np.array_equal(lse_full, lse_c)
+    # only the selected rows of the compact pages (the form used at full size)
+    ids, cslots = wl.compact_pool_tokens(w, pages, [(0, 0)])
+    assert ids.numel() == int(((w.topk >= 0) & (w.topk < int(w.seq_lens[0]))).sum())
+    lat_s, rope_s = wl.token_rows(w, ids)
+    pool_s = np.zeros((ns, 352), dtype=np.uint8)
+    assert oracle.quantize_write(to_bits(lat_s), to_bits(rope_s), cslots.numpy(), pool_s) == 0
+    st, out_s, lse_s = oracle.sparse_mla_decode(q, pool_s, pt_c.numpy(), w.topk.numpy(),
+                                                w.seq_lens.numpy(), w.sm_scale)
+    assert np.array_equal(out_full, out_s) and np.array_equal(lse_full, lse_s)
