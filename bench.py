@@ -91,55 +91,98 @@ def ncu_traffic_bytes():
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle sampling during the timed region."""
+    """SM clock and throttle reasons sampled every few ms during the timed
+    region, read through NVML (libnvidia-ml, read-only queries) in a
+    background thread; nvidia-smi is the fallback."""
 
-    def __init__(self, index: int):
-        self.index = index
-        self.proc = None
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, device_index: int, period_s: float = 0.002):
+        self.index = device_index
+        self.period = period_s
+        self.samples = []        # (sm_mhz, max_mhz, reasons bitmask)
+        self._stop = None
+        self._thread = None
+        self._nvml = None
+        self._handle = None
+
+    def _open_nvml(self):
+        import ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        handle = ctypes.c_void_p()
+        bus = None
+        try:
+            props = torch.cuda.get_device_properties(self.index)
+            bus = f"{props.pci_domain_id:08x}:{props.pci_bus_id:02x}:{props.pci_device_id:02x}.0"
+        except Exception:
+            bus = None
+        if bus is None or lib.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(handle)):
+            if lib.nvmlDeviceGetHandleByIndex_v2(self.index, ctypes.byref(handle)) != 0:
+                raise RuntimeError("no NVML handle")
+        self._nvml, self._handle = lib, handle
+
+    def _poll(self):
+        import ctypes
+        lib, h = self._nvml, self._handle
+        clk, mx, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            ok = (lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0 and
+                  lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0)
+            if lib.nvmlDeviceGetCurrentClocksThrottleReasons(h, ctypes.byref(rs)) != 0:
+                rs.value = 0
+            if ok:
+                self.samples.append((clk.value, mx.value, rs.value))
+            time.sleep(self.period)
 
     def __enter__(self):
-        q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        import threading
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={q}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._open_nvml()
+            self._stop = threading.Event()
+            self._thread = threading.Thread(target=self._poll, daemon=True)
+            self._thread.start()
         except Exception:
-            self.proc = None
+            self._thread = None
         return self
 
     def __exit__(self, *exc):
-        self.lines = []
-        if self.proc is not None:
-            self.proc.terminate()
-            try:
-                out, _ = self.proc.communicate(timeout=5)
-            except Exception:
-                self.proc.kill()
-                out = ""
-            self.lines = [l for l in out.splitlines() if l.strip()]
+        if self._thread is not None:
+            self._stop.set()
+            self._thread.join(timeout=5)
+        if not self.samples:
+            self._nvidia_smi_once()
+
+    def _nvidia_smi_once(self):
+        q = ("clocks.sm,clocks.max.sm,clocks_event_reasons.sw_power_cap,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+             "clocks_event_reasons.hw_thermal_slowdown")
+        try:
+            out = subprocess.run(["nvidia-smi", "-i", str(self.index), f"--query-gpu={q}",
+                                  "--format=csv,noheader,nounits"], capture_output=True,
+                                 text=True, timeout=20).stdout
+            p = [x.strip() for x in out.strip().split(",")]
+            bits = 0
+            for flag, val in zip((0x4, 0x8, 0x20, 0x40), p[2:6]):
+                if val.lower() == "active":
+                    bits |= flag
+            self.samples.append((float(p[0]), float(p[1]), bits))
+            self.source = "nvidia-smi (after the timed region)"
+        except Exception:
+            pass
 
     def summary(self):
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in getattr(self, "lines", []):
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 8:
-                continue
-            try:
-                sm.append(float(parts[0]))
-                mx.append(float(parts[1]))
-            except ValueError:
-                continue
-            for name, val in zip(names, parts[4:8]):
-                if val.lower() == "active":
-                    reasons.add(name)
-        if not sm:
+        if not self.samples:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
-                "reasons": sorted(reasons), "samples": len(sm)}
+        sm = [s[0] for s in self.samples]
+        bits = 0
+        for s in self.samples:
+            bits |= s[2]
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(s[1] for s in self.samples),
+                "sm_mhz_min": min(sm), "reasons": [n for b, n in self.REASONS.items() if bits & b],
+                "samples": len(sm), "source": getattr(self, "source", "nvml")}
 
 
 def dist_env():
@@ -298,6 +341,8 @@ def run_gpu(args):
     e1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     d0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     d1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    for e in d1:                 # create the events the library will record
+        e.record(stream)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)

@@ -186,15 +186,15 @@ def sparse_mla_decode(q: torch.Tensor, pool: torch.Tensor, page_table: torch.Ten
 
 def debug_gather_dequant(pool: torch.Tensor, page_table: torch.Tensor, topk_idx: torch.Tensor,
                          seq_lens: torch.Tensor, dev_err: torch.Tensor | None = None):
-    """The decode's gather + dequantization: bf16 [B,Sq,K,576] (masked rows 0)."""
+    """The decode's gather + dequantization: f16 [B,Sq,K,576] (masked rows 0)."""
     lib = load_library()
     B, Sq, K = topk_idx.shape
-    rows = torch.empty((B, Sq, K, QK_DIM), dtype=torch.bfloat16, device=pool.device)
+    rows = torch.empty((B, Sq, K, QK_DIM), dtype=torch.float16, device=pool.device)
     _check("kv4_debug_gather_dequant", lib.kv4_debug_gather_dequant(
         _dev(pool, "pool", torch.uint8), pool.shape[0],
         _dev(page_table, "page_table", torch.int32), page_table.shape[1], PAGE,
         _dev(topk_idx, "topk_idx", torch.int32), K, _dev(seq_lens, "seq_lens", torch.int32),
-        B, Sq, _dev(rows, "rows", torch.bfloat16), _err_ptr(dev_err), _stream(pool.device)))
+        B, Sq, _dev(rows, "rows", torch.float16), _err_ptr(dev_err), _stream(pool.device)))
     return rows
 
 

@@ -48,14 +48,19 @@ int heads_per_block(int H) {
   return 0;
 }
 
+constexpr double kBlockFixedTiles = 2.0;
+
 struct Plan {
   int HG, units, tiles, splits, tiles_per_split;
   size_t ws_bytes;
 };
 
 // Split-K planner: pick the number of partitions S of each query's tiles
-// that minimizes (waves of thread blocks) x (tiles per partition), plus a
-// half-tile charge for the merge when S > 1; ties go to the smaller S.
+// that minimizes (waves of thread blocks) x (fixed cost of a block + tiles
+// per partition), plus a half-tile charge for the merge when S > 1; ties go
+// to the smaller S.  One block runs per SM.  The fixed cost (prologue: Q
+// load and conversion, first dependent loads; epilogue: output or partial
+// writes) is about two tiles of work.
 Plan make_plan(int B, int Sq, int H, int K, int force_splits, int sms) {
   Plan p{};
   p.HG = heads_per_block(H);
@@ -70,7 +75,8 @@ Plan make_plan(int B, int Sq, int H, int K, int force_splits, int sms) {
       for (int c = 1; c <= p.tiles; ++c) {
         const long long waves = (static_cast<long long>(p.units) * c + sms - 1) / sms;
         const int per = (p.tiles + c - 1) / c;
-        const double cost = static_cast<double>(waves) * per + (c > 1 ? 0.5 : 0.0);
+        const double cost = static_cast<double>(waves) * (kBlockFixedTiles + per) +
+                            (c > 1 ? 0.5 : 0.0);
         if (cost < best - 1e-9) { best = cost; S = c; }
       }
     }
@@ -142,8 +148,8 @@ kv4_status kv4_sparse_mla_decode(const void* q_dev, const uint8_t* pool_dev, int
   if (shape != KV4_OK) return shape;
   if (page_size != KV4_PAGE) return KV4_ERR_UNSUPPORTED;
   if (B == 0) return KV4_OK;
-  if (!q_dev || !pool_dev || !page_table_dev || !topk_idx_dev || !seq_lens_dev || !out_dev ||
-      !lse_dev)
+  if (!q_dev || !pool_dev || !page_table_dev || (K > 0 && !topk_idx_dev) || !seq_lens_dev ||
+      !out_dev || !lse_dev)
     return KV4_ERR_INVALID_ARG;
   if (num_slots < 0 || num_slots > INT32_MAX || pt_stride < 1 || pt_stride > INT32_MAX)
     return KV4_ERR_INVALID_ARG;

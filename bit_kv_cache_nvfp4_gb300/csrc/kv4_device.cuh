@@ -53,6 +53,15 @@ __device__ __forceinline__ uint32_t swizzle(uint32_t off) {
   return off ^ (((off >> 7) & ((1u << B) - 1u)) << 4);
 }
 
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ void st_shared_v2(uint32_t addr, uint2 v) {
+  asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(addr), "r"(v.x), "r"(v.y) : "memory");
+}
+
 // ---------------------------------------------------------------------------
 // mbarrier
 // ---------------------------------------------------------------------------
@@ -197,6 +206,38 @@ __device__ __forceinline__ void tmem_ld8_sync(uint32_t taddr, uint32_t (&r)[8]) 
                : "memory");
 }
 
+// Two 32-column loads (e.g. two partial accumulators) and one wait.
+__device__ __forceinline__ void tmem_ld32x2_sync(uint32_t ta, uint32_t tb, uint32_t (&a)[32],
+                                                 uint32_t (&b)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%64];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, "
+      "%48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%65];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3]), "=r"(a[4]), "=r"(a[5]), "=r"(a[6]),
+        "=r"(a[7]), "=r"(a[8]), "=r"(a[9]), "=r"(a[10]), "=r"(a[11]), "=r"(a[12]), "=r"(a[13]),
+        "=r"(a[14]), "=r"(a[15]), "=r"(a[16]), "=r"(a[17]), "=r"(a[18]), "=r"(a[19]),
+        "=r"(a[20]), "=r"(a[21]), "=r"(a[22]), "=r"(a[23]), "=r"(a[24]), "=r"(a[25]),
+        "=r"(a[26]), "=r"(a[27]), "=r"(a[28]), "=r"(a[29]), "=r"(a[30]), "=r"(a[31]),
+        "=r"(b[0]), "=r"(b[1]), "=r"(b[2]), "=r"(b[3]), "=r"(b[4]), "=r"(b[5]), "=r"(b[6]),
+        "=r"(b[7]), "=r"(b[8]), "=r"(b[9]), "=r"(b[10]), "=r"(b[11]), "=r"(b[12]), "=r"(b[13]),
+        "=r"(b[14]), "=r"(b[15]), "=r"(b[16]), "=r"(b[17]), "=r"(b[18]), "=r"(b[19]),
+        "=r"(b[20]), "=r"(b[21]), "=r"(b[22]), "=r"(b[23]), "=r"(b[24]), "=r"(b[25]),
+        "=r"(b[26]), "=r"(b[27]), "=r"(b[28]), "=r"(b[29]), "=r"(b[30]), "=r"(b[31])
+      : "r"(ta), "r"(tb)
+      : "memory");
+}
+
+// 2^x (MUFU, about 2 ulp; flushes results below 2^-126 to zero).
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -227,15 +268,24 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes
   return d;
 }
 
-// Instruction descriptor: D fp32, A and B bf16, dense, no negation.
+// Instruction descriptor for kind::f16: D fp32, A and B both f16 (format 0)
+// or both bf16 (format 1), dense, no negation.
+__host__ __device__ constexpr uint32_t idesc_f16kind(int M, int N, bool a_mn_major,
+                                                     bool b_mn_major, bool bf16) {
+  return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) |
+         ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
+         (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major,
                                                   bool b_mn_major) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn_major ? 1u : 0u) << 15) |
-         ((b_mn_major ? 1u : 0u) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
-         (static_cast<uint32_t>(M >> 4) << 24);
+  return idesc_f16kind(M, N, a_mn_major, b_mn_major, true);
+}
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool a_mn_major,
+                                                 bool b_mn_major) {
+  return idesc_f16kind(M, N, a_mn_major, b_mn_major, false);
 }
 
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+__device__ __forceinline__ void mma_f16kind(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                          uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
@@ -280,37 +330,22 @@ __device__ __forceinline__ float e4m3_to_float(uint32_t byte) {
   return __half2float(__low2half(*reinterpret_cast<const __half2*>(&h)));
 }
 
-// f16x2 holding values whose f16 mantissa has at most 3 significant bits
-// (every E2M1 and E4M3 value) -> bf16x2 holding value * 2^-112.  Exact:
-// shifting the f16 exponent/mantissa field right by 3 re-biases the
-// exponent from 15 to 127 - 112, and zero stays zero.
-__device__ __forceinline__ uint32_t f16x2_to_bf16x2_scaled_down(uint32_t h) {
-  return ((h >> 3) & 0x0FFF0FFFu) | (h & 0x80008000u);
-}
-
-__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
-  __nv_bfloat162 x = *reinterpret_cast<__nv_bfloat162*>(&a);
-  __nv_bfloat162 y = *reinterpret_cast<__nv_bfloat162*>(&b);
-  __nv_bfloat162 z = __hmul2(x, y);
+__device__ __forceinline__ uint32_t f16x2_mul(uint32_t a, uint32_t b) {
+  __half2 x = *reinterpret_cast<__half2*>(&a);
+  __half2 y = *reinterpret_cast<__half2*>(&b);
+  __half2 z = __hmul2(x, y);
   return *reinterpret_cast<uint32_t*>(&z);
 }
 
-// bf16x2 {s * 2^112, s * 2^112} for an E4M3 scale s given as f16 (exact:
-// s has at most 4 significant bits and s * 2^112 < 2^121).
-__device__ __forceinline__ uint32_t scale_multiplier(__half s) {
-  const float f = __half2float(s) * 0x1p112f;
-  const __nv_bfloat16 b = __float2bfloat16_rn(f);
-  const uint32_t u = static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(&b));
-  return u | (u << 16);
-}
-
 // ---------------------------------------------------------------------------
-// row dequantization
+// row dequantization (to f16: every E2M1 x E4M3 product and every E4M3
+// value is exact in f16 -- at most 6 significant bits, magnitudes in
+// [2^-10, 2688] -- so the tensor-core operand equals the decoded value)
 // ---------------------------------------------------------------------------
 // A warp dequantizes one 352-byte row held as 32-bit words: lane l holds
 // w_lo = word l (latent elements 8l..8l+7), w_hi = word l+32 (latent
 // 256+8l..), w_ex = word l+64 for l < 24 (lanes 0..7: scale bytes 4l..4l+3,
-// lanes 8..23: rope bytes 4(l-8)..4(l-8)+3).  Outputs, as bf16:
+// lanes 8..23: rope bytes 4(l-8)..4(l-8)+3).  Outputs, as f16:
 //   lat_lo: latent 8l..8l+7, lat_hi: latent 256+8l..256+8l+7,
 //   rope:   rope 4(l-8)..4(l-8)+3 (lanes 8..23 only).
 // Every lane of the warp must call this (it shuffles).
@@ -319,45 +354,80 @@ struct DequantRow {
   uint2 rope;
 };
 
+// Per-lane constant for dequant_row_words: the byte selector that picks this
+// lane's two scale bytes out of the two shuffled scale words.
+__device__ __forceinline__ uint32_t dequant_scale_selector(int lane) {
+  const uint32_t b = (lane >> 1) & 3;                     // byte within each word
+  return b | ((4 + b) << 4);                              // {lo word byte b, hi word byte b}
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+  return r;
+}
+
 __device__ __forceinline__ DequantRow dequant_row_words(uint32_t w_lo, uint32_t w_hi,
-                                                        uint32_t w_ex, int lane) {
+                                                        uint32_t w_ex, int lane,
+                                                        uint32_t scale_sel) {
   // scale byte of latent block lane/2 lives in word lane/8 (lane lane/8), and
   // that of block 16 + lane/2 in word 4 + lane/8.
   const uint32_t sw_lo = __shfl_sync(0xFFFFFFFFu, w_ex, lane >> 3);
   const uint32_t sw_hi = __shfl_sync(0xFFFFFFFFu, w_ex, 4 + (lane >> 3));
-  const uint32_t sh = ((lane >> 1) & 3) * 8;
-  const uint32_t s_pair = ((sw_lo >> sh) & 0xFFu) | (((sw_hi >> sh) & 0xFFu) << 8);
-  uint32_t s_f16x2 = e4m3x2_to_f16x2(s_pair);
-  const __half2 s_h = *reinterpret_cast<const __half2*>(&s_f16x2);
-  const uint32_t m_lo = scale_multiplier(__low2half(s_h));
-  const uint32_t m_hi = scale_multiplier(__high2half(s_h));
+  const uint32_t s_pair = prmt(sw_lo, sw_hi, scale_sel);  // {s_lo byte, s_hi byte}
+  const uint32_t s2 = e4m3x2_to_f16x2(s_pair);            // {s_lo, s_hi} as f16
+  const uint32_t m_lo = (s2 & 0xFFFFu) * 0x00010001u;     // {s_lo, s_lo}
+  const uint32_t m_hi = (s2 >> 16) * 0x00010001u;         // {s_hi, s_hi}
 
   DequantRow r;
   uint32_t h[4];
   e2m1x8_to_f16x8(w_lo, h);
-  r.lat_lo.x = bf16x2_mul(f16x2_to_bf16x2_scaled_down(h[0]), m_lo);
-  r.lat_lo.y = bf16x2_mul(f16x2_to_bf16x2_scaled_down(h[1]), m_lo);
-  r.lat_lo.z = bf16x2_mul(f16x2_to_bf16x2_scaled_down(h[2]), m_lo);
-  r.lat_lo.w = bf16x2_mul(f16x2_to_bf16x2_scaled_down(h[3]), m_lo);
+  r.lat_lo.x = f16x2_mul(h[0], m_lo);
+  r.lat_lo.y = f16x2_mul(h[1], m_lo);
+  r.lat_lo.z = f16x2_mul(h[2], m_lo);
+  r.lat_lo.w = f16x2_mul(h[3], m_lo);
   e2m1x8_to_f16x8(w_hi, h);
-  r.lat_hi.x = bf16x2_mul(f16x2_to_bf16x2_scaled_down(h[0]), m_hi);
-  r.lat_hi.y = bf16x2_mul(f16x2_to_bf16x2_scaled_down(h[1]), m_hi);
-  r.lat_hi.z = bf16x2_mul(f16x2_to_bf16x2_scaled_down(h[2]), m_hi);
-  r.lat_hi.w = bf16x2_mul(f16x2_to_bf16x2_scaled_down(h[3]), m_hi);
-
-  const uint32_t two112 = 0x77807780u;   // bf16x2 {2^112, 2^112}
-  r.rope.x = bf16x2_mul(f16x2_to_bf16x2_scaled_down(e4m3x2_to_f16x2(w_ex & 0xFFFFu)), two112);
-  r.rope.y = bf16x2_mul(f16x2_to_bf16x2_scaled_down(e4m3x2_to_f16x2(w_ex >> 16)), two112);
+  r.lat_hi.x = f16x2_mul(h[0], m_hi);
+  r.lat_hi.y = f16x2_mul(h[1], m_hi);
+  r.lat_hi.z = f16x2_mul(h[2], m_hi);
+  r.lat_hi.w = f16x2_mul(h[3], m_hi);
+  r.rope.x = e4m3x2_to_f16x2(w_ex & 0xFFFFu);
+  r.rope.y = e4m3x2_to_f16x2(w_ex >> 16);
   return r;
 }
 
 // ---------------------------------------------------------------------------
 // top-k index -> pool slot (a2)
 // ---------------------------------------------------------------------------
-// Returns the slot of key k of one query, or -1 when masked.  A position
-// outside [0, l_eff) is padding (masked, no error); a page index past the
-// table, a negative page entry or a slot past the pool are masked and
-// flagged.
+// Resolution runs in two stages so that a caller can overlap each dependent
+// load with other work:
+//   stage 1: top-k position -> page-table index, or -1 when the position is
+//            padding (outside [0, l_eff): masked, no error) or the page index
+//            is past the table (masked, flagged);
+//   stage 2: page-table entry -> slot, or -1 when the entry is negative or the
+//            slot is past the pool (masked, flagged).
+__device__ __forceinline__ int32_t slot_page_index(int32_t idx, int64_t l_eff, int64_t pt_stride,
+                                                   int32_t* dev_err) {
+  if (idx < 0 || static_cast<int64_t>(idx) >= l_eff) return -1;
+  const int32_t pi = idx >> 6;
+  if (pi >= pt_stride) {
+    flag_error(dev_err, kDevBadPage);
+    return -1;
+  }
+  return pi;
+}
+
+__device__ __forceinline__ int32_t slot_from_page(int32_t page, int32_t idx, int64_t num_slots,
+                                                  int32_t* dev_err) {
+  const int64_t slot = static_cast<int64_t>(page) * kPage + (idx & (kPage - 1));
+  if (page < 0 || slot >= num_slots) {
+    flag_error(dev_err, kDevBadPage);
+    return -1;
+  }
+  return static_cast<int32_t>(slot);
+}
+
+// Both stages at once: the slot of key k of one query, or -1 when masked.
 __device__ __forceinline__ int32_t resolve_slot(const int32_t* __restrict__ topk_row, int k,
                                                 int K, int64_t l_eff,
                                                 const int32_t* __restrict__ pt_row,
@@ -365,19 +435,9 @@ __device__ __forceinline__ int32_t resolve_slot(const int32_t* __restrict__ topk
                                                 int32_t* dev_err) {
   if (k >= K) return -1;
   const int32_t idx = __ldg(topk_row + k);
-  if (idx < 0 || static_cast<int64_t>(idx) >= l_eff) return -1;
-  const int32_t pi = idx >> 6;
-  if (pi >= pt_stride) {
-    flag_error(dev_err, kDevBadPage);
-    return -1;
-  }
-  const int32_t page = __ldg(pt_row + pi);
-  const int64_t slot = static_cast<int64_t>(page) * kPage + (idx & (kPage - 1));
-  if (page < 0 || slot >= num_slots) {
-    flag_error(dev_err, kDevBadPage);
-    return -1;
-  }
-  return static_cast<int32_t>(slot);
+  const int32_t pi = slot_page_index(idx, l_eff, pt_stride, dev_err);
+  if (pi < 0) return -1;
+  return slot_from_page(__ldg(pt_row + pi), idx, num_slots, dev_err);
 }
 
 }  // namespace kv4

@@ -53,7 +53,7 @@ struct GatherArgs {
   int K;
   const int32_t* seq_lens;
   int B, Sq;
-  void* rows;                  // bf16 [B, Sq, K, 576]
+  void* rows;                  // f16 [B, Sq, K, 576]
   int32_t* dev_err;
 };
 

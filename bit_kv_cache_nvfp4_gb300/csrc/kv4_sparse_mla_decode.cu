@@ -12,16 +12,17 @@
 //   a2/a3  warp 8 resolves the next tile's slots (top-k -> page table);
 //          warps 0..7 gather the 352-byte rows (coalesced 4-byte loads,
 //          16 rows in flight per warp)
-//   a4     and dequantize them straight into the 128-byte-swizzled bf16
+//   a4     and dequantize them straight into the 128-byte-swizzled f16
 //          operand tile in shared memory (576 columns per key; E2M1 x E4M3
-//          and E4M3 values are exact in bf16)
+//          and E4M3 values are exact in f16); q is converted to f16 with a
+//          per-head power-of-two scale folded into the score scale
 //   a5     one thread issues S^T[128 x HG] = K_tile . Q^T on tcgen05
 //          (M = 128 keys, N = HG, K = 576; fp32 accumulator in TMEM)
 //   a6     warps 0..7 read S from TMEM (one key per thread; warps 0..3 take
 //          the first half of the heads, warps 4..7 the second half) and run
 //          the online softmax in base 2; the running maximum is only raised when
 //          a score exceeds it by more than 8 (so most tiles need no cross-
-//          thread reduction and no rescale), p is rounded to bf16 and
+//          thread reduction and no rescale), p is rounded to f16 and
 //          written as the PV operand over the tile's rope columns, which
 //          QK^T no longer needs
 //   a7     one thread issues O^T[512 x HG] += V^T . P^T (four M = 128 slabs
@@ -40,8 +41,7 @@
 namespace kv4 {
 namespace {
 
-constexpr int kThreads = 288;            // 8 gather/softmax warps + 1 MMA warp
-constexpr int kMmaWarp = 8;
+constexpr int kThreads = 256;            // 8 warps: gather, dequant, softmax; thread 0 issues MMAs
 constexpr float kRaiseThreshold = 8.0f;  // log2 units: p <= 256 between raises
 
 template <int HG>
@@ -54,15 +54,17 @@ struct Layout {
   // control block
   static constexpr uint32_t bar_off = ctl_off;                        // uint64 x 2
   static constexpr uint32_t tmem_off = ctl_off + 16;                  // uint32
-  static constexpr uint32_t slot_off = ctl_off + 32;                  // int32 [2][128]
-  static constexpr uint32_t mref_off = slot_off + 2 * 128 * 4;        // float [HG]
+  static constexpr uint32_t slot_off = ctl_off + 32;                  // int32 [3][128]
+  static constexpr uint32_t mref_off = slot_off + 3 * 128 * 4;        // float [HG]
   static constexpr uint32_t alpha_off = mref_off + HG * 4;            // float [HG]
   static constexpr uint32_t red_off = alpha_off + HG * 4;             // float [2][4][HPT]
   static constexpr uint32_t lsum_off = red_off + 4 * HG * 4;          // float [2][HG]
-  static constexpr uint32_t end = lsum_off + 2 * HG * 4;
+  static constexpr uint32_t qscale_off = lsum_off + 2 * HG * 4;       // float [HG]
+  static constexpr uint32_t end = qscale_off + HG * 4;
   static constexpr uint32_t smem_bytes = end + 1024;                  // + alignment slack
-  // tensor memory: O^T slabs at columns [0, 4HG), S^T at [4HG, 5HG)
-  static constexpr uint32_t tmem_cols = (5 * HG <= 128) ? 128 : (5 * HG <= 256 ? 256 : 512);
+  // tensor memory: O^T slabs at columns [0, 4HG); S^T as two partial sums
+  // (one per MMA issuer) at [4HG, 5HG) and [5HG, 6HG)
+  static constexpr uint32_t tmem_cols = (6 * HG <= 128) ? 128 : (6 * HG <= 256 ? 256 : 512);
   static constexpr uint32_t col_o = 0;
   static constexpr uint32_t col_s = 4 * HG;
   // P^T operand (MN-major, N = HG): one swizzle atom per 8 keys
@@ -154,6 +156,34 @@ __device__ __forceinline__ void tmem_load_cols(uint32_t taddr, float (&x)[N]) {
   }
 }
 
+// Scores: the sum of the two partial S^T accumulators (columns c and c + gap).
+template <int N>
+__device__ __forceinline__ void load_scores(uint32_t taddr, uint32_t gap, float (&x)[N]) {
+  __syncwarp();
+  if constexpr (N == 32) {
+    uint32_t va[32], vb[32];
+    tmem_ld32x2_sync(taddr, taddr + gap, va, vb);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(va[j]) + __uint_as_float(vb[j]);
+  } else {
+    float y[N];
+    tmem_load_cols<N>(taddr, x);
+    tmem_load_cols<N>(taddr + gap, y);
+#pragma unroll
+    for (int j = 0; j < N; ++j) x[j] += y[j];
+  }
+}
+
+// N consecutive floats of shared memory (16-byte aligned) into registers.
+template <int N>
+__device__ __forceinline__ void lds_vec(const float* src, float (&v)[N]) {
+#pragma unroll
+  for (int j = 0; j < N; j += 4) {
+    const float4 t = *reinterpret_cast<const float4*>(src + j);
+    v[j] = t.x; v[j + 1] = t.y; v[j + 2] = t.z; v[j + 3] = t.w;
+  }
+}
+
 template <int N>
 __device__ __forceinline__ void tmem_scale_cols(uint32_t taddr, const float* alpha) {
   __syncwarp();
@@ -212,33 +242,68 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
   float* alpha_s = reinterpret_cast<float*>(smem + L::alpha_off);
   float* red_all = reinterpret_cast<float*>(smem + L::red_off);
   float* lsum = reinterpret_cast<float*>(smem + L::lsum_off);
+  float* qscale = reinterpret_cast<float*>(smem + L::qscale_off);
 
   // ---- prologue ------------------------------------------------------------
-  if (warp == kMmaWarp) tmem_alloc(smem_addr(tmem_slot), L::tmem_cols);
-  if (tid == 0) {
-    mbar_init(bar_mma, 1);
+  if (warp == 0) tmem_alloc(smem_addr(tmem_slot), L::tmem_cols);
+  if (tid == 32) {
+    mbar_init(bar_mma, 2);                        // both MMA issuers commit to it
     mbar_init(bar_fault, 1);
     fence_mbar_init();
   }
   if (tid < HG) m_ref[tid] = -INFINITY;
-  // Q rows of this head group -> 128-byte-swizzled K-major operand
+  // Q rows of this head group -> f16, 128-byte-swizzled K-major operand.
+  // Each head is scaled by 2^-e_h (exact) so that its largest magnitude lies
+  // in [2^14, 2^15): every bf16 element then converts to f16 without loss
+  // (apart from elements below 2^-24 of the head's maximum); 2^e_h is folded
+  // into the head's score scale.  TPH threads own a head (its 72 16-byte
+  // units interleaved among them) and reduce its maximum with shuffles.
   {
+    constexpr int TPH = HG == 64 ? 4 : 8;          // threads per head
+    constexpr int UPT = 72 / TPH;                  // 16-byte units per thread
+    const int h = tid / TPH, part = tid % TPH;
+    const bool active = h < HG;                    // HG = 16 uses 128 threads
     const uint4* qsrc = reinterpret_cast<const uint4*>(
         static_cast<const __nv_bfloat16*>(a.q) + (static_cast<int64_t>(bs) * a.H + g * HG) * kQk);
-    for (int i = tid; i < HG * 72; i += kThreads) {
-      const int h = i / 72, gu = i % 72;          // 16-byte unit gu of head h
-      const uint32_t off = (gu >> 3) * (HG * 128) + (h >> 3) * 1024 + (h & 7) * 128 + (gu & 7) * 16;
-      *reinterpret_cast<uint4*>(q_s + swizzle<3>(off)) = __ldg(qsrc + h * 72 + gu);
+    uint4 qv[UPT];
+    uint32_t m = 0;
+#pragma unroll
+    for (int j = 0; j < UPT; ++j) {
+      qv[j] = active ? __ldg(qsrc + h * 72 + part + j * TPH) : make_uint4(0, 0, 0, 0);
+      const uint32_t w[4] = {qv[j].x, qv[j].y, qv[j].z, qv[j].w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        m = max(m, max((w[k] << 16) & 0x7FFFFFFFu, w[k] & 0x7FFF0000u));   // |bf16| as fp32 bits
+    }
+#pragma unroll
+    for (int off = 1; off < TPH; off <<= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
+    const float amax = __uint_as_float(m);
+    const int e = amax > 0.0f ? ilogbf(amax) + 1 - 15 : 0;
+    const float f = exp2f(static_cast<float>(-e));
+    if (active && part == 0) qscale[h] = a.sm_scale * 1.4426950408889634f * exp2f(static_cast<float>(e));
+    if (active) {
+#pragma unroll
+      for (int j = 0; j < UPT; ++j) {
+        const int gu = part + j * TPH;             // 16-byte unit of head h
+        const uint32_t w[4] = {qv[j].x, qv[j].y, qv[j].z, qv[j].w};
+        uint32_t o[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const __half2 hv = __floats2half2_rn(__uint_as_float(w[k] << 16) * f,
+                                               __uint_as_float(w[k] & 0xFFFF0000u) * f);
+          o[k] = *reinterpret_cast<const uint32_t*>(&hv);
+        }
+        const uint32_t off = (gu >> 3) * (HG * 128) + (h >> 3) * 1024 + (h & 7) * 128 + (gu & 7) * 16;
+        *reinterpret_cast<uint4*>(q_s + swizzle<3>(off)) = make_uint4(o[0], o[1], o[2], o[3]);
+      }
     }
   }
-  // slots of the first tile
-  if (warp == kMmaWarp && my_tiles > 0) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int r = lane + 32 * i;
-      slot_s[r] = resolve_slot(topk_row, tile_begin * kTileKeys + r, a.K, l_eff, pt_row,
-                               a.pt_stride, a.num_slots, a.dev_err);
-    }
+  // slots of the first two tiles (a ring of three tiles, filled two ahead)
+  {
+    const int t = tid >> 7, r = tid & 127;
+    if (t < my_tiles)
+      slot_s[t * 128 + r] = resolve_slot(topk_row, (tile_begin + t) * kTileKeys + r, a.K, l_eff,
+                                         pt_row, a.pt_stride, a.num_slots, a.dev_err);
   }
   fence_async_smem();
   tc_fence_before_sync();
@@ -246,16 +311,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
 
-  if (a.fault_site == 1 && warp == kMmaWarp) {
-    // test hook: the MMA warp waits on a barrier that nothing arrives on
+  if (a.fault_site == 1 && warp == 0) {
+    // test hook: warp 0 waits on a barrier that nothing arrives on
     const bool ok = mbar_wait_bounded(bar_fault, 0, a.timeout_ns);
     __syncwarp();
     if (!ok && lane == 0) flag_error(a.dev_err, kDevTimeout);
   }
 
-  // softmax roles (warps 0..7): group G owns heads [G*HPT, G*HPT + HPT);
-  // thread (quarter, lane) owns key row r = quarter*32 + lane of each tile,
-  // which is TMEM lane r.
+  // softmax roles: group G owns heads [G*HPT, G*HPT + HPT); thread (quarter,
+  // lane) owns key row r = quarter*32 + lane of each tile = TMEM lane r.
   const int G = warp >> 2;
   const int quarter = warp & 3;
   const int r_key = quarter * 32 + lane;
@@ -263,109 +327,163 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
   const int bar_group = 1 + G;
   float* red = red_all + G * 4 * HPT;
   const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-  const float scale = a.sm_scale * 1.4426950408889634f;   // base-2 exponent
 
-  float l_true[HPT], l_bf16[HPT];
+  // Running sum of p per head (fp32).  It normalizes O and gives lse; the
+  // f16 rounding of p inside PV changes each weight by at most 2^-12.
+  float l_sum[HPT];
 #pragma unroll
-  for (int h = 0; h < HPT; ++h) { l_true[h] = 0.0f; l_bf16[h] = 0.0f; }
-  uint32_t mma_phase = 0;
+  for (int h = 0; h < HPT; ++h) l_sum[h] = 0.0f;
   bool timed_out = false;
 
+  // MMA descriptors: built once, advanced by adding 16-byte-unit offsets to
+  // the start-address field (addresses stay below 2^18, so no carry).
   const uint32_t kv_addr = smem_addr(kv_s);
-  const uint32_t q_addr = smem_addr(q_s);
-  const uint32_t p_addr = kv_addr + 8 * kChunkBytes;   // over the rope slab
+  const uint64_t desc_k = smem_desc(kv_addr, 16, 1024, kSwizzle128);                // K-major A
+  const uint64_t desc_q = smem_desc(smem_addr(q_s), 16, 1024, kSwizzle128);         // K-major B
+  const uint64_t desc_v = smem_desc(kv_addr, kChunkBytes, 1024, kSwizzle128);       // MN-major A
+  const uint64_t desc_p = smem_desc(kv_addr + 8 * kChunkBytes, 8192, L::p_atom_bytes,
+                                    L::p_swizzle_mode);                            // MN-major B
+
+  // Rows of the next tile travel in registers: warp w holds rows 16w..16w+15
+  // as three 32-bit words per lane (latent lo, latent hi, scales/rope), so
+  // their HBM latency overlaps the MMAs and softmax of the current tile.
+  uint32_t wlo[16], whi[16], wex[16];
+  auto issue_row_loads = [&](const int32_t* slots) {
+    int32_t sv[16];
+#pragma unroll
+    for (int i = 0; i < 16; i += 4) {
+      const int4 t = *reinterpret_cast<const int4*>(slots + warp * 16 + i);
+      sv[i] = t.x; sv[i + 1] = t.y; sv[i + 2] = t.z; sv[i + 3] = t.w;
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int32_t sl = sv[i];
+      if (sl >= 0) {
+        const uint32_t* row =
+            reinterpret_cast<const uint32_t*>(a.pool + static_cast<int64_t>(sl) * kRowBytes);
+        wlo[i] = __ldg(row + lane);
+        whi[i] = __ldg(row + 32 + lane);
+        wex[i] = lane < 24 ? __ldg(row + 64 + lane) : 0u;
+      } else {
+        wlo[i] = whi[i] = wex[i] = 0u;                   // masked key: zero row
+      }
+    }
+  };
+  if (my_tiles > 0) issue_row_loads(slot_s);
+
+  // dequant store addresses: lane l writes latent units l%8 of slab l/8 (and
+  // slab 4 + l/8), lanes 8..23 rope half-units of slab 8; rows of this warp
+  // start at line 2*warp*1024.  Indexed by the row's r%8 (the swizzle phase).
+  const uint32_t scale_sel = dequant_scale_selector(lane);
+  uint32_t lat_base[8], rope_base[8];                 // shared-window addresses
+  {
+    const uint32_t kv = smem_addr(kv_s) + warp * 2048;
+    const uint32_t lr = (lane - 8) & 15;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      lat_base[j] = kv + (lane >> 3) * kChunkBytes + (((lane & 7) ^ j) << 4);
+      rope_base[j] = kv + 8 * kChunkBytes + ((((lr >> 1) ^ j) << 4) | ((lr & 1) << 3));
+    }
+  }
 
   for (int it = 0; it < my_tiles; ++it) {
     const int tile = tile_begin + it;
-    const int buf = it & 1;
-    // ---- a3/a4: gather + dequantize the tile into shared memory (warps 0..7)
-    if (warp < 8) {
-      const int32_t* slots = slot_s + buf * 128;
-      uint32_t wlo[16], whi[16], wex[16];
+    const int ring = it % 3;
+    // slot of key (tile + 2, row warp*16 + lane) for lanes 0..15, resolved in
+    // three steps spread over this iteration (top-k load, page-table load,
+    // slot) so that neither dependent load stalls the warp
+    const bool resolve_ahead = (it + 2 < my_tiles) && lane < 16;
+    const int k_ahead = (tile + 2) * kTileKeys + warp * 16 + lane;
+    int32_t idx_ahead = -1, page_ahead = -1, pi_ahead = -1;
+    if (resolve_ahead && k_ahead < a.K) idx_ahead = __ldg(topk_row + k_ahead);
+
+    // ---- a3/a4: dequantize the tile into shared memory ----
+    if (it > 0) {
+      // the tile buffer (and O) are free once the previous PV is done
+      if (!mbar_wait_bounded(bar_mma, 1, a.timeout_ns)) timed_out = true;
+      __syncwarp();
+      tc_fence_after_sync();
+    }
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const int32_t sl = slots[warp * 16 + i];
-        if (sl >= 0) {
-          const uint32_t* row =
-              reinterpret_cast<const uint32_t*>(a.pool + static_cast<int64_t>(sl) * kRowBytes);
-          wlo[i] = __ldg(row + lane);
-          whi[i] = __ldg(row + 32 + lane);
-          wex[i] = lane < 24 ? __ldg(row + 64 + lane) : 0u;
-        } else {
-          wlo[i] = whi[i] = wex[i] = 0u;                 // masked key: zero row
-        }
-      }
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const int r = warp * 16 + i;
-        const DequantRow d = dequant_row_words(wlo[i], whi[i], wex[i], lane);
-        const uint32_t rowoff = (r >> 3) * 1024 + (r & 7) * 128;
-        const uint32_t u = (lane & 7) * 16;
-        *reinterpret_cast<uint4*>(kv_s + swizzle<3>((lane >> 3) * kChunkBytes + rowoff + u)) =
-            d.lat_lo;
-        *reinterpret_cast<uint4*>(kv_s + swizzle<3>((4 + (lane >> 3)) * kChunkBytes + rowoff + u)) =
-            d.lat_hi;
-        if (lane >= 8 && lane < 24) {
-          const uint32_t lr = lane - 8;
-          *reinterpret_cast<uint2*>(kv_s + swizzle<3>(8 * kChunkBytes + rowoff + lr * 8)) = d.rope;
-        }
-      }
-    } else if (it + 1 < my_tiles) {
-      // ---- a2: next tile's slots (warp 8) ----
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int r = lane + 32 * i;
-        slot_s[(buf ^ 1) * 128 + r] =
-            resolve_slot(topk_row, (tile + 1) * kTileKeys + r, a.K, l_eff, pt_row, a.pt_stride,
-                         a.num_slots, a.dev_err);
-      }
+    for (int i = 0; i < 16; ++i) {
+      // row r = 16*warp + i: its 128-byte line in each slab is at
+      // (r/8)*1024 + (r%8)*128 and the 16-byte unit u sits at u ^ (r%8)
+      // (r%8 = i%8), so the addresses are per-lane constants plus immediates
+      const DequantRow d = dequant_row_words(wlo[i], whi[i], wex[i], lane, scale_sel);
+      const uint32_t line = (i >> 3) * 1024 + (i & 7) * 128;
+      st_shared_v4(lat_base[i & 7] + line, d.lat_lo);
+      st_shared_v4(lat_base[i & 7] + line + 4 * kChunkBytes, d.lat_hi);
+      if (lane >= 8 && lane < 24) st_shared_v2(rope_base[i & 7] + line, d.rope);
     }
     fence_async_smem();
     __syncthreads();
 
-    // ---- a5: S^T = K_tile . Q^T ----
-    if (warp == kMmaWarp && lane == 0) {
+    // ---- a5: S^T = K_tile . Q^T, issued by two threads (one MMA stream
+    // cannot keep the tensor core busy at N = HG): thread 0 sums k-steps
+    // 0..17 into S_a, thread 32 k-steps 18..35 into S_b ----
+    if (tid == 0 || tid == 32) {
       tc_fence_after_sync();
-      constexpr uint32_t idesc = idesc_bf16(128, HG, false, false);
+      constexpr uint32_t idesc = idesc_f16(128, HG, false, false);
+      const int half = tid >> 5;
 #pragma unroll
-      for (int kk = 0; kk < 36; ++kk) {
+      for (int j = 0; j < 18; ++j) {
+        const uint32_t kk = half * 18 + j;
         const uint32_t c = kk >> 2, sub = kk & 3;
-        const uint64_t ad = smem_desc(kv_addr + c * kChunkBytes + sub * 32, 16, 1024, kSwizzle128);
-        const uint64_t bd = smem_desc(q_addr + c * (HG * 128) + sub * 32, 16, 1024, kSwizzle128);
-        mma_bf16(tmem + L::col_s, ad, bd, idesc, kk > 0 ? 1u : 0u);
+        mma_f16kind(tmem + L::col_s + half * HG, desc_k + ((c * kChunkBytes + sub * 32) >> 4),
+                    desc_q + ((c * (HG * 128) + sub * 32) >> 4), idesc, j > 0 ? 1u : 0u);
       }
       mma_commit(bar_mma);
     }
+    // ---- a3: the next tile's gather runs under the QK MMAs (its slots were
+    // resolved earlier); the warps would otherwise wait for QK here
+    if (it + 1 < my_tiles) issue_row_loads(slot_s + ((it + 1) % 3) * 128);
+    // ---- a2, second step: page-table entry of the key two tiles ahead
+    if (resolve_ahead) {
+      pi_ahead = slot_page_index(idx_ahead, l_eff, a.pt_stride, a.dev_err);
+      if (pi_ahead >= 0) page_ahead = __ldg(pt_row + pi_ahead);
+    }
 
-    // ---- a6: online softmax (warps 0..7, two head groups) ----
-    if (warp < 8) {
-      if (!mbar_wait_bounded(bar_mma, mma_phase, a.timeout_ns)) timed_out = true;
+    // ---- a6: online softmax (two head groups) ----
+    {
+      if (!mbar_wait_bounded(bar_mma, 0, a.timeout_ns)) timed_out = true;   // QK done
       __syncwarp();                    // lanes may leave the wait at different times
       tc_fence_after_sync();
-      const bool valid = slot_s[buf * 128 + r_key] >= 0;
-      float x[HPT];
-      tmem_load_cols<HPT>(lane_base + L::col_s + h0, x);
-      bool need = false;
+      const bool valid = slot_s[ring * 128 + r_key] >= 0;
+      // x = log2-domain score relative to the head's reference maximum
+      float x[HPT], c[HPT], mr[HPT];
+      load_scores<HPT>(lane_base + L::col_s + h0, HG, x);
+      lds_vec<HPT>(qscale + h0, c);
+      lds_vec<HPT>(m_ref + h0, mr);
+      float xmax = -INFINITY;
 #pragma unroll
       for (int h = 0; h < HPT; ++h) {
-        x[h] = valid ? x[h] * scale : -INFINITY;
-        need |= x[h] > m_ref[h0 + h] + kRaiseThreshold;
+        x[h] = fmaf(x[h], c[h], -mr[h]);
+        xmax = fmaxf(xmax, x[h]);
       }
-      need = named_sync_or(bar_group, 128, need);
+      const bool need = named_sync_or(bar_group, 128, valid && xmax > kRaiseThreshold);
       if (need) {
-        // raise the reference maximum to the tile maximum
-        group_reduce<HPT, true>(x, quarter, lane, red, alpha_s + h0, bar_group);
+        // (rare) raise the reference maximum of every head to its tile maximum
+        load_scores<HPT>(lane_base + L::col_s + h0, HG, x);
+#pragma unroll
+        for (int h = 0; h < HPT; ++h) x[h] = valid ? x[h] * c[h] : -INFINITY;
+        float v[HPT];
+#pragma unroll
+        for (int h = 0; h < HPT; ++h) v[h] = x[h];
+        group_reduce<HPT, true>(v, quarter, lane, red, alpha_s + h0, bar_group);
         if (r_key < HPT) {
           const float mo = m_ref[h0 + r_key];
           const float mn = fmaxf(mo, alpha_s[h0 + r_key]);
-          alpha_s[h0 + r_key] = (mo == mn) ? 1.0f : exp2f(mo - mn);
+          alpha_s[h0 + r_key] = (mo == mn) ? 1.0f : fast_exp2(mo - mn);
           m_ref[h0 + r_key] = mn;
         }
         named_sync(bar_group, 128);
+        float al[HPT];
+        lds_vec<HPT>(alpha_s + h0, al);
+        lds_vec<HPT>(m_ref + h0, mr);
 #pragma unroll
         for (int h = 0; h < HPT; ++h) {
-          l_true[h] *= alpha_s[h0 + h];
-          l_bf16[h] *= alpha_s[h0 + h];
+          l_sum[h] *= al[h];
+          x[h] -= mr[h];
         }
         if (it > 0) {
 #pragma unroll
@@ -373,22 +491,22 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
             tmem_scale_cols<HPT>(lane_base + L::col_o + mb * HG + h0, alpha_s + h0);
           tmem_st_wait();
         }
-        tmem_load_cols<HPT>(lane_base + L::col_s + h0, x);   // scores again
-#pragma unroll
-        for (int h = 0; h < HPT; ++h) x[h] = valid ? x[h] * scale : -INFINITY;
       }
-      // probabilities -> bf16 P^T row r_key, heads [h0, h0 + HPT)
+      // probabilities -> f16 P^T row r_key, heads [h0, h0 + HPT)
       uint32_t packed[HPT / 2];
+      if (valid) {
 #pragma unroll
-      for (int h = 0; h < HPT; h += 2) {
-        const float p0 = valid ? exp2f(x[h] - m_ref[h0 + h]) : 0.0f;
-        const float p1 = valid ? exp2f(x[h + 1] - m_ref[h0 + h + 1]) : 0.0f;
-        const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
-        l_true[h] += p0;
-        l_true[h + 1] += p1;
-        l_bf16[h] += __low2float(pb);
-        l_bf16[h + 1] += __high2float(pb);
-        packed[h / 2] = *reinterpret_cast<const uint32_t*>(&pb);
+        for (int h = 0; h < HPT; h += 2) {
+          const float p0 = fast_exp2(x[h]);
+          const float p1 = fast_exp2(x[h + 1]);
+          l_sum[h] += p0;
+          l_sum[h + 1] += p1;
+          const __half2 ph = __floats2half2_rn(p0, p1);
+          packed[h / 2] = *reinterpret_cast<const uint32_t*>(&ph);
+        }
+      } else {
+#pragma unroll
+        for (int h = 0; h < HPT / 2; ++h) packed[h] = 0u;
       }
       uint8_t* p_s = kv_s + 8 * kChunkBytes;
 #pragma unroll
@@ -398,74 +516,84 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
         *reinterpret_cast<uint4*>(p_s + swizzle<L::p_swizzle_bits>(off)) =
             make_uint4(packed[4 * u], packed[4 * u + 1], packed[4 * u + 2], packed[4 * u + 3]);
       }
+      // ---- a2, last step: the slot of the key two tiles ahead.  Its ring
+      // entry was last read by the previous tile's softmax.
+      if (resolve_ahead)
+        slot_s[((it + 2) % 3) * 128 + warp * 16 + lane] =
+            pi_ahead >= 0 ? slot_from_page(page_ahead, idx_ahead, a.num_slots, a.dev_err) : -1;
       fence_async_smem();
       tc_fence_before_sync();
     }
-    mma_phase ^= 1;
     __syncthreads();
 
-    // ---- a7: O^T += V^T . P^T ----
-    if (warp == kMmaWarp && lane == 0) {
+    // ---- a7: O^T += V^T . P^T; thread 0 issues slabs 0-1, thread 32 slabs
+    // 2-3 (k-steps outer, so consecutive MMAs go to different accumulators)
+    if (tid == 0 || tid == 32) {
       tc_fence_after_sync();
-      constexpr uint32_t idesc = idesc_bf16(128, HG, true, true);
+      constexpr uint32_t idesc = idesc_f16(128, HG, true, true);
+      const int half = tid >> 5;
 #pragma unroll
-      for (int mb = 0; mb < 4; ++mb) {
+      for (int ks = 0; ks < 8; ++ks) {
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          const uint64_t ad = smem_desc(kv_addr + (2 * mb) * kChunkBytes + (2 * ks) * 1024,
-                                        kChunkBytes, 1024, kSwizzle128);
-          const uint64_t bd = smem_desc(p_addr + (2 * ks) * L::p_atom_bytes, 8192,
-                                        L::p_atom_bytes, L::p_swizzle_mode);
-          mma_bf16(tmem + L::col_o + mb * HG, ad, bd, idesc, (it > 0 || ks > 0) ? 1u : 0u);
+        for (int j = 0; j < 2; ++j) {
+          const int mb = 2 * half + j;
+          mma_f16kind(tmem + L::col_o + mb * HG,
+                      desc_v + (((2 * mb) * kChunkBytes + (2 * ks) * 1024) >> 4),
+                      desc_p + (((2 * ks) * L::p_atom_bytes) >> 4), idesc,
+                      (it > 0 || ks > 0) ? 1u : 0u);
         }
       }
       mma_commit(bar_mma);
     }
-    // the tile buffer is reused next iteration: wait for PV to finish
-    if (!mbar_wait_bounded(bar_mma, mma_phase, a.timeout_ns)) timed_out = true;
+  }
+  // the last PV must be complete before O is read or TMEM is freed
+  if (my_tiles > 0) {
+    if (!mbar_wait_bounded(bar_mma, 1, a.timeout_ns)) timed_out = true;
     __syncwarp();
-    mma_phase ^= 1;
     tc_fence_after_sync();
   }
 
-  // ---- a8: epilogue (warps 0..7) ----
+  // ---- a8: epilogue ----
   const bool partial = a.splits > 1;
   const int64_t out_head0 = static_cast<int64_t>(bs) * a.H + g * HG;   // first head row
   const int64_t part = static_cast<int64_t>(unit) * a.splits + split;
-  if (warp < 8) {
-    group_reduce<HPT, false>(l_true, quarter, lane, red, lsum + h0, bar_group);
-    group_reduce<HPT, false>(l_bf16, quarter, lane, red, lsum + HG + h0, bar_group);
-    if (r_key < HPT) {
-      const int h = h0 + r_key;
-      const float lt = lsum[h];
-      const float lse = (lt > 0.0f) ? (m_ref[h] + log2f(lt)) * 0.69314718055994531f : -INFINITY;
-      if (partial) a.ws_lse[part * HG + h] = lse;
-      else a.lse[out_head0 + h] = lse;
+  group_reduce<HPT, false>(l_sum, quarter, lane, red, lsum + h0, bar_group);
+  if (r_key < HPT) {
+    const float lt = lsum[h0 + r_key];
+    lsum[HG + h0 + r_key] = lt > 0.0f ? __frcp_rn(lt) : 0.0f;     // 1 / l
+  }
+  named_sync(bar_group, 128);
+  if (r_key < HPT) {
+    const int h = h0 + r_key;
+    const float lt = lsum[h];
+    const float lse = (lt > 0.0f) ? (m_ref[h] + log2f(lt)) * 0.69314718055994531f : -INFINITY;
+    if (partial) a.ws_lse[part * HG + h] = lse;
+    else a.lse[out_head0 + h] = lse;
+  }
+#pragma unroll
+  for (int mb = 0; mb < 4; ++mb) {
+    const int d = mb * 128 + r_key;
+    float o[HPT];
+    if (my_tiles > 0) {
+      tmem_load_cols<HPT>(lane_base + L::col_o + mb * HG + h0, o);
+    } else {
+#pragma unroll
+      for (int j = 0; j < HPT; ++j) o[j] = 0.0f;
     }
+    float inv[HPT];
+    lds_vec<HPT>(lsum + HG + h0, inv);
 #pragma unroll
-    for (int mb = 0; mb < 4; ++mb) {
-      const int d = mb * 128 + r_key;
-      float o[HPT];
-      if (my_tiles > 0) {
-        tmem_load_cols<HPT>(lane_base + L::col_o + mb * HG + h0, o);
-      } else {
-#pragma unroll
-        for (int j = 0; j < HPT; ++j) o[j] = 0.0f;
-      }
-#pragma unroll
-      for (int j = 0; j < HPT; ++j) {
-        const int h = h0 + j;
-        const float den = lsum[HG + h];
-        const float v = den > 0.0f ? o[j] / den : 0.0f;
-        if (partial) a.ws_o[(part * HG + h) * kLatent + d] = v;
-        else static_cast<__nv_bfloat16*>(a.out)[(out_head0 + h) * kLatent + d] = __float2bfloat16_rn(v);
-      }
+    for (int j = 0; j < HPT; ++j) {
+      const int h = h0 + j;
+      const float v = o[j] * inv[j];
+      if (partial) a.ws_o[(part * HG + h) * kLatent + d] = v;
+      else static_cast<__nv_bfloat16*>(a.out)[(out_head0 + h) * kLatent + d] = __float2bfloat16_rn(v);
     }
   }
   if (timed_out) flag_error(a.dev_err, kDevTimeout);
   tc_fence_before_sync();
   __syncthreads();
-  if (warp == kMmaWarp) {
+  if (warp == 0) {
     __syncwarp();
     tc_fence_after_sync();
     tmem_dealloc(tmem, L::tmem_cols);
@@ -519,8 +647,8 @@ __global__ void __launch_bounds__(256) merge_kernel(DecodeArgs a, int n_units) {
   if (lane == 0) a.lse[row] = (wsum > 0.0f) ? m + logf(wsum) : -INFINITY;
 }
 
-// Debug: the decode's index resolution and dequantization written to HBM.
-// One warp per (b, s, k) row.
+// Debug: the decode's index resolution and dequantization (the f16 operand
+// values) written to HBM.  One warp per (b, s, k) row.
 __global__ void __launch_bounds__(256) debug_gather_kernel(GatherArgs a) {
   const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
@@ -542,12 +670,12 @@ __global__ void __launch_bounds__(256) debug_gather_kernel(GatherArgs a) {
     whi = __ldg(row + 32 + lane);
     wex = lane < 24 ? __ldg(row + 64 + lane) : 0u;
   }
-  DequantRow d = dequant_row_words(wlo, whi, wex, lane);
+  DequantRow d = dequant_row_words(wlo, whi, wex, lane, dequant_scale_selector(lane));
   if (slot < 0) {
     d.lat_lo = d.lat_hi = make_uint4(0, 0, 0, 0);
     d.rope = make_uint2(0, 0);
   }
-  __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.rows) + gw * kQk;
+  __half* out = static_cast<__half*>(a.rows) + gw * kQk;
   *reinterpret_cast<uint4*>(out + 8 * lane) = d.lat_lo;
   *reinterpret_cast<uint4*>(out + 256 + 8 * lane) = d.lat_hi;
   if (lane >= 8 && lane < 24) *reinterpret_cast<uint2*>(out + 512 + 4 * (lane - 8)) = d.rope;

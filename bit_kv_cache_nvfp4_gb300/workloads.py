@@ -192,8 +192,10 @@ def _uniform_lens(key: int, B: int, lo: int, hi: int) -> torch.Tensor:
 CONFIG_NAMES = ("tiny", "decode", "long", "specverify", "splitk")
 
 
-def make_workload(name: str, seed: int = 0) -> Workload:
-    """The five decode configurations, deterministic in ``seed``."""
+def make_workload(name: str, seed: int = 0, sessions: int | None = None) -> Workload:
+    """The five decode configurations, deterministic in ``seed``.  For the
+    long-context configuration ``sessions`` overrides B (the first sessions
+    of the same seeded draw)."""
     cid = CONFIG_NAMES.index(name) + 1
     sub = seed * 1000 + cid
     kt = stream_key(sub, S_TOPK)
@@ -207,7 +209,7 @@ def make_workload(name: str, seed: int = 0) -> Workload:
         topk = torch.stack([_unique_sample(kt + b, 0, int(lens[b]), K)
                             for b in range(B)]).view(B, 1, K)
     elif name == "long":
-        B, Sq, H, K = 64, 1, 64, 2048
+        B, Sq, H, K = (sessions or 64), 1, 64, 2048
         L = 204800
         lens = torch.full((B,), L, dtype=torch.int32)
         rows = []

@@ -120,7 +120,10 @@ kv4_status kv4_decode_plan(int B, int Sq, int H, int K, int force_splits,
  *   workspace_dev  device scratch of at least the bytes kv4_decode_plan
  *                  returns (may be NULL when that is 0), 16-byte aligned
  * Duplicated positions count once per occurrence.  Scores use all 576 dims;
- * the weighted sum uses the 512 latent dims of the same rows.
+ * the weighted sum uses the 512 latent dims of the same rows.  Arithmetic:
+ * K/V rows are dequantized exactly to f16, q is converted to f16 after an
+ * exact per-head power-of-two scaling, QK^T and PV accumulate in fp32 on the
+ * tensor cores, softmax weights enter PV as f16.
  * ------------------------------------------------------------------------- */
 kv4_status kv4_sparse_mla_decode(const void* q_dev, const uint8_t* pool_dev,
                                  int64_t num_slots, const int32_t* page_table_dev,
@@ -134,10 +137,11 @@ kv4_status kv4_sparse_mla_decode(const void* q_dev, const uint8_t* pool_dev,
 
 /* ---------------------------------------------------------------------------
  * kv4_debug_gather_dequant -- the decode's own index resolution and
- * dequantization, written out: rows_dev bf16 [B, Sq, K, 576] receives the
- * dequantized selected rows (all zero for a masked key).  Exists so that the
- * gather indexing can be checked bit for bit; same argument meaning as
- * kv4_sparse_mla_decode.
+ * dequantization, written out: rows_dev f16 [B, Sq, K, 576] receives the
+ * dequantized selected rows, i.e. the tensor-core operand values (every
+ * E2M1 x E4M3 product and E4M3 value is exact in f16); a masked key gives an
+ * all-zero row.  Exists so that the gather indexing can be checked bit for
+ * bit; same argument meaning as kv4_sparse_mla_decode.
  * ------------------------------------------------------------------------- */
 kv4_status kv4_debug_gather_dequant(const uint8_t* pool_dev, int64_t num_slots,
                                     const int32_t* page_table_dev, int64_t pt_stride,

@@ -11,8 +11,21 @@ import torch
 import oracle
 from bit_kv_cache_nvfp4_gb300 import workloads as wl
 
-OUT_ATOL = 2e-2      # max |out_gpu (bf16) - out_oracle (fp32)|
-LSE_ATOL = 1e-3      # max |lse_gpu - lse_oracle|
+# Tolerances.  The computation must be within 2e-2 of the oracle on every
+# output element and within 1e-3 on every lse.  The output tensor is bf16,
+# and rounding an exact value to bf16 alone moves it by up to half a bf16
+# ulp -- more than 2e-2 once |out| >= 8, which the x8 outlier channels of the
+# workloads reach -- so each element is allowed 2e-2 plus half a bf16 ulp at
+# its magnitude.
+OUT_ATOL = 2e-2
+LSE_ATOL = 1e-3
+
+
+def bf16_half_ulp(x: np.ndarray) -> np.ndarray:
+    """Half the bf16 spacing at |x| (2^(e-8) for |x| in [2^e, 2^(e+1)))."""
+    a = np.abs(np.asarray(x, dtype=np.float64))
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    return np.where(a > 0, np.exp2(e - 8), 0.0)
 
 
 def need_gpu():
@@ -85,10 +98,14 @@ def assert_close(out_gpu: torch.Tensor, lse_gpu: torch.Tensor, out_ref: np.ndarr
     assert o.shape == out_ref.shape and l.shape == lse_ref.shape
     both_inf = np.isneginf(l) & np.isneginf(lse_ref)
     assert np.array_equal(np.isneginf(l), np.isneginf(lse_ref)), f"{what}: -inf lse pattern differs"
-    err_o = np.abs(o - out_ref)
+    err_o = np.abs(o.astype(np.float64) - out_ref)
     err_l = np.where(both_inf, 0.0, np.abs(l - lse_ref))
     assert np.isfinite(o).all(), f"{what}: non-finite output"
+    bound = OUT_ATOL + bf16_half_ulp(out_ref)
+    excess = err_o - bound
+    i = np.unravel_index(np.argmax(excess), excess.shape)
+    assert excess[i] <= 0, (f"{what}: |out err| {err_o[i]:.4g} > {bound[i]:.4g} at {i} "
+                            f"(oracle {out_ref[i]:.5g}, gpu {o[i]:.5g})")
     mo, ml = float(err_o.max()), float(err_l.max())
-    assert mo <= OUT_ATOL, f"{what}: max |out err| {mo:.4g} > {OUT_ATOL}"
     assert ml <= LSE_ATOL, f"{what}: max |lse err| {ml:.4g} > {LSE_ATOL}"
     return mo, ml
