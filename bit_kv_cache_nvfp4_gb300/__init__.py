@@ -30,7 +30,8 @@ ROW_BYTES, LATENT, ROPE, QK_DIM, PAGE, TILE_KEYS = 352, 512, 64, 576, 64, 128
 DEV_BAD_SLOT, DEV_BAD_PAGE, DEV_TIMEOUT = 1, 2, 4
 _STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported shape or page size",
            3: "device is not compute capability 10.3", 4: "kernel launch failed",
-           5: "workspace missing or too small"}
+           5: "workspace missing or too small",
+           6: "split-K partials exceed the library's static scratch"}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _lock = threading.Lock()

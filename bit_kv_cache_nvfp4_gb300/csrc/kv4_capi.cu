@@ -221,6 +221,71 @@ kv4_status kv4_debug_gather_dequant(const uint8_t* pool_dev, int64_t num_slots,
              : KV4_ERR_LAUNCH;
 }
 
+// ---------------------------------------------------------------------------
+// Decode without a caller-provided workspace.
+//
+// Some callers cannot allocate device memory at the point where they run the
+// decode -- for example a plugin that its host engine hands only input and
+// output buffers, while the engine owns and budgets every byte of device
+// memory, or code that must not call cudaMalloc because it synchronizes the
+// device.  For them the split-K partials go to a buffer that is part of the
+// library itself: a file-scope device array, created when the library's
+// module is loaded on a device and held by that device until the process
+// exits.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr size_t kStaticScratchBytes = size_t(24) << 20;   // 24 MiB
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+std::atomic<void*> g_static_scratch_ptr[kMaxDevices];      // per device, set up once
+
+// Device address of g_static_scratch on the current device.  In host code
+// the symbol's name is only a host-side stand-in, so its address comes from
+// cudaGetSymbolAddress, asked once per device with that device current.
+kv4_status static_scratch(void** ptr) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+    return KV4_ERR_LAUNCH;
+  void* p = g_static_scratch_ptr[dev].load();
+  if (p == nullptr) {
+    if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || p == nullptr)
+      return KV4_ERR_LAUNCH;
+    g_static_scratch_ptr[dev].store(p);
+  }
+  *ptr = p;
+  return KV4_OK;
+}
+
+}  // namespace
+
+kv4_status kv4_sparse_mla_decode_noalloc(const void* q_dev, const uint8_t* pool_dev,
+                                         int64_t num_slots, const int32_t* page_table_dev,
+                                         int64_t pt_stride, int page_size,
+                                         const int32_t* topk_idx_dev, int K,
+                                         const int32_t* seq_lens_dev, int B, int Sq, int H,
+                                         float sm_scale, void* out_dev, float* lse_dev,
+                                         int force_splits, int32_t* dev_err,
+                                         kv4_stream_t stream) {
+  const kv4_status shape = check_decode_shape(B, Sq, H, K);
+  if (shape != KV4_OK) return shape;
+  if (page_size != KV4_PAGE) return KV4_ERR_UNSUPPORTED;
+  if (B == 0) return KV4_OK;
+  int sms = 0;
+  kv4_status st = device_info(&sms);
+  if (st != KV4_OK) return st;
+  const Plan p = make_plan(B, Sq, H, K, force_splits, sms);
+  if (p.ws_bytes > kStaticScratchBytes) return KV4_ERR_SCRATCH_LIMIT;
+  void* scratch = nullptr;
+  st = static_scratch(&scratch);
+  if (st != KV4_OK) return st;
+  return kv4_sparse_mla_decode(q_dev, pool_dev, num_slots, page_table_dev, pt_stride, page_size,
+                               topk_idx_dev, K, seq_lens_dev, B, Sq, H, sm_scale, out_dev, lse_dev,
+                               scratch, kStaticScratchBytes, force_splits, dev_err, stream);
+}
+
+size_t kv4_noalloc_scratch_bytes(void) { return kStaticScratchBytes; }
+
 kv4_status kv4_set_wait_limit(int64_t timeout_ns, int fault_site) {
   if (timeout_ns < 0 || fault_site < 0 || fault_site > 1) return KV4_ERR_INVALID_ARG;
   g_timeout_ns.store(timeout_ns > 0 ? timeout_ns : 1000000000);
@@ -241,6 +306,9 @@ const char* kv4_status_str(kv4_status status) {
     case KV4_ERR_ARCH: return "current device is not compute capability 10.3";
     case KV4_ERR_LAUNCH: return "kernel launch failed";
     case KV4_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case KV4_ERR_SCRATCH_LIMIT:
+      return "split-K partials exceed the library's static scratch (see "
+             "kv4_noalloc_scratch_bytes); pass a workspace or force fewer splits";
   }
   return "unknown status";
 }

@@ -53,7 +53,9 @@ typedef enum {
   KV4_ERR_UNSUPPORTED = 2,   /* H or page size outside the supported set      */
   KV4_ERR_ARCH = 3,          /* current device is not compute capability 10.3 */
   KV4_ERR_LAUNCH = 4,        /* a kernel launch failed (cudaGetLastError)     */
-  KV4_ERR_WORKSPACE = 5      /* workspace missing or smaller than required    */
+  KV4_ERR_WORKSPACE = 5,     /* workspace missing or smaller than required    */
+  KV4_ERR_SCRATCH_LIMIT = 6  /* kv4_sparse_mla_decode_noalloc: the split-K
+                                partials would not fit the static scratch     */
 } kv4_status;
 
 /* Flags OR-ed into *dev_err by the kernels. */
@@ -149,6 +151,40 @@ kv4_status kv4_debug_gather_dequant(const uint8_t* pool_dev, int64_t num_slots,
                                     const int32_t* seq_lens_dev, int B, int Sq,
                                     void* rows_dev, int32_t* dev_err,
                                     kv4_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * kv4_sparse_mla_decode_noalloc -- the same decode for callers that cannot
+ * allocate device memory when they call it (for example a plugin whose host
+ * engine hands it only its input and output buffers and owns every byte of
+ * device memory, or code that must not call cudaMalloc because cudaMalloc can
+ * synchronize the device).  The pages have no counterpart: it is an interface
+ * variant of kv4_sparse_mla_decode, with the same arguments except the
+ * workspace, and the same results.
+ *   - The split-K partials go to a file-scope device array inside the library
+ *     of kv4_noalloc_scratch_bytes() bytes (24 MiB).  Every device that loads
+ *     the library holds it until the process exits.
+ *   - A shape whose planned partials need more than that returns
+ *     KV4_ERR_SCRATCH_LIMIT and launches nothing (force fewer splits, or use
+ *     kv4_sparse_mla_decode with a workspace).
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture.
+ *   - All calls share the one array, which keeps the last call's contents;
+ *     nothing in it needs to start at zero (every partial is written before
+ *     it is read).  Calls whose kernels overlap on the GPU (two streams, or
+ *     two threads) race on the array: serialize them.
+ *   - This entry point itself calls no cudaMalloc, cudaFree or allocating
+ *     library routine.
+ * ------------------------------------------------------------------------- */
+kv4_status kv4_sparse_mla_decode_noalloc(const void* q_dev, const uint8_t* pool_dev,
+                                         int64_t num_slots, const int32_t* page_table_dev,
+                                         int64_t pt_stride, int page_size,
+                                         const int32_t* topk_idx_dev, int K,
+                                         const int32_t* seq_lens_dev, int B, int Sq, int H,
+                                         float sm_scale, void* out_dev, float* lse_dev,
+                                         int force_splits, int32_t* dev_err,
+                                         kv4_stream_t stream);
+size_t kv4_noalloc_scratch_bytes(void);
 
 /* Test hook: the next kernel launches use this bounded-wait limit (ns) and,
  * when fault_site != 0, skip one internal mbarrier arrive so that the wait
