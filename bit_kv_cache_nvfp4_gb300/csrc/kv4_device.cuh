@@ -367,6 +367,36 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   return r;
 }
 
+// The three parts of a row, separately (the decode writes them in three
+// passes): latent elements 8l..8l+7, latent 256+8l..256+8l+7, and rope
+// 4(l-8)..4(l-8)+3.  Each latent part shuffles its scale word from the
+// lane that holds it, so every lane of the warp must call them.
+__device__ __forceinline__ uint4 dequant_latent_part(uint32_t w, uint32_t w_ex, int src_lane,
+                                                     uint32_t byte_sel) {
+  const uint32_t sw = __shfl_sync(0xFFFFFFFFu, w_ex, src_lane);
+  const uint32_t s2 = e4m3x2_to_f16x2(prmt(sw, 0u, byte_sel | 0x4440u));   // {s, 0} as f16
+  const uint32_t m = (s2 & 0xFFFFu) * 0x00010001u;               // {s, s}
+  uint32_t h[4];
+  e2m1x8_to_f16x8(w, h);
+  return make_uint4(f16x2_mul(h[0], m), f16x2_mul(h[1], m), f16x2_mul(h[2], m),
+                    f16x2_mul(h[3], m));
+}
+// Latent word w (elements 8w..8w+7) of a row whose scale words sit in lanes
+// 0..7 of the warp (w_ex): the scale byte of its block (w/2) is byte
+// (w/2)%4 of scale word w/8.
+__device__ __forceinline__ uint4 dequant_latent_word(uint32_t w, uint32_t w_ex, int word) {
+  return dequant_latent_part(w, w_ex, word >> 3, (word >> 1) & 3);
+}
+__device__ __forceinline__ uint4 dequant_latent_lo(uint32_t w_lo, uint32_t w_ex, int lane) {
+  return dequant_latent_part(w_lo, w_ex, lane >> 3, (lane >> 1) & 3);
+}
+__device__ __forceinline__ uint4 dequant_latent_hi(uint32_t w_hi, uint32_t w_ex, int lane) {
+  return dequant_latent_part(w_hi, w_ex, 4 + (lane >> 3), (lane >> 1) & 3);
+}
+__device__ __forceinline__ uint2 dequant_rope(uint32_t w_ex) {
+  return make_uint2(e4m3x2_to_f16x2(w_ex & 0xFFFFu), e4m3x2_to_f16x2(w_ex >> 16));
+}
+
 __device__ __forceinline__ DequantRow dequant_row_words(uint32_t w_lo, uint32_t w_hi,
                                                         uint32_t w_ex, int lane,
                                                         uint32_t scale_sel) {

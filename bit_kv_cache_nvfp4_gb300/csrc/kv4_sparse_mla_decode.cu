@@ -7,27 +7,31 @@
 //
 // Work unit: one thread block per (request b, draft token s, head group g,
 // split).  A head group holds HG = min(H, 64) query heads, which all share
-// every gathered row.  The block walks its share of the top-k list in tiles
-// of 128 keys:
-//   a2/a3  warp 8 resolves the next tile's slots (top-k -> page table);
-//          warps 0..7 gather the 352-byte rows (coalesced 4-byte loads,
-//          16 rows in flight per warp)
-//   a4     and dequantize them straight into the 128-byte-swizzled f16
+// every gathered row.  The block (8 warps) walks its share of the top-k list
+// in tiles of 128 keys:
+//   a2     slots are resolved two tiles ahead (top-k -> page table -> slot),
+//          each dependent load spread over a tile's work
+//   a3     each warp gathers 16 rows of the next tile into registers (three
+//          coalesced 4-byte loads per lane and row) while QK runs
+//   a4     and dequantizes them straight into the 128-byte-swizzled f16
 //          operand tile in shared memory (576 columns per key; E2M1 x E4M3
-//          and E4M3 values are exact in f16); q is converted to f16 with a
-//          per-head power-of-two scale folded into the score scale
-//   a5     one thread issues S^T[128 x HG] = K_tile . Q^T on tcgen05
-//          (M = 128 keys, N = HG, K = 576; fp32 accumulator in TMEM)
-//   a6     warps 0..7 read S from TMEM (one key per thread; warps 0..3 take
+//          and E4M3 values are exact in f16) in three passes -- latent
+//          0..255, latent 256..511, rope -- each into the slabs that the
+//          previous tile's PV has already released; q is converted to f16
+//          with a per-head power-of-two scale folded into the score scale
+//   a5     as each pass lands, lane 0 of warps 0 and 1 issue its share of
+//          S^T[128 x HG] = K_tile . Q^T on tcgen05 (M = 128 keys, N = HG,
+//          K = 576) into two fp32 TMEM accumulators
+//   a6     the 8 warps read S from TMEM (one key per thread; warps 0..3 take
 //          the first half of the heads, warps 4..7 the second half) and run
-//          the online softmax in base 2; the running maximum is only raised when
-//          a score exceeds it by more than 8 (so most tiles need no cross-
-//          thread reduction and no rescale), p is rounded to f16 and
+//          the online softmax in base 2; the running maximum is only raised
+//          when a score exceeds it by more than 8 (so most tiles need no
+//          cross-thread reduction and no rescale), p is rounded to f16 and
 //          written as the PV operand over the tile's rope columns, which
 //          QK^T no longer needs
-//   a7     one thread issues O^T[512 x HG] += V^T . P^T (four M = 128 slabs
-//          of latent columns; V^T is the same shared-memory tile read as an
-//          MN-major operand)
+//   a7     the two issuers run O^T[512 x HG] += V^T . P^T (slabs 0-1 and 2-3
+//          of the latent columns; V^T is the same shared-memory tile read as
+//          an MN-major operand) and signal each half's release
 //   a8     epilogue: O / sum(p) -> bf16 out, lse = ln 2 * (m + log2 sum(p));
 //          with several splits the normalized partial (o, lse) goes to the
 //          workspace and
@@ -52,9 +56,9 @@ struct Layout {
   static constexpr uint32_t kv_bytes = 9u * kChunkBytes;              // K/V tile
   static constexpr uint32_t ctl_off = kv_off + kv_bytes;
   // control block
-  static constexpr uint32_t bar_off = ctl_off;                        // uint64 x 2
-  static constexpr uint32_t tmem_off = ctl_off + 16;                  // uint32
-  static constexpr uint32_t slot_off = ctl_off + 32;                  // int32 [3][128]
+  static constexpr uint32_t bar_off = ctl_off;                        // uint64 x 9
+  static constexpr uint32_t tmem_off = ctl_off + 80;                  // uint32
+  static constexpr uint32_t slot_off = ctl_off + 96;                  // int32 [3][128]
   static constexpr uint32_t mref_off = slot_off + 3 * 128 * 4;        // float [HG]
   static constexpr uint32_t alpha_off = mref_off + HG * 4;            // float [HG]
   static constexpr uint32_t red_off = alpha_off + HG * 4;             // float [2][4][HPT]
@@ -234,8 +238,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
 
   uint8_t* q_s = smem;
   uint8_t* kv_s = smem + L::kv_off;
-  const uint32_t bar_mma = smem_addr(smem + L::bar_off);
-  const uint32_t bar_fault = smem_addr(smem + L::bar_off + 8);
+  // mbarriers: QK done (both issuers commit), PV done per 128-column slab of
+  // O (slabs 0-1 from issuer A, 2-3 from issuer B), tile parts written by all
+  // 8 warps (latent group a, latent group b, rope), and the test hook's one.
+  const uint32_t bars = smem_addr(smem + L::bar_off);
+  const uint32_t bar_qk = bars;
+  const uint32_t bar_pv0 = bars + 8;              // + 8 * slab: PV slab (128 columns) done
+  const uint32_t bar_part0 = bars + 40;           // + 8 * part: tile part written
+  const uint32_t bar_fault = bars + 64;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::tmem_off);
   int32_t* slot_s = reinterpret_cast<int32_t*>(smem + L::slot_off);
   float* m_ref = reinterpret_cast<float*>(smem + L::mref_off);
@@ -247,11 +257,19 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
   // ---- prologue ------------------------------------------------------------
   if (warp == 0) tmem_alloc(smem_addr(tmem_slot), L::tmem_cols);
   if (tid == 32) {
-    mbar_init(bar_mma, 2);                        // both MMA issuers commit to it
+    mbar_init(bar_qk, 2);
+    for (int p = 0; p < 4; ++p) mbar_init(bar_pv0 + 8 * p, 1);
+    for (int p = 0; p < 3; ++p) mbar_init(bar_part0 + 8 * p, 8);
     mbar_init(bar_fault, 1);
     fence_mbar_init();
   }
   if (tid < HG) m_ref[tid] = -INFINITY;
+  // slots of the first two tiles (a ring of three tiles, filled two ahead);
+  // started first so that their dependent loads overlap the Q conversion
+  int32_t pro_idx = -1, pro_page = -1, pro_pi = -1;
+  const int pro_t = tid >> 7, pro_r = tid & 127;
+  const int pro_k = (tile_begin + pro_t) * kTileKeys + pro_r;
+  if (pro_t < my_tiles && pro_k < a.K) pro_idx = __ldg(topk_row + pro_k);
   // Q rows of this head group -> f16, 128-byte-swizzled K-major operand.
   // Each head is scaled by 2^-e_h (exact) so that its largest magnitude lies
   // in [2^14, 2^15): every bf16 element then converts to f16 without loss
@@ -274,6 +292,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
 #pragma unroll
       for (int k = 0; k < 4; ++k)
         m = max(m, max((w[k] << 16) & 0x7FFFFFFFu, w[k] & 0x7FFF0000u));   // |bf16| as fp32 bits
+    }
+    if (pro_t < my_tiles) {                        // second step of the slot lookup
+      pro_pi = slot_page_index(pro_idx, l_eff, a.pt_stride, a.dev_err);
+      if (pro_pi >= 0) pro_page = __ldg(pt_row + pro_pi);
     }
 #pragma unroll
     for (int off = 1; off < TPH; off <<= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
@@ -298,25 +320,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
       }
     }
   }
-  // slots of the first two tiles (a ring of three tiles, filled two ahead)
-  {
-    const int t = tid >> 7, r = tid & 127;
-    if (t < my_tiles)
-      slot_s[t * 128 + r] = resolve_slot(topk_row, (tile_begin + t) * kTileKeys + r, a.K, l_eff,
-                                         pt_row, a.pt_stride, a.num_slots, a.dev_err);
-  }
+  if (pro_t < my_tiles)
+    slot_s[pro_t * 128 + pro_r] =
+        pro_pi >= 0 ? slot_from_page(pro_page, pro_idx, a.num_slots, a.dev_err) : -1;
   fence_async_smem();
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
-
-  if (a.fault_site == 1 && warp == 0) {
-    // test hook: warp 0 waits on a barrier that nothing arrives on
-    const bool ok = mbar_wait_bounded(bar_fault, 0, a.timeout_ns);
-    __syncwarp();
-    if (!ok && lane == 0) flag_error(a.dev_err, kDevTimeout);
-  }
 
   // softmax roles: group G owns heads [G*HPT, G*HPT + HPT); thread (quarter,
   // lane) owns key row r = quarter*32 + lane of each tile = TMEM lane r.
@@ -327,6 +338,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
   const int bar_group = 1 + G;
   float* red = red_all + G * 4 * HPT;
   const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+  // MMA issuers: lane 0 of warp 0 (issuer A) and of warp 1 (issuer B)
+  const bool issuer = (tid == 0 || tid == 32);
+  const int half = warp;                          // 0 = A, 1 = B (issuers only)
 
   // Running sum of p per head (fp32).  It normalizes O and gives lse; the
   // f16 rounding of p inside PV changes each weight by at most 2^-12.
@@ -334,6 +348,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
 #pragma unroll
   for (int h = 0; h < HPT; ++h) l_sum[h] = 0.0f;
   bool timed_out = false;
+  auto wait = [&](uint32_t bar, uint32_t parity) {
+    if (!mbar_wait_bounded(bar, parity, a.timeout_ns)) timed_out = true;
+  };
 
   // MMA descriptors: built once, advanced by adding 16-byte-unit offsets to
   // the start-address field (addresses stay below 2^18, so no carry).
@@ -343,45 +360,64 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
   const uint64_t desc_v = smem_desc(kv_addr, kChunkBytes, 1024, kSwizzle128);       // MN-major A
   const uint64_t desc_p = smem_desc(kv_addr + 8 * kChunkBytes, 8192, L::p_atom_bytes,
                                     L::p_swizzle_mode);                            // MN-major B
+  // QK k-steps [k0, k0 + n) into this issuer's partial sum (S_a for issuer
+  // A, S_b for issuer B); 'first' starts the sum.
+  auto issue_qk = [&](const int k0, const int n, const bool first) {
+    constexpr uint32_t idesc = idesc_f16(128, HG, false, false);
+#pragma unroll
+    for (int j = 0; j < n; ++j) {
+      const uint32_t kk = k0 + j;
+      const uint32_t c = kk >> 2, sub = kk & 3;
+      mma_f16kind(tmem + L::col_s + half * HG, desc_k + ((c * kChunkBytes + sub * 32) >> 4),
+                  desc_q + ((c * (HG * 128) + sub * 32) >> 4), idesc,
+                  (first && j == 0) ? 0u : 1u);
+    }
+  };
 
   // Rows of the next tile travel in registers: warp w holds rows 16w..16w+15
-  // as three 32-bit words per lane (latent lo, latent hi, scales/rope), so
-  // their HBM latency overlaps the MMAs and softmax of the current tile.
-  uint32_t wlo[16], whi[16], wex[16];
-  auto issue_row_loads = [&](const int32_t* slots) {
-    int32_t sv[16];
+  // as three 32-bit words per lane -- latent word wa(l), latent word wb(l),
+  // and word 64 + l (lanes 0..7: scales, 8..23: rope) -- where pass A
+  // covers slabs {0,1,4,5} and pass B slabs {2,3,6,7}:
+  //   wa(l) = l < 16 ? l : l + 16,   wb(l) = wa(l) + 16.
+  // Each group is reloaded for the next tile right after the pass that
+  // consumed it, so the gather is spread over the whole tile.
+  const int word_a = lane < 16 ? lane : lane + 16;
+  const int word_b = word_a + 16;
+  uint32_t wa[16], wb[16], wex[16];
+  int32_t sv[16];
+  auto load_slots = [&](const int32_t* slots) {
 #pragma unroll
     for (int i = 0; i < 16; i += 4) {
       const int4 t = *reinterpret_cast<const int4*>(slots + warp * 16 + i);
       sv[i] = t.x; sv[i + 1] = t.y; sv[i + 2] = t.z; sv[i + 3] = t.w;
     }
+  };
+  auto load_words = [&](uint32_t (&w)[16], int word, bool active) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-      const int32_t sl = sv[i];
-      if (sl >= 0) {
-        const uint32_t* row =
-            reinterpret_cast<const uint32_t*>(a.pool + static_cast<int64_t>(sl) * kRowBytes);
-        wlo[i] = __ldg(row + lane);
-        whi[i] = __ldg(row + 32 + lane);
-        wex[i] = lane < 24 ? __ldg(row + 64 + lane) : 0u;
-      } else {
-        wlo[i] = whi[i] = wex[i] = 0u;                   // masked key: zero row
-      }
+      const uint32_t* row =
+          reinterpret_cast<const uint32_t*>(a.pool + static_cast<int64_t>(sv[i]) * kRowBytes);
+      w[i] = (sv[i] >= 0 && active) ? __ldg(row + word) : 0u;    // masked key: zero row
     }
   };
-  if (my_tiles > 0) issue_row_loads(slot_s);
+  if (my_tiles > 0) {
+    load_slots(slot_s);
+    load_words(wa, word_a, true);
+    load_words(wb, word_b, true);
+    load_words(wex, 64 + lane, lane < 24);
+  }
 
-  // dequant store addresses: lane l writes latent units l%8 of slab l/8 (and
-  // slab 4 + l/8), lanes 8..23 rope half-units of slab 8; rows of this warp
-  // start at line 2*warp*1024.  Indexed by the row's r%8 (the swizzle phase).
-  const uint32_t scale_sel = dequant_scale_selector(lane);
-  uint32_t lat_base[8], rope_base[8];                 // shared-window addresses
+  // dequant store addresses (shared-window): latent word w of row r goes to
+  // slab w/8, unit (w%8) ^ (r%8) of the row's 128-byte line; rows of this
+  // warp start at line 2*warp*1024; indexed by r%8 (the swizzle phase).
+  uint32_t a_base[8], b_base[8], rope_base[8];
   {
-    const uint32_t kv = smem_addr(kv_s) + warp * 2048;
+    const uint32_t kv = kv_addr + warp * 2048;
     const uint32_t lr = (lane - 8) & 15;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      lat_base[j] = kv + (lane >> 3) * kChunkBytes + (((lane & 7) ^ j) << 4);
+      a_base[j] = kv + (word_a >> 3) * kChunkBytes + (((word_a & 7) ^ j) << 4);
+      b_base[j] = kv + (word_b >> 3) * kChunkBytes + (((word_b & 7) ^ j) << 4);
       rope_base[j] = kv + 8 * kChunkBytes + ((((lr >> 1) ^ j) << 4) | ((lr & 1) << 3));
     }
   }
@@ -389,6 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
   for (int it = 0; it < my_tiles; ++it) {
     const int tile = tile_begin + it;
     const int ring = it % 3;
+    const uint32_t par = it & 1;                 // phase parity of this tile's barriers
     // slot of key (tile + 2, row warp*16 + lane) for lanes 0..15, resolved in
     // three steps spread over this iteration (top-k load, page-table load,
     // slot) so that neither dependent load stalls the warp
@@ -397,46 +434,71 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
     int32_t idx_ahead = -1, page_ahead = -1, pi_ahead = -1;
     if (resolve_ahead && k_ahead < a.K) idx_ahead = __ldg(topk_row + k_ahead);
 
-    // ---- a3/a4: dequantize the tile into shared memory ----
+    // ---- a3/a4 in three passes, each into slabs that the previous tile's
+    // PV has released; QK starts on each part as soon as all warps wrote it.
+    // pass A: slabs 0,1 and 4,5 (PV slabs 0 and 2, which are issued first)
     if (it > 0) {
-      // the tile buffer (and O) are free once the previous PV is done
-      if (!mbar_wait_bounded(bar_mma, 1, a.timeout_ns)) timed_out = true;
+      wait(bar_pv0, par ^ 1);
+      wait(bar_pv0 + 16, par ^ 1);
       __syncwarp();
       tc_fence_after_sync();
     }
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      // row r = 16*warp + i: its 128-byte line in each slab is at
-      // (r/8)*1024 + (r%8)*128 and the 16-byte unit u sits at u ^ (r%8)
-      // (r%8 = i%8), so the addresses are per-lane constants plus immediates
-      const DequantRow d = dequant_row_words(wlo[i], whi[i], wex[i], lane, scale_sel);
-      const uint32_t line = (i >> 3) * 1024 + (i & 7) * 128;
-      st_shared_v4(lat_base[i & 7] + line, d.lat_lo);
-      st_shared_v4(lat_base[i & 7] + line + 4 * kChunkBytes, d.lat_hi);
-      if (lane >= 8 && lane < 24) st_shared_v2(rope_base[i & 7] + line, d.rope);
+    for (int i = 0; i < 16; ++i)
+      st_shared_v4(a_base[i & 7] + (i >> 3) * 1024 + (i & 7) * 128,
+                   dequant_latent_word(wa[i], wex[i], word_a));
+    fence_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar_part0);
+    if (it + 1 < my_tiles) {            // next tile: its slots, then word group a
+      load_slots(slot_s + ((it + 1) % 3) * 128);
+      load_words(wa, word_a, true);
+    }
+    if (issuer) {
+      wait(bar_part0, par);
+      tc_fence_after_sync();
+      issue_qk(half == 0 ? 0 : 16, 8, true);       // slabs 0,1 (A) / 4,5 (B)
+    }
+    __syncwarp();
+    // pass B: slabs 2,3 and 6,7 (PV slabs 1 and 3; PV is then complete)
+    if (it > 0) {
+      wait(bar_pv0 + 8, par ^ 1);
+      wait(bar_pv0 + 24, par ^ 1);
+      __syncwarp();
+      tc_fence_after_sync();
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      st_shared_v4(b_base[i & 7] + (i >> 3) * 1024 + (i & 7) * 128,
+                   dequant_latent_word(wb[i], wex[i], word_b));
+    fence_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar_part0 + 8);
+    if (it + 1 < my_tiles) load_words(wb, word_b, true);
+    if (issuer) {
+      wait(bar_part0 + 8, par);
+      tc_fence_after_sync();
+      issue_qk(half == 0 ? 8 : 24, 8, false);      // slabs 2,3 (A) / 6,7 (B)
+    }
+    __syncwarp();
+    // pass C: rope -> slab 8 (the previous tile's P lived there; PV is done)
+    if (lane >= 8 && lane < 24) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        st_shared_v2(rope_base[i & 7] + (i >> 3) * 1024 + (i & 7) * 128, dequant_rope(wex[i]));
     }
     fence_async_smem();
-    __syncthreads();
-
-    // ---- a5: S^T = K_tile . Q^T, issued by two threads (one MMA stream
-    // cannot keep the tensor core busy at N = HG): thread 0 sums k-steps
-    // 0..17 into S_a, thread 32 k-steps 18..35 into S_b ----
-    if (tid == 0 || tid == 32) {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar_part0 + 16);
+    if (it + 1 < my_tiles) load_words(wex, 64 + lane, lane < 24);
+    if (issuer) {
+      wait(bar_part0 + 16, par);
       tc_fence_after_sync();
-      constexpr uint32_t idesc = idesc_f16(128, HG, false, false);
-      const int half = tid >> 5;
-#pragma unroll
-      for (int j = 0; j < 18; ++j) {
-        const uint32_t kk = half * 18 + j;
-        const uint32_t c = kk >> 2, sub = kk & 3;
-        mma_f16kind(tmem + L::col_s + half * HG, desc_k + ((c * kChunkBytes + sub * 32) >> 4),
-                    desc_q + ((c * (HG * 128) + sub * 32) >> 4), idesc, j > 0 ? 1u : 0u);
-      }
-      mma_commit(bar_mma);
+      issue_qk(32 + 2 * half, 2, false);           // rope
+      mma_commit(bar_qk);
     }
-    // ---- a3: the next tile's gather runs under the QK MMAs (its slots were
-    // resolved earlier); the warps would otherwise wait for QK here
-    if (it + 1 < my_tiles) issue_row_loads(slot_s + ((it + 1) % 3) * 128);
+    __syncwarp();
+
     // ---- a2, second step: page-table entry of the key two tiles ahead
     if (resolve_ahead) {
       pi_ahead = slot_page_index(idx_ahead, l_eff, a.pt_stride, a.dev_err);
@@ -445,7 +507,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
 
     // ---- a6: online softmax (two head groups) ----
     {
-      if (!mbar_wait_bounded(bar_mma, 0, a.timeout_ns)) timed_out = true;   // QK done
+      wait(bar_qk, par);               // QK done
       __syncwarp();                    // lanes may leave the wait at different times
       tc_fence_after_sync();
       const bool valid = slot_s[ring * 128 + r_key] >= 0;
@@ -526,29 +588,30 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
     }
     __syncthreads();
 
-    // ---- a7: O^T += V^T . P^T; thread 0 issues slabs 0-1, thread 32 slabs
-    // 2-3 (k-steps outer, so consecutive MMAs go to different accumulators)
-    if (tid == 0 || tid == 32) {
+    // ---- a7: O^T += V^T . P^T; issuer A takes slabs 0 then 1, issuer B
+    // slabs 2 then 3, each slab (128 latent columns) committed on its own so
+    // the next tile's dequant can reuse its shared memory as early as possible
+    if (issuer) {
       tc_fence_after_sync();
       constexpr uint32_t idesc = idesc_f16(128, HG, true, true);
-      const int half = tid >> 5;
 #pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
+      for (int j = 0; j < 2; ++j) {
+        const int mb = 2 * half + j;
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          const int mb = 2 * half + j;
+        for (int ks = 0; ks < 8; ++ks)
           mma_f16kind(tmem + L::col_o + mb * HG,
                       desc_v + (((2 * mb) * kChunkBytes + (2 * ks) * 1024) >> 4),
                       desc_p + (((2 * ks) * L::p_atom_bytes) >> 4), idesc,
                       (it > 0 || ks > 0) ? 1u : 0u);
-        }
+        mma_commit(bar_pv0 + 8 * mb);
       }
-      mma_commit(bar_mma);
     }
+    __syncwarp();
   }
   // the last PV must be complete before O is read or TMEM is freed
   if (my_tiles > 0) {
-    if (!mbar_wait_bounded(bar_mma, 1, a.timeout_ns)) timed_out = true;
+    const uint32_t last = (my_tiles - 1) & 1;
+    for (int p = 0; p < 4; ++p) wait(bar_pv0 + 8 * p, last);
     __syncwarp();
     tc_fence_after_sync();
   }
@@ -589,6 +652,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
       if (partial) a.ws_o[(part * HG + h) * kLatent + d] = v;
       else static_cast<__nv_bfloat16*>(a.out)[(out_head0 + h) * kLatent + d] = __float2bfloat16_rn(v);
     }
+  }
+  if (a.fault_site == 1 && warp == 0) {
+    // test hook, after all work of the block: warp 0 waits on a barrier that
+    // nothing arrives on, so the wait runs out and reports a timeout
+    const bool ok = mbar_wait_bounded(bar_fault, 0, a.timeout_ns);
+    __syncwarp();
+    if (!ok) timed_out = true;
   }
   if (timed_out) flag_error(a.dev_err, kDevTimeout);
   tc_fence_before_sync();
