@@ -7,8 +7,8 @@
 //
 // Work unit: one thread block per (request b, draft token s, head group g,
 // split).  A head group holds HG = min(H, 64) query heads, which all share
-// every gathered row.  The block (8 warps) walks its share of the top-k list
-// in tiles of 128 keys:
+// every gathered row.  The block (8 compute warps and one MMA-issue
+// warpgroup) walks its share of the top-k list in tiles of 128 keys:
 //   a2     slots are resolved two tiles ahead (top-k -> page table -> slot),
 //          each dependent load spread over a tile's work
 //   a3     each warp gathers 16 rows of the next tile into registers (three
@@ -19,19 +19,20 @@
 //          0..255, latent 256..511, rope -- each into the slabs that the
 //          previous tile's PV has already released; q is converted to f16
 //          with a per-head power-of-two scale folded into the score scale
-//   a5     as each pass lands, lane 0 of warps 0 and 1 issue its share of
+//   a5     as each pass lands, lane 0 of warps 8..11 issue its share of
 //          S^T[128 x HG] = K_tile . Q^T on tcgen05 (M = 128 keys, N = HG,
-//          K = 576) into two fp32 TMEM accumulators
-//   a6     the 8 warps read S from TMEM (one key per thread; warps 0..3 take
-//          the first half of the heads, warps 4..7 the second half) and run
-//          the online softmax in base 2; the running maximum is only raised
+//          K = 576) into four fp32 TMEM accumulators
+//   a6     the 8 compute warps read S from TMEM (one key per thread; warps
+//          0..3 take the first half of the heads, warps 4..7 the second
+//          half) and run the online softmax in base 2; the running maximum
+//          is only raised
 //          when a score exceeds it by more than 8 (so most tiles need no
 //          cross-thread reduction and no rescale), p is rounded to f16 and
 //          written as the PV operand over the tile's rope columns, which
 //          QK^T no longer needs
-//   a7     the two issuers run O^T[512 x HG] += V^T . P^T (slabs 0-1 and 2-3
+//   a7     two issuers run O^T[512 x HG] += V^T . P^T (slabs 0-1 and 2-3
 //          of the latent columns; V^T is the same shared-memory tile read as
-//          an MN-major operand) and signal each half's release
+//          an MN-major operand) and signal each 128-column slab's release
 //   a8     epilogue: O / sum(p) -> bf16 out, lse = ln 2 * (m + log2 sum(p));
 //          with several splits the normalized partial (o, lse) goes to the
 //          workspace and
@@ -45,8 +46,21 @@
 namespace kv4 {
 namespace {
 
-constexpr int kThreads = 256;            // 8 warps: gather, dequant, softmax; thread 0 issues MMAs
-constexpr float kRaiseThreshold = 8.0f;  // log2 units: p <= 256 between raises
+// Block: warpgroups 0 and 1 (8 compute warps) gather, dequantize, run the
+// softmax and the epilogue; warpgroup 2 issues the MMAs (lane 0 of warps 8
+// and 9), so that no compute warp ever stalls behind the tensor-core queue.
+// Registers are moved from the issue warpgroup to the compute warpgroups
+// with setmaxnreg; per SM sub-partition (one warp of each warpgroup) that is
+// 2 x 232 + 40 = 504 of the 3 x 168 the block is launched with.
+constexpr int kComputeWarps = 8;
+constexpr int kComputeThreads = 32 * kComputeWarps;
+constexpr int kThreads = kComputeThreads + 128;
+constexpr int kLaunchRegs = 168;          // 65536 / 384, rounded down to a multiple of 8
+constexpr uint32_t kComputeRegs = 232;
+constexpr uint32_t kIssueRegs = 40;
+static_assert(2 * kComputeRegs + kIssueRegs <= 3 * kLaunchRegs, "register split exceeds the launch");
+constexpr int kBarCompute = 3;            // named barrier of the 256 compute threads (1, 2: softmax groups)
+constexpr float kRaiseThreshold = 8.0f;   // log2 units: p <= 256 between raises
 
 template <int HG>
 struct Layout {
@@ -56,7 +70,7 @@ struct Layout {
   static constexpr uint32_t kv_bytes = 9u * kChunkBytes;              // K/V tile
   static constexpr uint32_t ctl_off = kv_off + kv_bytes;
   // control block
-  static constexpr uint32_t bar_off = ctl_off;                        // uint64 x 9
+  static constexpr uint32_t bar_off = ctl_off;                        // uint64 x 10
   static constexpr uint32_t tmem_off = ctl_off + 80;                  // uint32
   static constexpr uint32_t slot_off = ctl_off + 96;                  // int32 [3][128]
   static constexpr uint32_t mref_off = slot_off + 3 * 128 * 4;        // float [HG]
@@ -66,9 +80,9 @@ struct Layout {
   static constexpr uint32_t qscale_off = lsum_off + 2 * HG * 4;       // float [HG]
   static constexpr uint32_t end = qscale_off + HG * 4;
   static constexpr uint32_t smem_bytes = end + 1024;                  // + alignment slack
-  // tensor memory: O^T slabs at columns [0, 4HG); S^T as two partial sums
-  // (one per MMA issuer) at [4HG, 5HG) and [5HG, 6HG)
-  static constexpr uint32_t tmem_cols = (6 * HG <= 128) ? 128 : (6 * HG <= 256 ? 256 : 512);
+  // tensor memory: O^T slabs at columns [0, 4HG); S^T as four partial sums
+  // (one per QK issuer) at [4HG + i HG, 5HG + i HG)
+  static constexpr uint32_t tmem_cols = (8 * HG <= 128) ? 128 : (8 * HG <= 256 ? 256 : 512);
   static constexpr uint32_t col_o = 0;
   static constexpr uint32_t col_s = 4 * HG;
   // P^T operand (MN-major, N = HG): one swizzle atom per 8 keys
@@ -160,7 +174,8 @@ __device__ __forceinline__ void tmem_load_cols(uint32_t taddr, float (&x)[N]) {
   }
 }
 
-// Scores: the sum of the two partial S^T accumulators (columns c and c + gap).
+// Scores: the sum of the four partial S^T accumulators (columns c + i gap),
+// added as (S0 + S1) + (S2 + S3).
 template <int N>
 __device__ __forceinline__ void load_scores(uint32_t taddr, uint32_t gap, float (&x)[N]) {
   __syncwarp();
@@ -169,12 +184,17 @@ __device__ __forceinline__ void load_scores(uint32_t taddr, uint32_t gap, float 
     tmem_ld32x2_sync(taddr, taddr + gap, va, vb);
 #pragma unroll
     for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(va[j]) + __uint_as_float(vb[j]);
+    tmem_ld32x2_sync(taddr + 2 * gap, taddr + 3 * gap, va, vb);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) x[j] += __uint_as_float(va[j]) + __uint_as_float(vb[j]);
   } else {
-    float y[N];
+    float y[N], z[N], u[N];
     tmem_load_cols<N>(taddr, x);
     tmem_load_cols<N>(taddr + gap, y);
+    tmem_load_cols<N>(taddr + 2 * gap, z);
+    tmem_load_cols<N>(taddr + 3 * gap, u);
 #pragma unroll
-    for (int j = 0; j < N; ++j) x[j] += y[j];
+    for (int j = 0; j < N; ++j) x[j] = (x[j] + y[j]) + (z[j] + u[j]);
   }
 }
 
@@ -238,14 +258,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
 
   uint8_t* q_s = smem;
   uint8_t* kv_s = smem + L::kv_off;
-  // mbarriers: QK done (both issuers commit), PV done per 128-column slab of
-  // O (slabs 0-1 from issuer A, 2-3 from issuer B), tile parts written by all
-  // 8 warps (latent group a, latent group b, rope), and the test hook's one.
+  // mbarriers: QK done (all four issuers commit), PV done per 128-column
+  // slab of O (slabs 0-1 from issuer 0, 2-3 from issuer 1), tile parts
+  // written by the 8 compute warps (latent group a, latent group b, rope), P
+  // written, and the test hook's one.
   const uint32_t bars = smem_addr(smem + L::bar_off);
   const uint32_t bar_qk = bars;
   const uint32_t bar_pv0 = bars + 8;              // + 8 * slab: PV slab (128 columns) done
   const uint32_t bar_part0 = bars + 40;           // + 8 * part: tile part written
-  const uint32_t bar_fault = bars + 64;
+  const uint32_t bar_p = bars + 64;
+  const uint32_t bar_fault = bars + 72;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::tmem_off);
   int32_t* slot_s = reinterpret_cast<int32_t*>(smem + L::slot_off);
   float* m_ref = reinterpret_cast<float*>(smem + L::mref_off);
@@ -255,11 +277,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
   float* qscale = reinterpret_cast<float*>(smem + L::qscale_off);
 
   // ---- prologue ------------------------------------------------------------
-  if (warp == 0) tmem_alloc(smem_addr(tmem_slot), L::tmem_cols);
-  if (tid == 32) {
-    mbar_init(bar_qk, 2);
+  if (warp == kComputeWarps) tmem_alloc(smem_addr(tmem_slot), L::tmem_cols);
+  if (tid == 32 * (kComputeWarps + 1)) {
+    mbar_init(bar_qk, 4);
     for (int p = 0; p < 4; ++p) mbar_init(bar_pv0 + 8 * p, 1);
-    for (int p = 0; p < 3; ++p) mbar_init(bar_part0 + 8 * p, 8);
+    for (int p = 0; p < 3; ++p) mbar_init(bar_part0 + 8 * p, kComputeWarps);
+    mbar_init(bar_p, 1);
     mbar_init(bar_fault, 1);
     fence_mbar_init();
   }
@@ -269,7 +292,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
   int32_t pro_idx = -1, pro_page = -1, pro_pi = -1;
   const int pro_t = tid >> 7, pro_r = tid & 127;
   const int pro_k = (tile_begin + pro_t) * kTileKeys + pro_r;
-  if (pro_t < my_tiles && pro_k < a.K) pro_idx = __ldg(topk_row + pro_k);
+  const bool pro_on = tid < kComputeThreads && pro_t < my_tiles;
+  if (pro_on && pro_k < a.K) pro_idx = __ldg(topk_row + pro_k);
   // Q rows of this head group -> f16, 128-byte-swizzled K-major operand.
   // Each head is scaled by 2^-e_h (exact) so that its largest magnitude lies
   // in [2^14, 2^15): every bf16 element then converts to f16 without loss
@@ -293,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
       for (int k = 0; k < 4; ++k)
         m = max(m, max((w[k] << 16) & 0x7FFFFFFFu, w[k] & 0x7FFF0000u));   // |bf16| as fp32 bits
     }
-    if (pro_t < my_tiles) {                        // second step of the slot lookup
+    if (pro_on) {                                  // second step of the slot lookup
       pro_pi = slot_page_index(pro_idx, l_eff, a.pt_stride, a.dev_err);
       if (pro_pi >= 0) pro_page = __ldg(pt_row + pro_pi);
     }
@@ -320,7 +344,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
       }
     }
   }
-  if (pro_t < my_tiles)
+  if (pro_on)
     slot_s[pro_t * 128 + pro_r] =
         pro_pi >= 0 ? slot_from_page(pro_page, pro_idx, a.num_slots, a.dev_err) : -1;
   fence_async_smem();
@@ -328,342 +352,349 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
-
-  // softmax roles: group G owns heads [G*HPT, G*HPT + HPT); thread (quarter,
-  // lane) owns key row r = quarter*32 + lane of each tile = TMEM lane r.
-  const int G = warp >> 2;
-  const int quarter = warp & 3;
-  const int r_key = quarter * 32 + lane;
-  const int h0 = G * HPT;
-  const int bar_group = 1 + G;
-  float* red = red_all + G * 4 * HPT;
-  const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-  // MMA issuers: lane 0 of warp 0 (issuer A) and of warp 1 (issuer B)
-  const bool issuer = (tid == 0 || tid == 32);
-  const int half = warp;                          // 0 = A, 1 = B (issuers only)
-
-  // Running sum of p per head (fp32).  It normalizes O and gives lse; the
-  // f16 rounding of p inside PV changes each weight by at most 2^-12.
-  float l_sum[HPT];
-#pragma unroll
-  for (int h = 0; h < HPT; ++h) l_sum[h] = 0.0f;
   bool timed_out = false;
   auto wait = [&](uint32_t bar, uint32_t parity) {
     if (!mbar_wait_bounded(bar, parity, a.timeout_ns)) timed_out = true;
   };
-
-  // MMA descriptors: built once, advanced by adding 16-byte-unit offsets to
-  // the start-address field (addresses stay below 2^18, so no carry).
   const uint32_t kv_addr = smem_addr(kv_s);
-  const uint64_t desc_k = smem_desc(kv_addr, 16, 1024, kSwizzle128);                // K-major A
-  const uint64_t desc_q = smem_desc(smem_addr(q_s), 16, 1024, kSwizzle128);         // K-major B
-  const uint64_t desc_v = smem_desc(kv_addr, kChunkBytes, 1024, kSwizzle128);       // MN-major A
-  const uint64_t desc_p = smem_desc(kv_addr + 8 * kChunkBytes, 8192, L::p_atom_bytes,
-                                    L::p_swizzle_mode);                            // MN-major B
-  // QK k-steps [k0, k0 + n) into this issuer's partial sum (S_a for issuer
-  // A, S_b for issuer B); 'first' starts the sum.
-  auto issue_qk = [&](const int k0, const int n, const bool first) {
-    constexpr uint32_t idesc = idesc_f16(128, HG, false, false);
-#pragma unroll
-    for (int j = 0; j < n; ++j) {
-      const uint32_t kk = k0 + j;
-      const uint32_t c = kk >> 2, sub = kk & 3;
-      mma_f16kind(tmem + L::col_s + half * HG, desc_k + ((c * kChunkBytes + sub * 32) >> 4),
-                  desc_q + ((c * (HG * 128) + sub * 32) >> 4), idesc,
-                  (first && j == 0) ? 0u : 1u);
-    }
-  };
 
-  // Rows of the next tile travel in registers: warp w holds rows 16w..16w+15
-  // as three 32-bit words per lane -- latent word wa(l), latent word wb(l),
-  // and word 64 + l (lanes 0..7: scales, 8..23: rope) -- where pass A
-  // covers slabs {0,1,4,5} and pass B slabs {2,3,6,7}:
-  //   wa(l) = l < 16 ? l : l + 16,   wb(l) = wa(l) + 16.
-  // Each group is reloaded for the next tile right after the pass that
-  // consumed it, so the gather is spread over the whole tile.
-  const int word_a = lane < 16 ? lane : lane + 16;
-  const int word_b = word_a + 16;
-  uint32_t wa[16], wb[16], wex[16];
-  int32_t sv[16];
-  auto load_slots = [&](const int32_t* slots) {
-#pragma unroll
-    for (int i = 0; i < 16; i += 4) {
-      const int4 t = *reinterpret_cast<const int4*>(slots + warp * 16 + i);
-      sv[i] = t.x; sv[i + 1] = t.y; sv[i + 2] = t.z; sv[i + 3] = t.w;
-    }
-  };
-  auto load_words = [&](uint32_t (&w)[16], int word, bool active) {
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const uint32_t* row =
-          reinterpret_cast<const uint32_t*>(a.pool + static_cast<int64_t>(sv[i]) * kRowBytes);
-      w[i] = (sv[i] >= 0 && active) ? __ldg(row + word) : 0u;    // masked key: zero row
-    }
-  };
-  if (my_tiles > 0) {
-    load_slots(slot_s);
-    load_words(wa, word_a, true);
-    load_words(wb, word_b, true);
-    load_words(wex, 64 + lane, lane < 24);
-  }
-
-  // dequant store addresses (shared-window): latent word w of row r goes to
-  // slab w/8, unit (w%8) ^ (r%8) of the row's 128-byte line; rows of this
-  // warp start at line 2*warp*1024; indexed by r%8 (the swizzle phase).
-  uint32_t a_base[8], b_base[8], rope_base[8];
-  {
-    const uint32_t kv = kv_addr + warp * 2048;
-    const uint32_t lr = (lane - 8) & 15;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      a_base[j] = kv + (word_a >> 3) * kChunkBytes + (((word_a & 7) ^ j) << 4);
-      b_base[j] = kv + (word_b >> 3) * kChunkBytes + (((word_b & 7) ^ j) << 4);
-      rope_base[j] = kv + 8 * kChunkBytes + ((((lr >> 1) ^ j) << 4) | ((lr & 1) << 3));
-    }
-  }
-
-  for (int it = 0; it < my_tiles; ++it) {
-    const int tile = tile_begin + it;
-    const int ring = it % 3;
-    const uint32_t par = it & 1;                 // phase parity of this tile's barriers
-    // slot of key (tile + 2, row warp*16 + lane) for lanes 0..15, resolved in
-    // three steps spread over this iteration (top-k load, page-table load,
-    // slot) so that neither dependent load stalls the warp
-    const bool resolve_ahead = (it + 2 < my_tiles) && lane < 16;
-    const int k_ahead = (tile + 2) * kTileKeys + warp * 16 + lane;
-    int32_t idx_ahead = -1, page_ahead = -1, pi_ahead = -1;
-    if (resolve_ahead && k_ahead < a.K) idx_ahead = __ldg(topk_row + k_ahead);
-
-    // ---- a3/a4 in three passes, each into slabs that the previous tile's
-    // PV has released; QK starts on each part as soon as all warps wrote it.
-    // pass A: slabs 0,1 and 4,5 (PV slabs 0 and 2, which are issued first)
-    if (it > 0) {
-      wait(bar_pv0, par ^ 1);
-      wait(bar_pv0 + 16, par ^ 1);
-      __syncwarp();
-      tc_fence_after_sync();
-    }
-#pragma unroll
-    for (int i = 0; i < 16; ++i)
-      st_shared_v4(a_base[i & 7] + (i >> 3) * 1024 + (i & 7) * 128,
-                   dequant_latent_word(wa[i], wex[i], word_a));
-    fence_async_smem();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(bar_part0);
-    if (it + 1 < my_tiles) {            // next tile: its slots, then word group a
-      load_slots(slot_s + ((it + 1) % 3) * 128);
-      load_words(wa, word_a, true);
-    }
-    if (issuer) {
-      wait(bar_part0, par);
-      tc_fence_after_sync();
-      issue_qk(half == 0 ? 0 : 16, 8, true);       // slabs 0,1 (A) / 4,5 (B)
+  if (warp >= kComputeWarps) {
+    // ==== MMA issue warpgroup: lane 0 of each of its warps is an issuer ====
+    // A thread's MMAs run one after another, each fetching fresh operands,
+    // so QK is spread over four issuers (four partial sums of S^T) and PV
+    // over two (issuer 0: O slabs 0 then 1, issuer 1: slabs 2 then 3, so
+    // that slabs 0 and 2 are released half way through).
+    setmaxnreg_dec<kIssueRegs>();
+    if (lane == 0) {
+      const int qi = warp - kComputeWarps;         // issuer 0..3
+      // descriptors built once, advanced by adding 16-byte-unit offsets to the
+      // start-address field (addresses stay below 2^18, so no carry)
+      const uint64_t desc_k = smem_desc(kv_addr, 16, 1024, kSwizzle128);             // K-major A
+      const uint64_t desc_q = smem_desc(smem_addr(q_s), 16, 1024, kSwizzle128);      // K-major B
+      const uint64_t desc_v = smem_desc(kv_addr, kChunkBytes, 1024, kSwizzle128);    // MN-major A
+      const uint64_t desc_p = smem_desc(kv_addr + 8 * kChunkBytes, 8192, L::p_atom_bytes,
+                                        L::p_swizzle_mode);                         // MN-major B
+      // QK k-steps [k0, k0 + n) (16 columns each; chunk = k-step / 4) into
+      // this issuer's partial sum; 'first' starts the sum.
+      auto issue_qk = [&](const int k0, const int n, const bool first) {
+        constexpr uint32_t idesc = idesc_f16(128, HG, false, false);
+#pragma unroll 1
+        for (int j = 0; j < n; ++j) {
+          const uint32_t kk = k0 + j;
+          const uint32_t c = kk >> 2, sub = kk & 3;
+          mma_f16kind(tmem + L::col_s + qi * HG, desc_k + ((c * kChunkBytes + sub * 32) >> 4),
+                      desc_q + ((c * (HG * 128) + sub * 32) >> 4), idesc,
+                      (first && j == 0) ? 0u : 1u);
+        }
+      };
+      // latent chunk of each pass for this issuer: pass a writes chunks
+      // 0, 1, 4, 5 and pass b chunks 2, 3, 6, 7
+      const int chunk_a = (qi & 1) + 4 * (qi >> 1);
+      const int chunk_b = chunk_a + 2;
+      for (int it = 0; it < my_tiles; ++it) {
+        const uint32_t par = it & 1;
+        // a5: each part of S^T = K_tile . Q^T as soon as the compute warps wrote it
+        wait(bar_part0, par);
+        tc_fence_after_sync();
+        issue_qk(4 * chunk_a, 4, true);
+        wait(bar_part0 + 8, par);
+        tc_fence_after_sync();
+        issue_qk(4 * chunk_b, 4, false);
+        wait(bar_part0 + 16, par);
+        tc_fence_after_sync();
+        issue_qk(32 + qi, 1, false);                 // rope: one 16-column step each
+        mma_commit(bar_qk);
+        if (qi >= 2) continue;
+        // a7: O^T += V^T . P^T; issuer 0 takes O slabs 0 then 1, issuer 1
+        // slabs 2 then 3, each committed on its own so that the next tile's
+        // dequantization can reuse its shared memory as early as possible
+        wait(bar_p, par);
+        tc_fence_after_sync();
+        constexpr uint32_t idesc = idesc_f16(128, HG, true, true);
+#pragma unroll 1
+        for (int j = 0; j < 2; ++j) {
+          const int mb = 2 * qi + j;
+#pragma unroll 1
+          for (int ks = 0; ks < 8; ++ks)
+            mma_f16kind(tmem + L::col_o + mb * HG,
+                        desc_v + (((2 * mb) * kChunkBytes + (2 * ks) * 1024) >> 4),
+                        desc_p + (((2 * ks) * L::p_atom_bytes) >> 4), idesc,
+                        (it > 0 || ks > 0) ? 1u : 0u);
+          mma_commit(bar_pv0 + 8 * mb);
+        }
+      }
     }
     __syncwarp();
-    // pass B: slabs 2,3 and 6,7 (PV slabs 1 and 3; PV is then complete)
-    if (it > 0) {
-      wait(bar_pv0 + 8, par ^ 1);
-      wait(bar_pv0 + 24, par ^ 1);
-      __syncwarp();
-      tc_fence_after_sync();
-    }
+  } else {
+    // ==== compute warpgroups (warps 0..7) ====
+    setmaxnreg_inc<kComputeRegs>();
+
+    // softmax roles: group G owns heads [G*HPT, G*HPT + HPT); thread (quarter,
+    // lane) owns key row r = quarter*32 + lane of each tile = TMEM lane r.
+    const int G = warp >> 2;
+    const int quarter = warp & 3;
+    const int r_key = quarter * 32 + lane;
+    const int h0 = G * HPT;
+    const int bar_group = 1 + G;
+    float* red = red_all + G * 4 * HPT;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    // Running sum of p per head (fp32).  It normalizes O and gives lse; the
+    // f16 rounding of p inside PV changes each weight by at most 2^-12.
+    float l_sum[HPT];
 #pragma unroll
-    for (int i = 0; i < 16; ++i)
-      st_shared_v4(b_base[i & 7] + (i >> 3) * 1024 + (i & 7) * 128,
-                   dequant_latent_word(wb[i], wex[i], word_b));
-    fence_async_smem();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(bar_part0 + 8);
-    if (it + 1 < my_tiles) load_words(wb, word_b, true);
-    if (issuer) {
-      wait(bar_part0 + 8, par);
-      tc_fence_after_sync();
-      issue_qk(half == 0 ? 8 : 24, 8, false);      // slabs 2,3 (A) / 6,7 (B)
+    for (int h = 0; h < HPT; ++h) l_sum[h] = 0.0f;
+    // Rows of the next tile travel in registers: warp w holds rows 16w..16w+15
+    // as three 32-bit words per lane -- latent word wa(l), latent word wb(l),
+    // and word 64 + l (lanes 0..7: scales, 8..23: rope) -- where pass A
+    // covers slabs {0,1,4,5} and pass B slabs {2,3,6,7}:
+    //   wa(l) = l < 16 ? l : l + 16,   wb(l) = wa(l) + 16.
+    // Each group is reloaded for the next tile right after the pass that
+    // consumed it, so the gather is spread over the whole tile.
+    const int word_a = lane < 16 ? lane : lane + 16;
+    const int word_b = word_a + 16;
+    uint32_t wa[16], wb[16], wex[16];
+    // one word of each of this warp's 16 rows of the tile whose slots are
+    // at `slots` (the slots are re-read from shared memory for every group,
+    // so that they hold no registers across the tile)
+    auto load_words = [&](uint32_t (&w)[16], const int32_t* slots, int word, bool active) {
+      int32_t sv[16];
+#pragma unroll
+      for (int i = 0; i < 16; i += 4) {
+        const int4 t = *reinterpret_cast<const int4*>(slots + warp * 16 + i);
+        sv[i] = t.x; sv[i + 1] = t.y; sv[i + 2] = t.z; sv[i + 3] = t.w;
+      }
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const uint32_t* row =
+            reinterpret_cast<const uint32_t*>(a.pool + static_cast<int64_t>(sv[i]) * kRowBytes);
+        w[i] = (sv[i] >= 0 && active) ? __ldg(row + word) : 0u;    // masked key: zero row
+      }
+    };
+    if (my_tiles > 0) {
+      load_words(wa, slot_s, word_a, true);
+      load_words(wb, slot_s, word_b, true);
+      load_words(wex, slot_s, 64 + lane, lane < 24);
     }
-    __syncwarp();
-    // pass C: rope -> slab 8 (the previous tile's P lived there; PV is done)
-    if (lane >= 8 && lane < 24) {
+
+    // dequant store addresses (shared-window): latent word w of row r goes to
+    // slab w/8, unit (w%8) ^ (r%8) of the row's 128-byte line; rows of this
+    // warp start at line 2*warp*1024; indexed by r%8 (the swizzle phase).
+    uint32_t a_base[8], b_base[8], rope_base[8];
+    {
+      const uint32_t kv = kv_addr + warp * 2048;
+      const uint32_t lr = (lane - 8) & 15;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        a_base[j] = kv + (word_a >> 3) * kChunkBytes + (((word_a & 7) ^ j) << 4);
+        b_base[j] = kv + (word_b >> 3) * kChunkBytes + (((word_b & 7) ^ j) << 4);
+        rope_base[j] = kv + 8 * kChunkBytes + ((((lr >> 1) ^ j) << 4) | ((lr & 1) << 3));
+      }
+    }
+
+    for (int it = 0; it < my_tiles; ++it) {
+      const int tile = tile_begin + it;
+      const int ring = it % 3;
+      const int32_t* next_slots = slot_s + ((it + 1) % 3) * 128;
+      const uint32_t par = it & 1;                 // phase parity of this tile's barriers
+      // slot of key (tile + 2, row warp*16 + lane) for lanes 0..15, resolved in
+      // three steps spread over this iteration (top-k load, page-table load,
+      // slot) so that neither dependent load stalls the warp
+      const bool resolve_ahead = (it + 2 < my_tiles) && lane < 16;
+      const int k_ahead = (tile + 2) * kTileKeys + warp * 16 + lane;
+      int32_t idx_ahead = -1, page_ahead = -1, pi_ahead = -1;
+      if (resolve_ahead && k_ahead < a.K) idx_ahead = __ldg(topk_row + k_ahead);
+
+      // ---- a3/a4 in three passes, each into slabs that the previous tile's
+      // PV has released; QK starts on each part as soon as all warps wrote it.
+      // pass A: slabs 0,1 and 4,5 (PV slabs 0 and 2, which are issued first)
+      if (it > 0) {
+        wait(bar_pv0, par ^ 1);
+        wait(bar_pv0 + 16, par ^ 1);
+        __syncwarp();
+        tc_fence_after_sync();
+      }
 #pragma unroll
       for (int i = 0; i < 16; ++i)
-        st_shared_v2(rope_base[i & 7] + (i >> 3) * 1024 + (i & 7) * 128, dequant_rope(wex[i]));
-    }
-    fence_async_smem();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(bar_part0 + 16);
-    if (it + 1 < my_tiles) load_words(wex, 64 + lane, lane < 24);
-    if (issuer) {
-      wait(bar_part0 + 16, par);
-      tc_fence_after_sync();
-      issue_qk(32 + 2 * half, 2, false);           // rope
-      mma_commit(bar_qk);
-    }
-    __syncwarp();
-
-    // ---- a2, second step: page-table entry of the key two tiles ahead
-    if (resolve_ahead) {
-      pi_ahead = slot_page_index(idx_ahead, l_eff, a.pt_stride, a.dev_err);
-      if (pi_ahead >= 0) page_ahead = __ldg(pt_row + pi_ahead);
-    }
-
-    // ---- a6: online softmax (two head groups) ----
-    {
-      wait(bar_qk, par);               // QK done
-      __syncwarp();                    // lanes may leave the wait at different times
-      tc_fence_after_sync();
-      const bool valid = slot_s[ring * 128 + r_key] >= 0;
-      // x = log2-domain score relative to the head's reference maximum
-      float x[HPT], c[HPT], mr[HPT];
-      load_scores<HPT>(lane_base + L::col_s + h0, HG, x);
-      lds_vec<HPT>(qscale + h0, c);
-      lds_vec<HPT>(m_ref + h0, mr);
-      float xmax = -INFINITY;
-#pragma unroll
-      for (int h = 0; h < HPT; ++h) {
-        x[h] = fmaf(x[h], c[h], -mr[h]);
-        xmax = fmaxf(xmax, x[h]);
+        st_shared_v4(a_base[i & 7] + (i >> 3) * 1024 + (i & 7) * 128,
+                     dequant_latent_word(wa[i], wex[i], word_a));
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_part0);
+      if (it + 1 < my_tiles) load_words(wa, next_slots, word_a, true);   // next tile
+      // pass B: slabs 2,3 and 6,7 (PV slabs 1 and 3; PV is then complete)
+      if (it > 0) {
+        wait(bar_pv0 + 8, par ^ 1);
+        wait(bar_pv0 + 24, par ^ 1);
+        __syncwarp();
+        tc_fence_after_sync();
       }
-      const bool need = named_sync_or(bar_group, 128, valid && xmax > kRaiseThreshold);
-      if (need) {
-        // (rare) raise the reference maximum of every head to its tile maximum
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        st_shared_v4(b_base[i & 7] + (i >> 3) * 1024 + (i & 7) * 128,
+                     dequant_latent_word(wb[i], wex[i], word_b));
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_part0 + 8);
+      if (it + 1 < my_tiles) load_words(wb, next_slots, word_b, true);
+      // pass C: rope -> slab 8 (the previous tile's P lived there; PV is done)
+      if (lane >= 8 && lane < 24) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          st_shared_v2(rope_base[i & 7] + (i >> 3) * 1024 + (i & 7) * 128, dequant_rope(wex[i]));
+      }
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_part0 + 16);
+      if (it + 1 < my_tiles) load_words(wex, next_slots, 64 + lane, lane < 24);
+
+      // ---- a2, second step: page-table entry of the key two tiles ahead
+      if (resolve_ahead) {
+        pi_ahead = slot_page_index(idx_ahead, l_eff, a.pt_stride, a.dev_err);
+        if (pi_ahead >= 0) page_ahead = __ldg(pt_row + pi_ahead);
+      }
+
+      // ---- a6: online softmax (two head groups) ----
+      {
+        wait(bar_qk, par);               // QK done
+        __syncwarp();                    // lanes may leave the wait at different times
+        tc_fence_after_sync();
+        const bool valid = slot_s[ring * 128 + r_key] >= 0;
+        // x = log2-domain score relative to the head's reference maximum
+        float x[HPT], c[HPT], mr[HPT];
         load_scores<HPT>(lane_base + L::col_s + h0, HG, x);
-#pragma unroll
-        for (int h = 0; h < HPT; ++h) x[h] = valid ? x[h] * c[h] : -INFINITY;
-        float v[HPT];
-#pragma unroll
-        for (int h = 0; h < HPT; ++h) v[h] = x[h];
-        group_reduce<HPT, true>(v, quarter, lane, red, alpha_s + h0, bar_group);
-        if (r_key < HPT) {
-          const float mo = m_ref[h0 + r_key];
-          const float mn = fmaxf(mo, alpha_s[h0 + r_key]);
-          alpha_s[h0 + r_key] = (mo == mn) ? 1.0f : fast_exp2(mo - mn);
-          m_ref[h0 + r_key] = mn;
-        }
-        named_sync(bar_group, 128);
-        float al[HPT];
-        lds_vec<HPT>(alpha_s + h0, al);
+        lds_vec<HPT>(qscale + h0, c);
         lds_vec<HPT>(m_ref + h0, mr);
+        float xmax = -INFINITY;
 #pragma unroll
         for (int h = 0; h < HPT; ++h) {
-          l_sum[h] *= al[h];
-          x[h] -= mr[h];
+          x[h] = fmaf(x[h], c[h], -mr[h]);
+          xmax = fmaxf(xmax, x[h]);
         }
-        if (it > 0) {
+        const bool need = named_sync_or(bar_group, 128, valid && xmax > kRaiseThreshold);
+        if (need) {
+          // (rare) raise the reference maximum of every head to its tile maximum
+          load_scores<HPT>(lane_base + L::col_s + h0, HG, x);
 #pragma unroll
-          for (int mb = 0; mb < 4; ++mb)
-            tmem_scale_cols<HPT>(lane_base + L::col_o + mb * HG + h0, alpha_s + h0);
-          tmem_st_wait();
+          for (int h = 0; h < HPT; ++h) x[h] = valid ? x[h] * c[h] : -INFINITY;
+          float v[HPT];
+#pragma unroll
+          for (int h = 0; h < HPT; ++h) v[h] = x[h];
+          group_reduce<HPT, true>(v, quarter, lane, red, alpha_s + h0, bar_group);
+          if (r_key < HPT) {
+            const float mo = m_ref[h0 + r_key];
+            const float mn = fmaxf(mo, alpha_s[h0 + r_key]);
+            alpha_s[h0 + r_key] = (mo == mn) ? 1.0f : fast_exp2(mo - mn);
+            m_ref[h0 + r_key] = mn;
+          }
+          named_sync(bar_group, 128);
+          float al[HPT];
+          lds_vec<HPT>(alpha_s + h0, al);
+          lds_vec<HPT>(m_ref + h0, mr);
+#pragma unroll
+          for (int h = 0; h < HPT; ++h) {
+            l_sum[h] *= al[h];
+            x[h] -= mr[h];
+          }
+          if (it > 0) {
+#pragma unroll
+            for (int mb = 0; mb < 4; ++mb)
+              tmem_scale_cols<HPT>(lane_base + L::col_o + mb * HG + h0, alpha_s + h0);
+            tmem_st_wait();
+          }
         }
+        // probabilities -> f16 P^T row r_key, heads [h0, h0 + HPT)
+        uint32_t packed[HPT / 2];
+        if (valid) {
+#pragma unroll
+          for (int h = 0; h < HPT; h += 2) {
+            const float p0 = fast_exp2(x[h]);
+            const float p1 = fast_exp2(x[h + 1]);
+            l_sum[h] += p0;
+            l_sum[h + 1] += p1;
+            const __half2 ph = __floats2half2_rn(p0, p1);
+            packed[h / 2] = *reinterpret_cast<const uint32_t*>(&ph);
+          }
+        } else {
+#pragma unroll
+          for (int h = 0; h < HPT / 2; ++h) packed[h] = 0u;
+        }
+        uint8_t* p_s = kv_s + 8 * kChunkBytes;
+#pragma unroll
+        for (int u = 0; u < HPT / 8; ++u) {
+          const uint32_t off = (r_key >> 3) * L::p_atom_bytes + (r_key & 7) * L::p_row_bytes +
+                               (h0 * 2) + u * 16;
+          *reinterpret_cast<uint4*>(p_s + swizzle<L::p_swizzle_bits>(off)) =
+              make_uint4(packed[4 * u], packed[4 * u + 1], packed[4 * u + 2], packed[4 * u + 3]);
+        }
+        // ---- a2, last step: the slot of the key two tiles ahead.  Its ring
+        // entry was last read by the previous tile's softmax.
+        if (resolve_ahead)
+          slot_s[((it + 2) % 3) * 128 + warp * 16 + lane] =
+              pi_ahead >= 0 ? slot_from_page(page_ahead, idx_ahead, a.num_slots, a.dev_err) : -1;
+        fence_async_smem();
+        tc_fence_before_sync();
       }
-      // probabilities -> f16 P^T row r_key, heads [h0, h0 + HPT)
-      uint32_t packed[HPT / 2];
-      if (valid) {
+      // P of all 128 keys (and any O rescale) is in place: hand over to the issuers
+      named_sync(kBarCompute, kComputeThreads);
+      if (tid == 0) mbar_arrive(bar_p);
+    }
+    // the last PV must be complete before O is read or TMEM is freed
+    if (my_tiles > 0) {
+      const uint32_t last = (my_tiles - 1) & 1;
+      for (int p = 0; p < 4; ++p) wait(bar_pv0 + 8 * p, last);
+      __syncwarp();
+      tc_fence_after_sync();
+    }
+
+    // ---- a8: epilogue ----
+    const bool partial = a.splits > 1;
+    const int64_t out_head0 = static_cast<int64_t>(bs) * a.H + g * HG;   // first head row
+    const int64_t part = static_cast<int64_t>(unit) * a.splits + split;
+    group_reduce<HPT, false>(l_sum, quarter, lane, red, lsum + h0, bar_group);
+    if (r_key < HPT) {
+      const float lt = lsum[h0 + r_key];
+      lsum[HG + h0 + r_key] = lt > 0.0f ? __frcp_rn(lt) : 0.0f;     // 1 / l
+    }
+    named_sync(bar_group, 128);
+    if (r_key < HPT) {
+      const int h = h0 + r_key;
+      const float lt = lsum[h];
+      const float lse = (lt > 0.0f) ? (m_ref[h] + log2f(lt)) * 0.69314718055994531f : -INFINITY;
+      if (partial) a.ws_lse[part * HG + h] = lse;
+      else a.lse[out_head0 + h] = lse;
+    }
 #pragma unroll
-        for (int h = 0; h < HPT; h += 2) {
-          const float p0 = fast_exp2(x[h]);
-          const float p1 = fast_exp2(x[h + 1]);
-          l_sum[h] += p0;
-          l_sum[h + 1] += p1;
-          const __half2 ph = __floats2half2_rn(p0, p1);
-          packed[h / 2] = *reinterpret_cast<const uint32_t*>(&ph);
-        }
+    for (int mb = 0; mb < 4; ++mb) {
+      const int d = mb * 128 + r_key;
+      float o[HPT];
+      if (my_tiles > 0) {
+        tmem_load_cols<HPT>(lane_base + L::col_o + mb * HG + h0, o);
       } else {
 #pragma unroll
-        for (int h = 0; h < HPT / 2; ++h) packed[h] = 0u;
+        for (int j = 0; j < HPT; ++j) o[j] = 0.0f;
       }
-      uint8_t* p_s = kv_s + 8 * kChunkBytes;
+      float inv[HPT];
+      lds_vec<HPT>(lsum + HG + h0, inv);
 #pragma unroll
-      for (int u = 0; u < HPT / 8; ++u) {
-        const uint32_t off = (r_key >> 3) * L::p_atom_bytes + (r_key & 7) * L::p_row_bytes +
-                             (h0 * 2) + u * 16;
-        *reinterpret_cast<uint4*>(p_s + swizzle<L::p_swizzle_bits>(off)) =
-            make_uint4(packed[4 * u], packed[4 * u + 1], packed[4 * u + 2], packed[4 * u + 3]);
-      }
-      // ---- a2, last step: the slot of the key two tiles ahead.  Its ring
-      // entry was last read by the previous tile's softmax.
-      if (resolve_ahead)
-        slot_s[((it + 2) % 3) * 128 + warp * 16 + lane] =
-            pi_ahead >= 0 ? slot_from_page(page_ahead, idx_ahead, a.num_slots, a.dev_err) : -1;
-      fence_async_smem();
-      tc_fence_before_sync();
-    }
-    __syncthreads();
-
-    // ---- a7: O^T += V^T . P^T; issuer A takes slabs 0 then 1, issuer B
-    // slabs 2 then 3, each slab (128 latent columns) committed on its own so
-    // the next tile's dequant can reuse its shared memory as early as possible
-    if (issuer) {
-      tc_fence_after_sync();
-      constexpr uint32_t idesc = idesc_f16(128, HG, true, true);
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const int mb = 2 * half + j;
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks)
-          mma_f16kind(tmem + L::col_o + mb * HG,
-                      desc_v + (((2 * mb) * kChunkBytes + (2 * ks) * 1024) >> 4),
-                      desc_p + (((2 * ks) * L::p_atom_bytes) >> 4), idesc,
-                      (it > 0 || ks > 0) ? 1u : 0u);
-        mma_commit(bar_pv0 + 8 * mb);
+      for (int j = 0; j < HPT; ++j) {
+        const int h = h0 + j;
+        const float v = o[j] * inv[j];
+        if (partial) a.ws_o[(part * HG + h) * kLatent + d] = v;
+        else static_cast<__nv_bfloat16*>(a.out)[(out_head0 + h) * kLatent + d] = __float2bfloat16_rn(v);
       }
     }
-    __syncwarp();
-  }
-  // the last PV must be complete before O is read or TMEM is freed
-  if (my_tiles > 0) {
-    const uint32_t last = (my_tiles - 1) & 1;
-    for (int p = 0; p < 4; ++p) wait(bar_pv0 + 8 * p, last);
-    __syncwarp();
-    tc_fence_after_sync();
-  }
-
-  // ---- a8: epilogue ----
-  const bool partial = a.splits > 1;
-  const int64_t out_head0 = static_cast<int64_t>(bs) * a.H + g * HG;   // first head row
-  const int64_t part = static_cast<int64_t>(unit) * a.splits + split;
-  group_reduce<HPT, false>(l_sum, quarter, lane, red, lsum + h0, bar_group);
-  if (r_key < HPT) {
-    const float lt = lsum[h0 + r_key];
-    lsum[HG + h0 + r_key] = lt > 0.0f ? __frcp_rn(lt) : 0.0f;     // 1 / l
-  }
-  named_sync(bar_group, 128);
-  if (r_key < HPT) {
-    const int h = h0 + r_key;
-    const float lt = lsum[h];
-    const float lse = (lt > 0.0f) ? (m_ref[h] + log2f(lt)) * 0.69314718055994531f : -INFINITY;
-    if (partial) a.ws_lse[part * HG + h] = lse;
-    else a.lse[out_head0 + h] = lse;
-  }
-#pragma unroll
-  for (int mb = 0; mb < 4; ++mb) {
-    const int d = mb * 128 + r_key;
-    float o[HPT];
-    if (my_tiles > 0) {
-      tmem_load_cols<HPT>(lane_base + L::col_o + mb * HG + h0, o);
-    } else {
-#pragma unroll
-      for (int j = 0; j < HPT; ++j) o[j] = 0.0f;
+    if (a.fault_site == 1 && warp == 0) {
+      // test hook, after all work of the block: warp 0 waits on a barrier that
+      // nothing arrives on, so the wait runs out and reports a timeout
+      const bool ok = mbar_wait_bounded(bar_fault, 0, a.timeout_ns);
+      __syncwarp();
+      if (!ok) timed_out = true;
     }
-    float inv[HPT];
-    lds_vec<HPT>(lsum + HG + h0, inv);
-#pragma unroll
-    for (int j = 0; j < HPT; ++j) {
-      const int h = h0 + j;
-      const float v = o[j] * inv[j];
-      if (partial) a.ws_o[(part * HG + h) * kLatent + d] = v;
-      else static_cast<__nv_bfloat16*>(a.out)[(out_head0 + h) * kLatent + d] = __float2bfloat16_rn(v);
-    }
-  }
-  if (a.fault_site == 1 && warp == 0) {
-    // test hook, after all work of the block: warp 0 waits on a barrier that
-    // nothing arrives on, so the wait runs out and reports a timeout
-    const bool ok = mbar_wait_bounded(bar_fault, 0, a.timeout_ns);
-    __syncwarp();
-    if (!ok) timed_out = true;
-  }
+  }  // compute warpgroups
   if (timed_out) flag_error(a.dev_err, kDevTimeout);
   tc_fence_before_sync();
   __syncthreads();
-  if (warp == 0) {
+  if (warp == kComputeWarps) {
     __syncwarp();
     tc_fence_after_sync();
     tmem_dealloc(tmem, L::tmem_cols);
@@ -756,9 +787,16 @@ cudaError_t launch_decode_hg(const DecodeArgs& a, cudaStream_t stream) {
   const size_t smem = Layout<HG>::smem_bytes;
   static bool configured = false;   // per process; attribute is per kernel
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel<HG>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+    // The setmaxnreg split assumes the block is launched with exactly
+    // kLaunchRegs registers per thread; with fewer the compute warpgroups'
+    // increase could never be granted, so refuse to launch instead.
+    cudaFuncAttributes attr;
+    cudaError_t e = cudaFuncGetAttributes(&attr, decode_kernel<HG>);
+    if (e != cudaSuccess) return e;
+    if (attr.numRegs != kLaunchRegs || attr.maxThreadsPerBlock < kThreads)
+      return cudaErrorInvalidConfiguration;
+    e = cudaFuncSetAttribute(decode_kernel<HG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     configured = true;
   }
