@@ -52,6 +52,7 @@ constexpr double kBlockFixedTiles = 2.0;
 
 struct Plan {
   int HG, units, tiles, splits, tiles_per_split;
+  bool cluster_merge;          // the splits of a unit merge inside a thread-block cluster
   size_t ws_bytes;
 };
 
@@ -83,9 +84,16 @@ Plan make_plan(int B, int Sq, int H, int K, int force_splits, int sms) {
   }
   p.tiles_per_split = p.tiles > 0 ? (p.tiles + S - 1) / S : 0;
   p.splits = p.tiles_per_split > 0 ? (p.tiles + p.tiles_per_split - 1) / p.tiles_per_split : 1;
-  p.ws_bytes = p.splits > 1 ? static_cast<size_t>(p.units) * p.splits * p.HG *
-                                  (KV4_LATENT + 1) * sizeof(float)
-                            : 0;
+  // Two splits of a unit run as one cluster and merge in distributed shared
+  // memory (no workspace, no merge kernel) when all units' clusters fit on
+  // the device at once; otherwise the partials go to the workspace for
+  // merge_kernel.
+  p.cluster_merge = p.splits > 1 && p.splits <= kv4::kMaxClusterSplits &&
+                    p.units <= kv4::decode_max_active_clusters(p.HG, p.splits);
+  p.ws_bytes = (p.splits > 1 && !p.cluster_merge)
+                   ? static_cast<size_t>(p.units) * p.splits * p.HG * (KV4_LATENT + 1) *
+                         sizeof(float)
+                   : 0;
   return p;
 }
 
@@ -185,7 +193,8 @@ kv4_status kv4_sparse_mla_decode(const void* q_dev, const uint8_t* pool_dev, int
   a.sm_scale = sm_scale;
   a.out = out_dev;
   a.lse = lse_dev;
-  if (p.splits > 1) {
+  a.cluster_merge = p.cluster_merge ? 1 : 0;
+  if (p.splits > 1 && !p.cluster_merge) {
     a.ws_o = static_cast<float*>(workspace_dev);
     a.ws_lse = a.ws_o + static_cast<size_t>(p.units) * p.splits * p.HG * KV4_LATENT;
   }

@@ -42,6 +42,7 @@ struct DecodeArgs {
   uint64_t timeout_ns;
   int fault_site;
   cudaEvent_t after_decode;    // recorded between the decode and merge kernels (may be null)
+  int cluster_merge;           // splits > 1 merged inside a cluster of `splits` blocks
 };
 
 struct GatherArgs {
@@ -61,5 +62,11 @@ cudaError_t launch_quantize_write(const QuantizeArgs& a, int num_sms, cudaStream
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 cudaError_t launch_debug_gather(const GatherArgs& a, cudaStream_t stream);
 size_t decode_smem_bytes(int HG);
+// How many clusters of `splits` blocks of the HG variant can be resident at
+// once on this device (0: such clusters cannot run).  A unit split in two
+// runs as a cluster of two blocks that merge through distributed shared
+// memory; more splits merge through the workspace.
+int decode_max_active_clusters(int HG, int splits);
+constexpr int kMaxClusterSplits = 2;
 
 }  // namespace kv4

@@ -70,15 +70,25 @@ struct Layout {
   static constexpr uint32_t kv_bytes = 9u * kChunkBytes;              // K/V tile
   static constexpr uint32_t ctl_off = kv_off + kv_bytes;
   // control block
-  static constexpr uint32_t bar_off = ctl_off;                        // uint64 x 10
-  static constexpr uint32_t tmem_off = ctl_off + 80;                  // uint32
-  static constexpr uint32_t slot_off = ctl_off + 96;                  // int32 [3][128]
+  static constexpr uint32_t bar_off = ctl_off;                        // uint64 x 11
+  static constexpr uint32_t tmem_off = ctl_off + 96;                  // uint32
+  static constexpr uint32_t slot_off = ctl_off + 112;                 // int32 [3][128]
   static constexpr uint32_t mref_off = slot_off + 3 * 128 * 4;        // float [HG]
   static constexpr uint32_t alpha_off = mref_off + HG * 4;            // float [HG]
   static constexpr uint32_t red_off = alpha_off + HG * 4;             // float [2][4][HPT]
   static constexpr uint32_t lsum_off = red_off + 4 * HG * 4;          // float [2][HG]
   static constexpr uint32_t qscale_off = lsum_off + 2 * HG * 4;       // float [HG]
-  static constexpr uint32_t end = qscale_off + HG * 4;
+  // cluster merge of two splits: this block's partial lse, the peer's (copied
+  // in), and the two weights and 1/sum per head
+  static constexpr uint32_t xlse_off = qscale_off + HG * 4;           // float [HG]
+  static constexpr uint32_t xlse_in_off = xlse_off + HG * 4;          // float [HG]
+  static constexpr uint32_t xw_off = xlse_in_off + HG * 4;            // float [2][HG]
+  static constexpr uint32_t xinv_off = xw_off + 2 * HG * 4;           // float [HG]
+  static constexpr uint32_t end = xinv_off + HG * 4;
+  // The peer's half of this block's output slice of O lands in the Q region
+  // (free after the last QK): half of HG x 512 fp32 fits in Q's 9 x HG x 128 B.
+  static_assert(HG * kLatent * 4 / 2 <= q_bytes, "peer slice must fit in the Q region");
+  static_assert(xlse_off % 16 == 0 && xlse_in_off % 16 == 0, "bulk-copy operands are 16-byte aligned");
   static constexpr uint32_t smem_bytes = end + 1024;                  // + alignment slack
   // tensor memory: O^T slabs at columns [0, 4HG); S^T as four partial sums
   // (one per QK issuer) at [4HG + i HG, 5HG + i HG)
@@ -268,6 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
   const uint32_t bar_part0 = bars + 40;           // + 8 * part: tile part written
   const uint32_t bar_p = bars + 64;
   const uint32_t bar_fault = bars + 72;
+  const uint32_t bar_merge = bars + 80;           // cluster merge: the peer's data arrived
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::tmem_off);
   int32_t* slot_s = reinterpret_cast<int32_t*>(smem + L::slot_off);
   float* m_ref = reinterpret_cast<float*>(smem + L::mref_off);
@@ -284,6 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
     for (int p = 0; p < 3; ++p) mbar_init(bar_part0 + 8 * p, kComputeWarps);
     mbar_init(bar_p, 1);
     mbar_init(bar_fault, 1);
+    mbar_init(bar_merge, 1);
     fence_mbar_init();
   }
   if (tid < HG) m_ref[tid] = -INFINITY;
@@ -425,6 +437,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
       }
     }
     __syncwarp();
+    if (a.cluster_merge) {                     // the compute warps' merge barriers
+      cluster_sync();
+      cluster_sync();
+    }
   } else {
     // ==== compute warpgroups (warps 0..7) ====
     setmaxnreg_inc<kComputeRegs>();
@@ -647,7 +663,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
     }
 
     // ---- a8: epilogue ----
+    // Normalized partial (o, lse) of this split: into this block's shared
+    // memory when the splits of the unit form a cluster (the K/V tile is
+    // free once the last PV is done), else into the workspace; with one
+    // split, straight to out / lse.
+    const bool cmerge = a.cluster_merge != 0;
     const bool partial = a.splits > 1;
+    float* o_x = reinterpret_cast<float*>(kv_s);
+    float* xlse = reinterpret_cast<float*>(smem + L::xlse_off);
     const int64_t out_head0 = static_cast<int64_t>(bs) * a.H + g * HG;   // first head row
     const int64_t part = static_cast<int64_t>(unit) * a.splits + split;
     group_reduce<HPT, false>(l_sum, quarter, lane, red, lsum + h0, bar_group);
@@ -660,7 +683,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
       const int h = h0 + r_key;
       const float lt = lsum[h];
       const float lse = (lt > 0.0f) ? (m_ref[h] + log2f(lt)) * 0.69314718055994531f : -INFINITY;
-      if (partial) a.ws_lse[part * HG + h] = lse;
+      if (cmerge) xlse[h] = lse;
+      else if (partial) a.ws_lse[part * HG + h] = lse;
       else a.lse[out_head0 + h] = lse;
     }
 #pragma unroll
@@ -679,7 +703,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
       for (int j = 0; j < HPT; ++j) {
         const int h = h0 + j;
         const float v = o[j] * inv[j];
-        if (partial) a.ws_o[(part * HG + h) * kLatent + d] = v;
+        if (cmerge) o_x[h * kLatent + d] = v;
+        else if (partial) a.ws_o[(part * HG + h) * kLatent + d] = v;
         else static_cast<__nv_bfloat16*>(a.out)[(out_head0 + h) * kLatent + d] = __float2bfloat16_rn(v);
       }
     }
@@ -689,6 +714,71 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
       const bool ok = mbar_wait_bounded(bar_fault, 0, a.timeout_ns);
       __syncwarp();
       if (!ok) timed_out = true;
+    }
+
+    // ---- a9 inside a cluster of the unit's two splits: block r produces
+    // half of the output elements, out = (w_0 o_0 + w_1 o_1) / (w_0 + w_1)
+    // with w_i = exp(lse_i - max lse), lse = max lse + log(w_0 + w_1).  Each
+    // block pushes the peer's half of its normalized partial (and its lse)
+    // into the peer's shared memory with one bulk copy, then merges its own
+    // half locally.  (The issue warpgroup meets the same two cluster
+    // barriers in its branch.)
+    if (cmerge) {
+      constexpr int kUnits = HG * kLatent / 4;                // float4 units of o
+      constexpr uint32_t kHalfBytes = kUnits / 2 * 16;
+      const uint32_t rank = cluster_ctarank();
+      const uint32_t peer = rank ^ 1u;
+      float* xlse_in = reinterpret_cast<float*>(smem + L::xlse_in_off);
+      float* xw = reinterpret_cast<float*>(smem + L::xw_off);
+      float* xinv = reinterpret_cast<float*>(smem + L::xinv_off);
+      if (tid == 0) mbar_arrive_expect_tx(bar_merge, kHalfBytes + HG * 4);
+      fence_async_smem();                      // o_x / xlse are read by the async proxy
+      cluster_sync();                          // both partials written, both barriers armed
+      if (tid == 0) {
+        const uint32_t peer_bar = cluster_map(bar_merge, peer);
+        bulk_copy_to_cluster(cluster_map(smem_addr(q_s), peer), smem_addr(o_x) + peer * kHalfBytes,
+                             kHalfBytes, peer_bar);
+        bulk_copy_to_cluster(cluster_map(smem_addr(xlse_in), peer), smem_addr(xlse), HG * 4,
+                             peer_bar);
+      }
+      wait(bar_merge, 0);
+      if (tid < HG) {
+        const float l0 = rank == 0 ? xlse[tid] : xlse_in[tid];
+        const float l1 = rank == 0 ? xlse_in[tid] : xlse[tid];
+        const float m = fmaxf(l0, l1);
+        const float w0 = l0 != -INFINITY ? expf(l0 - m) : 0.0f;
+        const float w1 = l1 != -INFINITY ? expf(l1 - m) : 0.0f;
+        const float wsum = w0 + w1;
+        xw[tid] = w0;
+        xw[HG + tid] = w1;
+        xinv[tid] = wsum > 0.0f ? 1.0f / wsum : 0.0f;
+        if (rank == 0) a.lse[out_head0 + tid] = wsum > 0.0f ? m + logf(wsum) : -INFINITY;
+      }
+      named_sync(kBarCompute, kComputeThreads);
+      const float4* mine = reinterpret_cast<const float4*>(o_x) + rank * (kUnits / 2);
+      const float4* theirs = reinterpret_cast<const float4*>(q_s);
+      const float* w_mine = xw + rank * HG;
+      const float* w_theirs = xw + peer * HG;
+      __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
+      for (int i = tid; i < kUnits / 2; i += kComputeThreads) {
+        const int u = static_cast<int>(rank) * (kUnits / 2) + i;
+        const int h = u / (kLatent / 4);
+        const float4 va = mine[i], vb = theirs[i];
+        const float wa = w_mine[h], wb = w_theirs[h];
+        // summed in split order, as the merge kernel does
+        const float4 v0 = rank == 0 ? va : vb, v1 = rank == 0 ? vb : va;
+        const float w0 = rank == 0 ? wa : wb, w1 = rank == 0 ? wb : wa;
+        const float inv = xinv[h];
+        const __nv_bfloat162 lo = __floats2bfloat162_rn((w0 * v0.x + w1 * v1.x) * inv,
+                                                        (w0 * v0.y + w1 * v1.y) * inv);
+        const __nv_bfloat162 hi = __floats2bfloat162_rn((w0 * v0.z + w1 * v1.z) * inv,
+                                                        (w0 * v0.w + w1 * v1.w) * inv);
+        uint2 pk;
+        pk.x = *reinterpret_cast<const uint32_t*>(&lo);
+        pk.y = *reinterpret_cast<const uint32_t*>(&hi);
+        *reinterpret_cast<uint2*>(out + (out_head0 + h) * kLatent + (u % (kLatent / 4)) * 4) = pk;
+      }
+      cluster_sync();                          // the peer's copy out of this block is done
     }
   }  // compute warpgroups
   if (timed_out) flag_error(a.dev_err, kDevTimeout);
@@ -783,28 +873,76 @@ __global__ void __launch_bounds__(256) debug_gather_kernel(GatherArgs a) {
 }
 
 template <int HG>
-cudaError_t launch_decode_hg(const DecodeArgs& a, cudaStream_t stream) {
-  const size_t smem = Layout<HG>::smem_bytes;
-  static bool configured = false;   // per process; attribute is per kernel
-  if (!configured) {
+cudaError_t configure_decode() {
+  static cudaError_t state = cudaErrorNotReady;   // per process; attributes are per kernel
+  if (state == cudaErrorNotReady) {
     // The setmaxnreg split assumes the block is launched with exactly
     // kLaunchRegs registers per thread; with fewer the compute warpgroups'
     // increase could never be granted, so refuse to launch instead.
     cudaFuncAttributes attr;
     cudaError_t e = cudaFuncGetAttributes(&attr, decode_kernel<HG>);
-    if (e != cudaSuccess) return e;
-    if (attr.numRegs != kLaunchRegs || attr.maxThreadsPerBlock < kThreads)
-      return cudaErrorInvalidConfiguration;
-    e = cudaFuncSetAttribute(decode_kernel<HG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    configured = true;
+    if (e == cudaSuccess && (attr.numRegs != kLaunchRegs || attr.maxThreadsPerBlock < kThreads))
+      e = cudaErrorInvalidConfiguration;
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(decode_kernel<HG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(Layout<HG>::smem_bytes));
+    state = e;
   }
+  return state;
+}
+
+template <int HG>
+int max_active_clusters_hg(int splits) {
+  static int known[kMaxClusterSplits + 1] = {};   // 0 unknown, else 1 + the count
+  if (splits < 2 || splits > kMaxClusterSplits) return 0;
+  if (known[splits] == 0) {
+    int n = 0;
+    if (configure_decode<HG>() == cudaSuccess) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(splits);
+      cfg.blockDim = dim3(kThreads);
+      cfg.dynamicSmemBytes = Layout<HG>::smem_bytes;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = splits;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      if (cudaOccupancyMaxActiveClusters(&n, decode_kernel<HG>, &cfg) != cudaSuccess) n = 0;
+    }
+    (void)cudaGetLastError();
+    known[splits] = 1 + (n > 0 ? n : 0);
+  }
+  return known[splits] - 1;
+}
+
+template <int HG>
+cudaError_t launch_decode_hg(const DecodeArgs& a, cudaStream_t stream) {
+  const size_t smem = Layout<HG>::smem_bytes;
+  cudaError_t e = configure_decode<HG>();
+  if (e != cudaSuccess) return e;
   const int units = a.B * a.Sq * (a.H / HG);
-  decode_kernel<HG><<<units * a.splits, kThreads, smem, stream>>>(a);
-  cudaError_t e = cudaGetLastError();
+  if (a.cluster_merge) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(units * a.splits);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = a.splits;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, decode_kernel<HG>, a);
+  } else {
+    decode_kernel<HG><<<units * a.splits, kThreads, smem, stream>>>(a);
+    e = cudaGetLastError();
+  }
   if (e == cudaSuccess && a.after_decode != nullptr) e = cudaEventRecord(a.after_decode, stream);
-  if (e != cudaSuccess || a.splits == 1) return e;
+  if (e != cudaSuccess || a.splits == 1 || a.cluster_merge) return e;
   const int warps = units * HG;
   merge_kernel<<<(warps + 7) / 8, 256, 0, stream>>>(a, units);
   return cudaGetLastError();
@@ -817,6 +955,15 @@ size_t decode_smem_bytes(int HG) {
     case 16: return Layout<16>::smem_bytes;
     case 32: return Layout<32>::smem_bytes;
     case 64: return Layout<64>::smem_bytes;
+    default: return 0;
+  }
+}
+
+int decode_max_active_clusters(int HG, int splits) {
+  switch (HG) {
+    case 16: return max_active_clusters_hg<16>(splits);
+    case 32: return max_active_clusters_hg<32>(splits);
+    case 64: return max_active_clusters_hg<64>(splits);
     default: return 0;
   }
 }

@@ -152,12 +152,15 @@ def test_heads_and_ragged_k(H, K):
     assert_close(out, lse, out_ref, lse_ref, f"H={H} K={K}")
 
 
-@pytest.mark.parametrize("S", [1, 2, 3, 5, 8])
-def test_forced_splits(S):
+# up to 8 splits merge inside a thread-block cluster (distributed shared
+# memory); more go through the workspace and the merge kernel
+@pytest.mark.parametrize("K,S", [(1000, 1), (1000, 2), (1000, 3), (1000, 5), (1000, 8),
+                                 (2000, 9), (2000, 16)])
+def test_forced_splits(K, S):
     need_gpu()
-    p = small_problem(L=3000, B=2, Sq=1, H=64, K=1000, seed=77)
+    p = small_problem(L=3000, B=2, Sq=1, H=64, K=K, seed=77)
     out, lse, out_ref, lse_ref, st = run_both(p, force_splits=S)
-    assert_close(out, lse, out_ref, lse_ref, f"S={S}")
+    assert_close(out, lse, out_ref, lse_ref, f"K={K} S={S}")
 
 
 def test_masking_padding_duplicates_and_draft():
@@ -241,11 +244,13 @@ def test_invalid_arguments_raise():
         m.sparse_mla_decode(q, pool, pt, topk, lens, 0.1)
     assert e.value.status == 2
     q16 = q[:, :, :16].contiguous()
-    topk300 = torch.zeros((1, 1, 300), dtype=torch.int32, device=dev)
-    with pytest.raises(m.Kv4Error) as e:          # workspace too small for 2 splits
-        m.sparse_mla_decode(q16, pool, pt, topk300, lens, 0.1,
+    # 10 splits (more than a cluster merges) keep their partials in the
+    # workspace: one that is too small is refused
+    topk1200 = torch.zeros((1, 1, 1200), dtype=torch.int32, device=dev)
+    with pytest.raises(m.Kv4Error) as e:
+        m.sparse_mla_decode(q16, pool, pt, topk1200, lens, 0.1,
                             workspace=torch.zeros(4, dtype=torch.uint8, device=dev),
-                            force_splits=2)
+                            force_splits=10)
     assert e.value.status == 5
     # misaligned pool
     big = torch.zeros((65 * 352 + 1,), dtype=torch.uint8, device=dev)

@@ -5,9 +5,9 @@ decode -- e.g. a plugin whose host engine gives it only its inputs and
 outputs and owns all device memory -- and keeps its split-K partials in a
 static device array inside the library.  This test calls it through the
 C ABI twice in a row (the second call reuses the array with the first call's
-contents still in it) on a shape that plans 8 splits, checks both results
-against the regular entry point (which gets a caller workspace) within the
-parity tolerance, and checks that a shape needing more partial storage than
+contents still in it) on a shape forced to 16 splits -- more than one thread
+block cluster merges, so the partials do go to the array -- checks both
+results against the regular entry point within the parity tolerance, and checks that a shape needing more partial storage than
 the array holds is refused with KV4_ERR_SCRATCH_LIMIT.  It sits in a file of
 its own that pytest collects last, and builds everything it needs itself, so
 it passes both alone in a fresh process and after the other tests.
@@ -51,14 +51,14 @@ def test_noalloc_decode_matches_regular_entry_point():
     lib = kv.load_library()
     f = _noalloc_fn(lib)
     dev = torch.device("cuda")
-    w = wl.make_workload("decode")
+    w = wl.make_workload("splitk")           # 2 requests x 64 tiles of 128 keys
     pool = torch.zeros((w.num_slots, 352), dtype=torch.uint8, device=dev)
     for lat, rope, slots in wl.iter_pool_chunks(w, device=dev):
         kv.quantize_write(lat, rope, slots, pool)
     q = wl.queries(w, dev)
     pt, topk, lens = w.page_table.to(dev), w.topk.to(dev), w.seq_lens.to(dev)
-    splits, ws_bytes = kv.decode_plan(w.B, w.Sq, w.H, w.K)
-    assert splits > 1 and 0 < ws_bytes <= lib.kv4_noalloc_scratch_bytes()
+    splits, ws_bytes = kv.decode_plan(w.B, w.Sq, w.H, w.K, 16)
+    assert splits == 16 and 0 < ws_bytes <= lib.kv4_noalloc_scratch_bytes()
 
     ref_out, ref_lse = kv.sparse_mla_decode(q, pool, pt, topk, lens, w.sm_scale)
     torch.cuda.synchronize()
@@ -69,7 +69,7 @@ def test_noalloc_decode_matches_regular_entry_point():
         out = torch.full_like(ref_out, float("nan"))
         lse = torch.full_like(ref_lse, float("nan"))
         err = torch.zeros(1, dtype=torch.int32, device=dev)
-        assert _call(f, q, pool, pt, topk, lens, w, out, lse, err) == 0
+        assert _call(f, q, pool, pt, topk, lens, w, out, lse, err, force_splits=16) == 0
         torch.cuda.synchronize()
         assert int(err.item()) == 0
         o = out.float().cpu().numpy()
