@@ -12,9 +12,10 @@ Timing: W warm-up steps, then K steps, each bracketed by CUDA events on the
 launching stream, with a 256 MiB write between steps to flush L2 (outside the
 events); barrier + synchronize around the timed loop; max over ranks.
 value = gathered-KV bytes of all ranks / max step time (GB/s).  The decode
-kernel alone is timed with an event the library records between the decode
-and merge kernels.  e2e repeats the step through the public API from pinned
-host buffers (inputs in, out/lse back) inside the timed region.
+kernel alone (the roofline's kernel) is timed in a second loop, with an
+event the library records right after the decode kernel.  e2e repeats the
+step through the public API from pinned host buffers (inputs in, out/lse
+back) inside the timed region.
 
 --impl reference times the CPU oracle (single-threaded C++, the method's
 plain definition) on a bounded sample of the same workload.
@@ -347,7 +348,9 @@ def run_gpu(args):
     kv_bytes = valid * 352
     alg_bytes = algorithmic_bytes(w, valid)
     flops = 2.0 * w.H * valid * (576 + 512)
-    launches_per_step = 2 + (1 if splits > 1 else 0)
+    # cache write + decode, + the merge kernel when the split-K partials go
+    # through the workspace (a unit split in two merges inside its cluster)
+    launches_per_step = 2 + (1 if ws_bytes > 0 else 0)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -357,32 +360,43 @@ def run_gpu(args):
 
     e0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     e1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    d0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    d1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    for e in d1:                 # create the events the library will record
-        e.record(stream)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)
     wall0 = time.perf_counter()
+    # The step's kernels run back to back (the decode may start while the
+    # cache write finishes), so no event sits between them.
     with ClockSampler(local) as clocks:
         for i in range(args.steps):
             flush.zero_()
             e0[i].record(stream)
-            kv.quantize_write(new_lat, new_rope, new_slots, pool, err)
-            d0[i].record(stream)
-            kv.set_timing_event(d1[i])
-            kv.sparse_mla_decode(q, pool, pt, topk, lens, w.sm_scale, out=out, lse=lse,
-                                 workspace=ws, dev_err=err, force_splits=args.splits)
+            step()
             e1[i].record(stream)
-        kv.set_timing_event(None)
         torch.cuda.synchronize(dev)
     wall = time.perf_counter() - wall0
     if world > 1:
         torch.distributed.barrier()
     step_ms = [a.elapsed_time(b) for a, b in zip(e0, e1)]
-    dec_ms = [a.elapsed_time(b) for a, b in zip(d0, d1)]
     t_ms = sum(step_ms) / len(step_ms)
+    assert int(err.item()) == 0, f"device error flags {int(err.item())}"
+
+    # The decode kernel alone (for the roofline): a second loop on the same
+    # inputs, the library recording an event right after the decode kernel
+    # (before a merge kernel, if any).
+    d0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    d1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    for e in d1:                 # create the events the library will record
+        e.record(stream)
+    torch.cuda.synchronize(dev)
+    for i in range(args.steps):
+        flush.zero_()
+        d0[i].record(stream)
+        kv.set_timing_event(d1[i])
+        kv.sparse_mla_decode(q, pool, pt, topk, lens, w.sm_scale, out=out, lse=lse, workspace=ws,
+                             dev_err=err, force_splits=args.splits)
+    kv.set_timing_event(None)
+    torch.cuda.synchronize(dev)
+    dec_ms = [a.elapsed_time(b) for a, b in zip(d0, d1)]
     dec_ms_avg = sum(dec_ms) / len(dec_ms)
     assert int(err.item()) == 0, f"device error flags {int(err.item())}"
 

@@ -183,6 +183,20 @@ __device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst_cluster, uint3
       : "memory");
 }
 
+// ---------------------------------------------------------------------------
+// programmatic dependent launch: the kernels are launched so that they may
+// start while the previous kernel of the stream is finishing; each waits for
+// it (all of its memory operations visible) before its first global access,
+// and lets the next kernel start early.  Without the launch attribute both
+// are no-ops.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Named barrier among `count` threads (a multiple of 32).
 __device__ __forceinline__ void named_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");

@@ -52,6 +52,10 @@ __device__ __forceinline__ uint4 ld_stream(const void* p) {
 }
 
 __global__ void __launch_bounds__(256) quantize_write_kernel(QuantizeArgs a) {
+  // the previous kernel (e.g. a decode still gathering from the pool) must
+  // be complete before any row is written
+  grid_dependency_wait();
+  grid_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
@@ -118,8 +122,7 @@ cudaError_t launch_quantize_write(const QuantizeArgs& a, int num_sms, cudaStream
   int64_t blocks = (warps_needed + 7) / 8;
   const int64_t cap = static_cast<int64_t>(num_sms > 0 ? num_sms : 1) * 16;
   if (blocks > cap) blocks = cap;
-  quantize_write_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(quantize_write_kernel, static_cast<unsigned>(blocks), 256, 0, stream, 1, a);
 }
 
 }  // namespace kv4

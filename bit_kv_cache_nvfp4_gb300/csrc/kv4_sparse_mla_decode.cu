@@ -59,6 +59,11 @@ constexpr int kLaunchRegs = 168;          // 65536 / 384, rounded down to a mult
 constexpr uint32_t kComputeRegs = 232;
 constexpr uint32_t kIssueRegs = 40;
 static_assert(2 * kComputeRegs + kIssueRegs <= 3 * kLaunchRegs, "register split exceeds the launch");
+#ifndef KV4_PV_ISSUERS
+#define KV4_PV_ISSUERS 2
+#endif
+constexpr int kPvIssuers = KV4_PV_ISSUERS;    // 2: slabs 0,2 are released half way through PV
+static_assert(kPvIssuers == 2 || kPvIssuers == 4, "PV issuers");
 constexpr int kBarCompute = 3;            // named barrier of the 256 compute threads (1, 2: softmax groups)
 constexpr float kRaiseThreshold = 8.0f;   // log2 units: p <= 256 between raises
 
@@ -258,7 +263,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
   const int bs = unit / NG;                        // b * Sq + s
   const int b = bs / a.Sq;
   const int s = bs % a.Sq;
-  const int64_t l_eff = static_cast<int64_t>(__ldg(a.seq_lens + b)) - (a.Sq - 1 - s);
   const int32_t* topk_row = a.topk + static_cast<int64_t>(bs) * a.K;
   const int32_t* pt_row = a.page_table + static_cast<int64_t>(b) * a.pt_stride;
   const int num_tiles = (a.K + kTileKeys - 1) / kTileKeys;
@@ -298,6 +302,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
     mbar_init(bar_merge, 1);
     fence_mbar_init();
   }
+  // everything above touches no global memory and may overlap the end of
+  // the previous kernel of the stream (which may have produced any input)
+  grid_dependency_wait();
+  grid_launch_dependents();
+  const int64_t l_eff = static_cast<int64_t>(__ldg(a.seq_lens + b)) - (a.Sq - 1 - s);
   if (tid < HG) m_ref[tid] = -INFINITY;
   // slots of the first two tiles (a ring of three tiles, filled two ahead);
   // started first so that their dependent loads overlap the Q conversion
@@ -416,16 +425,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
         tc_fence_after_sync();
         issue_qk(32 + qi, 1, false);                 // rope: one 16-column step each
         mma_commit(bar_qk);
-        if (qi >= 2) continue;
-        // a7: O^T += V^T . P^T; issuer 0 takes O slabs 0 then 1, issuer 1
-        // slabs 2 then 3, each committed on its own so that the next tile's
+        if (qi >= kPvIssuers) continue;
+        // a7: O^T += V^T . P^T, 4 / kPvIssuers O slabs (128 columns each) per
+        // issuer, each committed on its own so that the next tile's
         // dequantization can reuse its shared memory as early as possible
         wait(bar_p, par);
         tc_fence_after_sync();
         constexpr uint32_t idesc = idesc_f16(128, HG, true, true);
+        constexpr int kSlabsPerIssuer = 4 / kPvIssuers;
 #pragma unroll 1
-        for (int j = 0; j < 2; ++j) {
-          const int mb = 2 * qi + j;
+        for (int j = 0; j < kSlabsPerIssuer; ++j) {
+          const int mb = kSlabsPerIssuer * qi + j;
 #pragma unroll 1
           for (int ks = 0; ks < 8; ++ks)
             mma_f16kind(tmem + L::col_o + mb * HG,
@@ -794,6 +804,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
 // a9: out = sum_i exp(lse_i - lse) o_i, lse = log sum_i exp(lse_i).
 // One warp per (unit, head); lane l covers columns 4l..4l+3 of each 128.
 __global__ void __launch_bounds__(256) merge_kernel(DecodeArgs a, int n_units) {
+  grid_dependency_wait();                      // the decode's partials
+  grid_launch_dependents();
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   const int HG = a.HG;
@@ -923,29 +935,13 @@ cudaError_t launch_decode_hg(const DecodeArgs& a, cudaStream_t stream) {
   cudaError_t e = configure_decode<HG>();
   if (e != cudaSuccess) return e;
   const int units = a.B * a.Sq * (a.H / HG);
-  if (a.cluster_merge) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(units * a.splits);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = a.splits;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, decode_kernel<HG>, a);
-  } else {
-    decode_kernel<HG><<<units * a.splits, kThreads, smem, stream>>>(a);
-    e = cudaGetLastError();
-  }
+  e = launch_pdl(decode_kernel<HG>, static_cast<unsigned>(units * a.splits), kThreads, smem, stream,
+                 a.cluster_merge ? a.splits : 1, a);
   if (e == cudaSuccess && a.after_decode != nullptr) e = cudaEventRecord(a.after_decode, stream);
   if (e != cudaSuccess || a.splits == 1 || a.cluster_merge) return e;
   const int warps = units * HG;
-  merge_kernel<<<(warps + 7) / 8, 256, 0, stream>>>(a, units);
-  return cudaGetLastError();
+  return launch_pdl(merge_kernel, static_cast<unsigned>((warps + 7) / 8), 256, 0, stream, 1, a,
+                    units);
 }
 
 }  // namespace
