@@ -186,9 +186,12 @@ kv4_status kv4_sparse_mla_decode_noalloc(const void* q_dev, const uint8_t* pool_
                                          kv4_stream_t stream);
 size_t kv4_noalloc_scratch_bytes(void);
 
-/* Test hook: the next kernel launches use this bounded-wait limit (ns) and,
- * when fault_site != 0, skip one internal mbarrier arrive so that the wait
- * runs out and KV4_DEV_TIMEOUT is reported.  0, 0 restores the defaults. */
+/* Test hook: the next decode launches use this bounded-wait limit (ns; 0
+ * keeps the 1 s default) and, when fault_site == 1, one warp of each block
+ * finishes its work and then waits on an mbarrier that nothing arrives on,
+ * so that the wait runs out and KV4_DEV_TIMEOUT is reported while the block
+ * still exits normally.  fault_site must be 0 or 1.  0, 0 restores the
+ * defaults. */
 kv4_status kv4_set_wait_limit(int64_t timeout_ns, int fault_site);
 
 /* Measurement hook: when `cuda_event` (a cudaEvent_t) is non-NULL, every
