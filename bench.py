@@ -405,6 +405,11 @@ def run_gpu(args):
 
     # end to end through the public API, host buffers in and out
     e2e = run_e2e(kv, w, dev, pool, pt, lens, flush, args)
+    latent = None
+    if not args.skip_latent:
+        del pool
+        torch.cuda.empty_cache()
+        latent = run_latent_rows(kv, w, dev, q, pt, topk, lens, flush, err, args, valid)
 
     peak_gbs, peak_tflops, peak_kind = measured_peaks()
     achieved_gbs = alg_bytes / (dec_ms_avg * 1e-3) / 1e9
@@ -460,6 +465,7 @@ def run_gpu(args):
             "roofline": roof,
             "cpu_baseline": cpu,
             "e2e": e2e,
+            "latent_rows_288B": latent,
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clocks.summary(),
             "wall_s_timed_loop": wall,
@@ -468,6 +474,65 @@ def run_gpu(args):
     if world > 1:
         torch.distributed.destroy_process_group()
     return 0
+
+
+def run_latent_rows(kv, w, dev, q, pt, topk, lens, flush, err, args, valid):
+    """The same step on 288-byte latent-only rows (no rope; QK over the 512
+    latent columns): cache write of the new tokens + decode, timed like the
+    main step, and the decode kernel alone."""
+    pool = torch.zeros((w.num_slots, 288), dtype=torch.uint8, device=dev)
+    for lat, _rope, slots in wl.iter_pool_chunks(w, chunk=1 << 18, device=dev):
+        kv.quantize_write_latent(lat, slots, pool)
+    new_lat, _new_rope, new_slots = wl.newest_tokens(w, dev)
+    q512 = q[..., :512].contiguous()
+    splits, ws_bytes = kv.decode_plan_latent(w.B, w.Sq, w.H, w.K, args.splits)
+    out = torch.empty((w.B, w.Sq, w.H, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((w.B, w.Sq, w.H), dtype=torch.float32, device=dev)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        kv.quantize_write_latent(new_lat, new_slots, pool, err)
+        kv.sparse_mla_decode_latent(q512, pool, pt, topk, lens, w.sm_scale, out=out, lse=lse,
+                                    workspace=ws, dev_err=err, force_splits=args.splits)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    e0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    e1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.zero_()
+        e0[i].record(stream)
+        step()
+        e1[i].record(stream)
+    d0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    d1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    for e in d1:
+        e.record(stream)
+    torch.cuda.synchronize(dev)
+    for i in range(args.steps):
+        flush.zero_()
+        d0[i].record(stream)
+        kv.set_timing_event(d1[i])
+        kv.sparse_mla_decode_latent(q512, pool, pt, topk, lens, w.sm_scale, out=out, lse=lse,
+                                    workspace=ws, dev_err=err, force_splits=args.splits)
+    kv.set_timing_event(None)
+    torch.cuda.synchronize(dev)
+    assert int(err.item()) == 0, f"device error flags {int(err.item())}"
+    t_ms = sum(a.elapsed_time(b) for a, b in zip(e0, e1)) / args.steps
+    d_ms = sum(a.elapsed_time(b) for a, b in zip(d0, d1)) / args.steps
+    n_q = w.B * w.Sq
+    alg = valid * 288 + n_q * w.K * 4 * 2 + n_q * w.H * (1024 + 1024 + 4)
+    flops = 2.0 * w.H * valid * (512 + 512)
+    del pool
+    return {"row_bytes": 288, "us_per_step": t_ms * 1e3,
+            "kv_gbs": valid * 288 / (t_ms * 1e-3) / 1e9, "splits": splits,
+            "decode_kernel_us": d_ms * 1e3,
+            "decode_tflops": flops / (d_ms * 1e-3) / 1e12,
+            "decode_algorithmic_gbs": alg / (d_ms * 1e-3) / 1e9,
+            "note": "QK over the 512 latent columns, PV over the same 512; same workload"}
 
 
 def run_e2e(kv, w, dev, pool, pt, lens, flush, args):
@@ -526,6 +591,8 @@ def main(argv=None):
     p.add_argument("--skip-cpu", action="store_true")
     p.add_argument("--sessions", type=int, default=64,
                    help="sessions of the long-context workload per rank (smaller: profiling)")
+    p.add_argument("--skip-latent", action="store_true",
+                   help="skip the 288-byte latent-only row measurement")
     p.add_argument("--splits", type=int, default=0,
                    help="force the split-K count (0: the library's plan)")
     args = p.parse_args(argv)

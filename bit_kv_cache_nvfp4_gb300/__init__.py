@@ -8,8 +8,9 @@ status codes into exceptions.  There is no CPU fallback: if the library
 cannot be loaded, importing the functions raises.
 
 Row format and method: numinousmuses "inference-optimizations" README,
-sections "4-bit KV cache" (352-byte NVFP4 row, kv4mla decode) and
-"Attention kernels" (split-K sparse decode).
+sections "4-bit KV cache" (352-byte NVFP4 row, kv4mla decode; the 288-byte
+rope-free row of the GLM-5.3-Flash bullet, served by the ``*_latent``
+functions) and "Attention kernels" (split-K sparse decode).
 """
 from __future__ import annotations
 
@@ -22,11 +23,13 @@ import torch
 __all__ = [
     "Kv4Error", "library_path", "load_library", "quantize_write", "decode_plan",
     "sparse_mla_decode", "debug_gather_dequant", "set_wait_limit", "set_timing_event",
-    "ROW_BYTES", "LATENT", "ROPE", "QK_DIM", "PAGE", "DEV_BAD_SLOT", "DEV_BAD_PAGE",
+    "quantize_write_latent", "decode_plan_latent", "sparse_mla_decode_latent",
+    "debug_gather_dequant_latent", "ROW_BYTES", "ROW_BYTES_LATENT", "LATENT", "ROPE", "QK_DIM", "PAGE", "DEV_BAD_SLOT", "DEV_BAD_PAGE",
     "DEV_TIMEOUT",
 ]
 
 ROW_BYTES, LATENT, ROPE, QK_DIM, PAGE, TILE_KEYS = 352, 512, 64, 576, 64, 128
+ROW_BYTES_LATENT = 288
 DEV_BAD_SLOT, DEV_BAD_PAGE, DEV_TIMEOUT = 1, 2, 4
 _STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported shape or page size",
            3: "device is not compute capability 10.3", 4: "kernel launch failed",
@@ -71,6 +74,14 @@ def load_library():
         lib.kv4_debug_gather_dequant.argtypes = [P, i64, P, i64, i32, P, i32, P, i32, i32, P, P,
                                                  P]
         lib.kv4_debug_gather_dequant.restype = i32
+        lib.kv4_quantize_write_latent.argtypes = [P, i64, P, i64, P, i64, P, P]
+        lib.kv4_quantize_write_latent.restype = i32
+        lib.kv4_decode_plan_latent.argtypes = lib.kv4_decode_plan.argtypes
+        lib.kv4_decode_plan_latent.restype = i32
+        lib.kv4_sparse_mla_decode_latent.argtypes = lib.kv4_sparse_mla_decode.argtypes
+        lib.kv4_sparse_mla_decode_latent.restype = i32
+        lib.kv4_debug_gather_dequant_latent.argtypes = lib.kv4_debug_gather_dequant.argtypes
+        lib.kv4_debug_gather_dequant_latent.restype = i32
         lib.kv4_set_wait_limit.argtypes = [i64, i32]
         lib.kv4_set_wait_limit.restype = i32
         lib.kv4_set_timing_event.argtypes = [P]
@@ -126,14 +137,41 @@ def quantize_write(latent: torch.Tensor, rope: torch.Tensor, slot_mapping: torch
         _stream(pool.device)))
 
 
-def decode_plan(B: int, Sq: int, H: int, K: int, force_splits: int = 0):
-    """(splits, workspace_bytes) the decode will use on the current device."""
+def quantize_write_latent(latent: torch.Tensor, slot_mapping: torch.Tensor, pool: torch.Tensor,
+                          dev_err: torch.Tensor | None = None) -> None:
+    """Latent-only rows: quantize latent bf16 [N,512] into pool uint8
+    [num_slots,288] at slot_mapping int64 [N] (negative = skip)."""
     lib = load_library()
+    n = slot_mapping.shape[0]
+    if latent.dim() != 2 or latent.shape[0] != n:
+        raise ValueError("latent [N,512] and slot_mapping [N] must agree")
+    if latent.stride(1) != 1:
+        raise ValueError("latent rows must be contiguous")
+    if pool.dim() != 2 or pool.shape[1] != ROW_BYTES_LATENT:
+        raise ValueError("pool must be [num_slots, 288]")
+    _check("kv4_quantize_write_latent", lib.kv4_quantize_write_latent(
+        _dev(latent, "latent", torch.bfloat16, False), latent.stride(0),
+        _dev(slot_mapping, "slot_mapping", torch.int64), n,
+        _dev(pool, "pool", torch.uint8), pool.shape[0], _err_ptr(dev_err),
+        _stream(pool.device)))
+
+
+def _plan(fn: str, B: int, Sq: int, H: int, K: int, force_splits: int):
     s = ctypes.c_int(0)
     ws = ctypes.c_size_t(0)
-    _check("kv4_decode_plan", lib.kv4_decode_plan(B, Sq, H, K, force_splits, ctypes.byref(s),
-                                                  ctypes.byref(ws)))
+    _check(fn, getattr(load_library(), fn)(B, Sq, H, K, force_splits, ctypes.byref(s),
+                                           ctypes.byref(ws)))
     return s.value, ws.value
+
+
+def decode_plan(B: int, Sq: int, H: int, K: int, force_splits: int = 0):
+    """(splits, workspace_bytes) the decode will use on the current device."""
+    return _plan("kv4_decode_plan", B, Sq, H, K, force_splits)
+
+
+def decode_plan_latent(B: int, Sq: int, H: int, K: int, force_splits: int = 0):
+    """(splits, workspace_bytes) of sparse_mla_decode_latent on the current device."""
+    return _plan("kv4_decode_plan_latent", B, Sq, H, K, force_splits)
 
 
 def _workspace(device, nbytes: int):
@@ -158,10 +196,30 @@ def sparse_mla_decode(q: torch.Tensor, pool: torch.Tensor, page_table: torch.Ten
     [B,pt_stride]; topk_idx int32 [B,Sq,K] (logical positions, -1 = pad);
     seq_lens int32 [B].  Returns (out bf16 [B,Sq,H,512], lse fp32 [B,Sq,H]).
     """
+    return _decode(False, q, pool, page_table, topk_idx, seq_lens, sm_scale, out, lse, workspace,
+                   force_splits, dev_err)
+
+
+def sparse_mla_decode_latent(q: torch.Tensor, pool: torch.Tensor, page_table: torch.Tensor,
+                             topk_idx: torch.Tensor, seq_lens: torch.Tensor, sm_scale: float,
+                             out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
+                             workspace: torch.Tensor | None = None, force_splits: int = 0,
+                             dev_err: torch.Tensor | None = None):
+    """The same decode over latent-only rows: q bf16 [B,Sq,H,512], pool uint8
+    [num_slots,288]; QK^T over the 512 latent columns."""
+    return _decode(True, q, pool, page_table, topk_idx, seq_lens, sm_scale, out, lse, workspace,
+                   force_splits, dev_err)
+
+
+def _decode(latent_only, q, pool, page_table, topk_idx, seq_lens, sm_scale, out, lse, workspace,
+            force_splits, dev_err):
     lib = load_library()
     B, Sq, H, D = q.shape
-    if D != QK_DIM:
-        raise ValueError("q must be [B, Sq, H, 576]")
+    qk, row = (LATENT, ROW_BYTES_LATENT) if latent_only else (QK_DIM, ROW_BYTES)
+    if D != qk:
+        raise ValueError(f"q must be [B, Sq, H, {qk}]")
+    if pool.dim() != 2 or pool.shape[1] != row:
+        raise ValueError(f"pool must be [num_slots, {row}]")
     K = topk_idx.shape[2]
     if tuple(topk_idx.shape[:2]) != (B, Sq) or seq_lens.shape[0] != B or page_table.shape[0] != B:
         raise ValueError("topk_idx [B,Sq,K], seq_lens [B] and page_table [B,*] must agree with q")
@@ -170,12 +228,14 @@ def sparse_mla_decode(q: torch.Tensor, pool: torch.Tensor, page_table: torch.Ten
         out = torch.empty((B, Sq, H, LATENT), dtype=torch.bfloat16, device=dev)
     if lse is None:
         lse = torch.empty((B, Sq, H), dtype=torch.float32, device=dev)
-    splits, ws_bytes = decode_plan(B, Sq, H, K, force_splits)
+    fn = "kv4_sparse_mla_decode_latent" if latent_only else "kv4_sparse_mla_decode"
+    splits, ws_bytes = (decode_plan_latent if latent_only else decode_plan)(B, Sq, H, K,
+                                                                           force_splits)
     if workspace is None:
         workspace = _workspace(dev, ws_bytes)
     ws_ptr = None if workspace is None else _dev(workspace, "workspace", workspace.dtype)
     ws_len = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    _check("kv4_sparse_mla_decode", lib.kv4_sparse_mla_decode(
+    _check(fn, getattr(lib, fn)(
         _dev(q, "q", torch.bfloat16), _dev(pool, "pool", torch.uint8), pool.shape[0],
         _dev(page_table, "page_table", torch.int32), page_table.shape[1], PAGE,
         _dev(topk_idx, "topk_idx", torch.int32), K, _dev(seq_lens, "seq_lens", torch.int32),
@@ -188,10 +248,23 @@ def sparse_mla_decode(q: torch.Tensor, pool: torch.Tensor, page_table: torch.Ten
 def debug_gather_dequant(pool: torch.Tensor, page_table: torch.Tensor, topk_idx: torch.Tensor,
                          seq_lens: torch.Tensor, dev_err: torch.Tensor | None = None):
     """The decode's gather + dequantization: f16 [B,Sq,K,576] (masked rows 0)."""
+    return _gather(False, pool, page_table, topk_idx, seq_lens, dev_err)
+
+
+def debug_gather_dequant_latent(pool: torch.Tensor, page_table: torch.Tensor,
+                                topk_idx: torch.Tensor, seq_lens: torch.Tensor,
+                                dev_err: torch.Tensor | None = None):
+    """The same over latent-only rows: f16 [B,Sq,K,512] (masked rows 0)."""
+    return _gather(True, pool, page_table, topk_idx, seq_lens, dev_err)
+
+
+def _gather(latent_only, pool, page_table, topk_idx, seq_lens, dev_err):
     lib = load_library()
     B, Sq, K = topk_idx.shape
-    rows = torch.empty((B, Sq, K, QK_DIM), dtype=torch.float16, device=pool.device)
-    _check("kv4_debug_gather_dequant", lib.kv4_debug_gather_dequant(
+    fn = "kv4_debug_gather_dequant_latent" if latent_only else "kv4_debug_gather_dequant"
+    rows = torch.empty((B, Sq, K, LATENT if latent_only else QK_DIM), dtype=torch.float16,
+                       device=pool.device)
+    _check(fn, getattr(lib, fn)(
         _dev(pool, "pool", torch.uint8), pool.shape[0],
         _dev(page_table, "page_table", torch.int32), page_table.shape[1], PAGE,
         _dev(topk_idx, "topk_idx", torch.int32), K, _dev(seq_lens, "seq_lens", torch.int32),

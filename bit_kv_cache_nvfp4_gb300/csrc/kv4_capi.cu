@@ -62,7 +62,7 @@ struct Plan {
 // to the smaller S.  One block runs per SM.  The fixed cost (prologue: Q
 // load and conversion, first dependent loads; epilogue: output or partial
 // writes) is about two tiles of work.
-Plan make_plan(int B, int Sq, int H, int K, int force_splits, int sms) {
+Plan make_plan(int B, int Sq, int H, int K, int force_splits, int sms, bool rope) {
   Plan p{};
   p.HG = heads_per_block(H);
   p.units = B * Sq * (H / p.HG);
@@ -89,7 +89,7 @@ Plan make_plan(int B, int Sq, int H, int K, int force_splits, int sms) {
   // the device at once; otherwise the partials go to the workspace for
   // merge_kernel.
   p.cluster_merge = p.splits > 1 && p.splits <= kv4::kMaxClusterSplits &&
-                    p.units <= kv4::decode_max_active_clusters(p.HG, p.splits);
+                    p.units <= kv4::decode_max_active_clusters(p.HG, p.splits, rope);
   p.ws_bytes = (p.splits > 1 && !p.cluster_merge)
                    ? static_cast<size_t>(p.units) * p.splits * p.HG * (KV4_LATENT + 1) *
                          sizeof(float)
@@ -106,52 +106,56 @@ kv4_status check_decode_shape(int B, int Sq, int H, int K) {
 
 }  // namespace
 
-extern "C" {
+namespace {
 
-kv4_status kv4_quantize_write(const void* latent_dev, int64_t latent_row_stride,
-                              const void* rope_dev, int64_t rope_row_stride,
-                              const int64_t* slot_mapping_dev, int64_t n_tokens,
-                              uint8_t* pool_dev, int64_t num_slots, int32_t* dev_err,
-                              kv4_stream_t stream) {
+// The entry points below share these bodies; `rope` selects the 352-byte row
+// (latent + rope) or the 288-byte latent-only row.
+kv4_status quantize_impl(const void* latent_dev, int64_t latent_row_stride, const void* rope_dev,
+                         int64_t rope_row_stride, const int64_t* slot_mapping_dev,
+                         int64_t n_tokens, uint8_t* pool_dev, int64_t num_slots,
+                         int32_t* dev_err, kv4_stream_t stream, bool rope) {
   if (n_tokens < 0 || num_slots < 0) return KV4_ERR_INVALID_ARG;
   if (n_tokens == 0) return KV4_OK;
-  if (!latent_dev || !rope_dev || !slot_mapping_dev || !pool_dev) return KV4_ERR_INVALID_ARG;
-  if (latent_row_stride < KV4_LATENT || latent_row_stride % 8 != 0 ||
-      rope_row_stride < KV4_ROPE || rope_row_stride % 8 != 0)
+  if (!latent_dev || (rope && !rope_dev) || !slot_mapping_dev || !pool_dev)
     return KV4_ERR_INVALID_ARG;
-  if (!aligned16(latent_dev) || !aligned16(rope_dev) || !aligned16(pool_dev) ||
+  if (latent_row_stride < KV4_LATENT || latent_row_stride % 8 != 0 ||
+      (rope && (rope_row_stride < KV4_ROPE || rope_row_stride % 8 != 0)))
+    return KV4_ERR_INVALID_ARG;
+  if (!aligned16(latent_dev) || (rope && !aligned16(rope_dev)) || !aligned16(pool_dev) ||
       (reinterpret_cast<uintptr_t>(slot_mapping_dev) & 7u) != 0)
     return KV4_ERR_INVALID_ARG;
-  if (num_slots > INT64_MAX / KV4_ROW_BYTES) return KV4_ERR_INVALID_ARG;
+  const int row_bytes = rope ? KV4_ROW_BYTES : KV4_ROW_BYTES_LATENT;
+  if (num_slots > INT64_MAX / row_bytes) return KV4_ERR_INVALID_ARG;
   int sms = 0;
   const kv4_status st = device_info(&sms);
   if (st != KV4_OK) return st;
-  kv4::QuantizeArgs a{latent_dev, latent_row_stride, rope_dev,  rope_row_stride, slot_mapping_dev,
-                      n_tokens,   pool_dev,          num_slots, dev_err};
+  kv4::QuantizeArgs a{latent_dev, latent_row_stride, rope ? rope_dev : nullptr,
+                      rope ? rope_row_stride : 0, slot_mapping_dev, n_tokens, pool_dev,
+                      num_slots, row_bytes, dev_err};
   return kv4::launch_quantize_write(a, sms, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
              ? KV4_OK
              : KV4_ERR_LAUNCH;
 }
 
-kv4_status kv4_decode_plan(int B, int Sq, int H, int K, int force_splits, int* splits,
-                           size_t* workspace_bytes) {
+kv4_status plan_impl(int B, int Sq, int H, int K, int force_splits, int* splits,
+                     size_t* workspace_bytes, bool rope) {
   const kv4_status shape = check_decode_shape(B, Sq, H, K);
   if (shape != KV4_OK) return shape;
   int sms = 0;
   const kv4_status st = device_info(&sms);
   if (st != KV4_OK) return st;
-  const Plan p = make_plan(B, Sq, H, K, force_splits, sms);
+  const Plan p = make_plan(B, Sq, H, K, force_splits, sms, rope);
   if (splits) *splits = p.splits;
   if (workspace_bytes) *workspace_bytes = p.ws_bytes;
   return KV4_OK;
 }
 
-kv4_status kv4_sparse_mla_decode(const void* q_dev, const uint8_t* pool_dev, int64_t num_slots,
-                                 const int32_t* page_table_dev, int64_t pt_stride, int page_size,
-                                 const int32_t* topk_idx_dev, int K, const int32_t* seq_lens_dev,
-                                 int B, int Sq, int H, float sm_scale, void* out_dev,
-                                 float* lse_dev, void* workspace_dev, size_t workspace_bytes,
-                                 int force_splits, int32_t* dev_err, kv4_stream_t stream) {
+kv4_status decode_impl(const void* q_dev, const uint8_t* pool_dev, int64_t num_slots,
+                       const int32_t* page_table_dev, int64_t pt_stride, int page_size,
+                       const int32_t* topk_idx_dev, int K, const int32_t* seq_lens_dev, int B,
+                       int Sq, int H, float sm_scale, void* out_dev, float* lse_dev,
+                       void* workspace_dev, size_t workspace_bytes, int force_splits,
+                       int32_t* dev_err, kv4_stream_t stream, bool rope) {
   const kv4_status shape = check_decode_shape(B, Sq, H, K);
   if (shape != KV4_OK) return shape;
   if (page_size != KV4_PAGE) return KV4_ERR_UNSUPPORTED;
@@ -170,7 +174,7 @@ kv4_status kv4_sparse_mla_decode(const void* q_dev, const uint8_t* pool_dev, int
   int sms = 0;
   const kv4_status st = device_info(&sms);
   if (st != KV4_OK) return st;
-  const Plan p = make_plan(B, Sq, H, K, force_splits, sms);
+  const Plan p = make_plan(B, Sq, H, K, force_splits, sms, rope);
   if (p.ws_bytes > 0 &&
       (workspace_dev == nullptr || workspace_bytes < p.ws_bytes || !aligned16(workspace_dev)))
     return KV4_ERR_WORKSPACE;
@@ -194,6 +198,7 @@ kv4_status kv4_sparse_mla_decode(const void* q_dev, const uint8_t* pool_dev, int
   a.out = out_dev;
   a.lse = lse_dev;
   a.cluster_merge = p.cluster_merge ? 1 : 0;
+  a.rope = rope ? 1 : 0;
   if (p.splits > 1 && !p.cluster_merge) {
     a.ws_o = static_cast<float*>(workspace_dev);
     a.ws_lse = a.ws_o + static_cast<size_t>(p.units) * p.splits * p.HG * KV4_LATENT;
@@ -207,11 +212,10 @@ kv4_status kv4_sparse_mla_decode(const void* q_dev, const uint8_t* pool_dev, int
              : KV4_ERR_LAUNCH;
 }
 
-kv4_status kv4_debug_gather_dequant(const uint8_t* pool_dev, int64_t num_slots,
-                                    const int32_t* page_table_dev, int64_t pt_stride,
-                                    int page_size, const int32_t* topk_idx_dev, int K,
-                                    const int32_t* seq_lens_dev, int B, int Sq, void* rows_dev,
-                                    int32_t* dev_err, kv4_stream_t stream) {
+kv4_status gather_impl(const uint8_t* pool_dev, int64_t num_slots, const int32_t* page_table_dev,
+                       int64_t pt_stride, int page_size, const int32_t* topk_idx_dev, int K,
+                       const int32_t* seq_lens_dev, int B, int Sq, void* rows_dev,
+                       int32_t* dev_err, kv4_stream_t stream, bool rope) {
   if (B < 0 || Sq < 1 || K < 0) return KV4_ERR_INVALID_ARG;
   if (page_size != KV4_PAGE) return KV4_ERR_UNSUPPORTED;
   if (B == 0 || K == 0) return KV4_OK;
@@ -223,11 +227,86 @@ kv4_status kv4_debug_gather_dequant(const uint8_t* pool_dev, int64_t num_slots,
   int sms = 0;
   const kv4_status st = device_info(&sms);
   if (st != KV4_OK) return st;
-  kv4::GatherArgs a{pool_dev, num_slots, page_table_dev, pt_stride, topk_idx_dev,
-                    K,        seq_lens_dev, B,          Sq,        rows_dev, dev_err};
+  kv4::GatherArgs a{pool_dev, num_slots,    page_table_dev, pt_stride,   topk_idx_dev, K,
+                    seq_lens_dev, B,     Sq,             rows_dev,    rope ? 1 : 0, dev_err};
   return kv4::launch_debug_gather(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
              ? KV4_OK
              : KV4_ERR_LAUNCH;
+}
+
+}  // namespace
+
+extern "C" {
+
+kv4_status kv4_quantize_write(const void* latent_dev, int64_t latent_row_stride,
+                              const void* rope_dev, int64_t rope_row_stride,
+                              const int64_t* slot_mapping_dev, int64_t n_tokens,
+                              uint8_t* pool_dev, int64_t num_slots, int32_t* dev_err,
+                              kv4_stream_t stream) {
+  return quantize_impl(latent_dev, latent_row_stride, rope_dev, rope_row_stride,
+                       slot_mapping_dev, n_tokens, pool_dev, num_slots, dev_err, stream, true);
+}
+
+kv4_status kv4_decode_plan(int B, int Sq, int H, int K, int force_splits, int* splits,
+                           size_t* workspace_bytes) {
+  return plan_impl(B, Sq, H, K, force_splits, splits, workspace_bytes, true);
+}
+
+kv4_status kv4_sparse_mla_decode(const void* q_dev, const uint8_t* pool_dev, int64_t num_slots,
+                                 const int32_t* page_table_dev, int64_t pt_stride, int page_size,
+                                 const int32_t* topk_idx_dev, int K, const int32_t* seq_lens_dev,
+                                 int B, int Sq, int H, float sm_scale, void* out_dev,
+                                 float* lse_dev, void* workspace_dev, size_t workspace_bytes,
+                                 int force_splits, int32_t* dev_err, kv4_stream_t stream) {
+  return decode_impl(q_dev, pool_dev, num_slots, page_table_dev, pt_stride, page_size,
+                     topk_idx_dev, K, seq_lens_dev, B, Sq, H, sm_scale, out_dev, lse_dev,
+                     workspace_dev, workspace_bytes, force_splits, dev_err, stream, true);
+}
+
+kv4_status kv4_debug_gather_dequant(const uint8_t* pool_dev, int64_t num_slots,
+                                    const int32_t* page_table_dev, int64_t pt_stride,
+                                    int page_size, const int32_t* topk_idx_dev, int K,
+                                    const int32_t* seq_lens_dev, int B, int Sq, void* rows_dev,
+                                    int32_t* dev_err, kv4_stream_t stream) {
+  return gather_impl(pool_dev, num_slots, page_table_dev, pt_stride, page_size, topk_idx_dev, K,
+                     seq_lens_dev, B, Sq, rows_dev, dev_err, stream, true);
+}
+
+kv4_status kv4_quantize_write_latent(const void* latent_dev, int64_t latent_row_stride,
+                                     const int64_t* slot_mapping_dev, int64_t n_tokens,
+                                     uint8_t* pool_dev, int64_t num_slots, int32_t* dev_err,
+                                     kv4_stream_t stream) {
+  return quantize_impl(latent_dev, latent_row_stride, nullptr, 0, slot_mapping_dev, n_tokens,
+                       pool_dev, num_slots, dev_err, stream, false);
+}
+
+kv4_status kv4_decode_plan_latent(int B, int Sq, int H, int K, int force_splits, int* splits,
+                                  size_t* workspace_bytes) {
+  return plan_impl(B, Sq, H, K, force_splits, splits, workspace_bytes, false);
+}
+
+kv4_status kv4_sparse_mla_decode_latent(const void* q_dev, const uint8_t* pool_dev,
+                                        int64_t num_slots, const int32_t* page_table_dev,
+                                        int64_t pt_stride, int page_size,
+                                        const int32_t* topk_idx_dev, int K,
+                                        const int32_t* seq_lens_dev, int B, int Sq, int H,
+                                        float sm_scale, void* out_dev, float* lse_dev,
+                                        void* workspace_dev, size_t workspace_bytes,
+                                        int force_splits, int32_t* dev_err,
+                                        kv4_stream_t stream) {
+  return decode_impl(q_dev, pool_dev, num_slots, page_table_dev, pt_stride, page_size,
+                     topk_idx_dev, K, seq_lens_dev, B, Sq, H, sm_scale, out_dev, lse_dev,
+                     workspace_dev, workspace_bytes, force_splits, dev_err, stream, false);
+}
+
+kv4_status kv4_debug_gather_dequant_latent(const uint8_t* pool_dev, int64_t num_slots,
+                                           const int32_t* page_table_dev, int64_t pt_stride,
+                                           int page_size, const int32_t* topk_idx_dev, int K,
+                                           const int32_t* seq_lens_dev, int B, int Sq,
+                                           void* rows_dev, int32_t* dev_err,
+                                           kv4_stream_t stream) {
+  return gather_impl(pool_dev, num_slots, page_table_dev, pt_stride, page_size, topk_idx_dev, K,
+                     seq_lens_dev, B, Sq, rows_dev, dev_err, stream, false);
 }
 
 // ---------------------------------------------------------------------------
@@ -283,7 +362,7 @@ kv4_status kv4_sparse_mla_decode_noalloc(const void* q_dev, const uint8_t* pool_
   int sms = 0;
   kv4_status st = device_info(&sms);
   if (st != KV4_OK) return st;
-  const Plan p = make_plan(B, Sq, H, K, force_splits, sms);
+  const Plan p = make_plan(B, Sq, H, K, force_splits, sms, true);
   if (p.ws_bytes > kStaticScratchBytes) return KV4_ERR_SCRATCH_LIMIT;
   void* scratch = nullptr;
   st = static_scratch(&scratch);

@@ -17,6 +17,7 @@
 namespace kv4 {
 
 constexpr int kRowBytes = 352;
+constexpr int kRowBytesLatent = 288;   // latent-only row: codes + scales, no rope
 constexpr int kLatent = 512;
 constexpr int kRope = 64;
 constexpr int kQk = 576;

@@ -19,6 +19,7 @@ struct QuantizeArgs {
   int64_t n_tokens;
   uint8_t* pool;
   int64_t num_slots;
+  int row_bytes;               // 352 (latent + rope) or 288 (latent only; rope unused)
   int32_t* dev_err;
 };
 
@@ -45,6 +46,7 @@ struct DecodeArgs {
   int fault_site;
   cudaEvent_t after_decode;    // recorded between the decode and merge kernels (may be null)
   int cluster_merge;           // splits > 1 merged inside a cluster of `splits` blocks
+  int rope;                    // 1: 352-byte rows, q of 576 columns; 0: 288-byte rows, q of 512
 };
 
 struct GatherArgs {
@@ -56,7 +58,8 @@ struct GatherArgs {
   int K;
   const int32_t* seq_lens;
   int B, Sq;
-  void* rows;                  // f16 [B, Sq, K, 576]
+  void* rows;                  // f16 [B, Sq, K, 576] (rope) or [B, Sq, K, 512]
+  int rope;                    // 1: 352-byte rows; 0: 288-byte latent-only rows
   int32_t* dev_err;
 };
 
@@ -92,12 +95,12 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), unsigned grid, unsigned block, 
 cudaError_t launch_quantize_write(const QuantizeArgs& a, int num_sms, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 cudaError_t launch_debug_gather(const GatherArgs& a, cudaStream_t stream);
-size_t decode_smem_bytes(int HG);
+size_t decode_smem_bytes(int HG, bool rope);
 // How many clusters of `splits` blocks of the HG variant can be resident at
 // once on this device (0: such clusters cannot run).  A unit split in two
 // runs as a cluster of two blocks that merge through distributed shared
 // memory; more splits merge through the workspace.
-int decode_max_active_clusters(int HG, int splits);
+int decode_max_active_clusters(int HG, int splits, bool rope);
 constexpr int kMaxClusterSplits = 2;
 
 }  // namespace kv4

@@ -10,7 +10,9 @@
 // 0..7 also convert 8 rope values each to E4M3.  The row is written with
 // coalesced stores: codes as 32 x 8 bytes, scales as 8 x 4 bytes, rope as
 // 8 x 8 bytes.  The kernel is HBM-bound (1152 bytes read, 352 written per
-// token).
+// token).  Rows of 288 bytes (the latent-only layout of the same README
+// section, for models whose keys carry no rope part) are the first 288
+// bytes of the same row: no rope is read or written.
 #include "kv4_device.cuh"
 #include "kv4_launch.h"
 
@@ -94,7 +96,7 @@ __global__ void __launch_bounds__(256) quantize_write_kernel(QuantizeArgs a) {
       for (int i = 0; i < 8; ++i) r[i] = __fdiv_rn(x[8 + i], s);
       c1 = f32x8_to_e2m1x8(r);
     }
-    uint8_t* row = a.pool + slot * kRowBytes;
+    uint8_t* row = a.pool + slot * a.row_bytes;
     *reinterpret_cast<uint2*>(row + lane * 8) = make_uint2(c0, c1);
 
     // scale bytes: lane i holds byte i; lanes 0..7 write word k = bytes 4k..4k+3
@@ -104,6 +106,8 @@ __global__ void __launch_bounds__(256) quantize_write_kernel(QuantizeArgs a) {
     const uint32_t b3 = __shfl_sync(0xFFFFFFFFu, s8, (lane * 4 + 3) & 31);
     if (lane < 8) {
       *reinterpret_cast<uint32_t*>(row + 256 + lane * 4) = b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
+    }
+    if (lane < 8 && rope != nullptr) {
       const uint4 rv = ld_stream(rope + t * a.rope_stride + lane * 8);
       const uint32_t lo = f32x2_to_e4m3x2(bf16_high(rv.x), bf16_low(rv.x)) |
                           (f32x2_to_e4m3x2(bf16_high(rv.y), bf16_low(rv.y)) << 16);

@@ -67,10 +67,15 @@ static_assert(kPvIssuers == 2 || kPvIssuers == 4, "PV issuers");
 constexpr int kBarCompute = 3;            // named barrier of the 256 compute threads (1, 2: softmax groups)
 constexpr float kRaiseThreshold = 8.0f;   // log2 units: p <= 256 between raises
 
-template <int HG>
+// ROPE: rows of 352 B (latent + rope, QK over 576 columns) or of 288 B
+// (latent only, QK over the 512 latent columns).
+template <int HG, bool ROPE>
 struct Layout {
   static constexpr int HPT = HG / 2;                                  // heads per softmax group
-  static constexpr uint32_t q_bytes = 9u * HG * 128u;                 // Q, 9 slabs
+  static constexpr int QK = ROPE ? kQk : kLatent;                     // columns of QK^T
+  static constexpr int row_bytes = ROPE ? kRowBytes : kRowBytesLatent;
+  static constexpr uint32_t q_slabs = QK / 64;                        // 64-column slabs of Q
+  static constexpr uint32_t q_bytes = q_slabs * HG * 128u;            // Q
   static constexpr uint32_t kv_off = (q_bytes + 1023u) & ~1023u;
   static constexpr uint32_t kv_bytes = 9u * kChunkBytes;              // K/V tile
   static constexpr uint32_t ctl_off = kv_off + kv_bytes;
@@ -91,7 +96,8 @@ struct Layout {
   static constexpr uint32_t xinv_off = xw_off + 2 * HG * 4;           // float [HG]
   static constexpr uint32_t end = xinv_off + HG * 4;
   // The peer's half of this block's output slice of O lands in the Q region
-  // (free after the last QK): half of HG x 512 fp32 fits in Q's 9 x HG x 128 B.
+  // (free after the last QK): half of HG x 512 fp32 fits in Q's 8 or 9 slabs
+  // of HG x 128 B.
   static_assert(HG * kLatent * 4 / 2 <= q_bytes, "peer slice must fit in the Q region");
   static_assert(xlse_off % 16 == 0 && xlse_in_off % 16 == 0, "bulk-copy operands are 16-byte aligned");
   static constexpr uint32_t smem_bytes = end + 1024;                  // + alignment slack
@@ -245,9 +251,9 @@ __device__ __forceinline__ void tmem_scale_cols(uint32_t taddr, const float* alp
   }
 }
 
-template <int HG>
+template <int HG, bool ROPE>
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
-  using L = Layout<HG>;
+  using L = Layout<HG, ROPE>;
   constexpr int HPT = L::HPT;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -319,20 +325,22 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
   // Each head is scaled by 2^-e_h (exact) so that its largest magnitude lies
   // in [2^14, 2^15): every bf16 element then converts to f16 without loss
   // (apart from elements below 2^-24 of the head's maximum); 2^e_h is folded
-  // into the head's score scale.  TPH threads own a head (its 72 16-byte
+  // into the head's score scale.  TPH threads own a head (its QK/8 16-byte
   // units interleaved among them) and reduce its maximum with shuffles.
   {
+    constexpr int UNITS = L::QK / 8;               // 16-byte units of a head
     constexpr int TPH = HG == 64 ? 4 : 8;          // threads per head
-    constexpr int UPT = 72 / TPH;                  // 16-byte units per thread
+    constexpr int UPT = UNITS / TPH;               // 16-byte units per thread
+    static_assert(UNITS % TPH == 0, "units per thread");
     const int h = tid / TPH, part = tid % TPH;
     const bool active = h < HG;                    // HG = 16 uses 128 threads
     const uint4* qsrc = reinterpret_cast<const uint4*>(
-        static_cast<const __nv_bfloat16*>(a.q) + (static_cast<int64_t>(bs) * a.H + g * HG) * kQk);
+        static_cast<const __nv_bfloat16*>(a.q) + (static_cast<int64_t>(bs) * a.H + g * HG) * L::QK);
     uint4 qv[UPT];
     uint32_t m = 0;
 #pragma unroll
     for (int j = 0; j < UPT; ++j) {
-      qv[j] = active ? __ldg(qsrc + h * 72 + part + j * TPH) : make_uint4(0, 0, 0, 0);
+      qv[j] = active ? __ldg(qsrc + h * UNITS + part + j * TPH) : make_uint4(0, 0, 0, 0);
       const uint32_t w[4] = {qv[j].x, qv[j].y, qv[j].z, qv[j].w};
 #pragma unroll
       for (int k = 0; k < 4; ++k)
@@ -421,9 +429,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
         wait(bar_part0 + 8, par);
         tc_fence_after_sync();
         issue_qk(4 * chunk_b, 4, false);
-        wait(bar_part0 + 16, par);
-        tc_fence_after_sync();
-        issue_qk(32 + qi, 1, false);                 // rope: one 16-column step each
+        if constexpr (ROPE) {
+          wait(bar_part0 + 16, par);
+          tc_fence_after_sync();
+          issue_qk(32 + qi, 1, false);               // rope: one 16-column step each
+        }
         mma_commit(bar_qk);
         if (qi >= kPvIssuers) continue;
         // a7: O^T += V^T . P^T, 4 / kPvIssuers O slabs (128 columns each) per
@@ -471,11 +481,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
     for (int h = 0; h < HPT; ++h) l_sum[h] = 0.0f;
     // Rows of the next tile travel in registers: warp w holds rows 16w..16w+15
     // as three 32-bit words per lane -- latent word wa(l), latent word wb(l),
-    // and word 64 + l (lanes 0..7: scales, 8..23: rope) -- where pass A
+    // and word 64 + l (lanes 0..7: scales, 8..23: rope, which only 352-byte
+    // rows have) -- where pass A
     // covers slabs {0,1,4,5} and pass B slabs {2,3,6,7}:
     //   wa(l) = l < 16 ? l : l + 16,   wb(l) = wa(l) + 16.
     // Each group is reloaded for the next tile right after the pass that
     // consumed it, so the gather is spread over the whole tile.
+    constexpr int kExtraLanes = ROPE ? 24 : 8;        // lanes loading words 64 + l
     const int word_a = lane < 16 ? lane : lane + 16;
     const int word_b = word_a + 16;
     uint32_t wa[16], wb[16], wex[16];
@@ -492,14 +504,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         const uint32_t* row =
-            reinterpret_cast<const uint32_t*>(a.pool + static_cast<int64_t>(sv[i]) * kRowBytes);
+            reinterpret_cast<const uint32_t*>(a.pool + static_cast<int64_t>(sv[i]) * L::row_bytes);
         w[i] = (sv[i] >= 0 && active) ? __ldg(row + word) : 0u;    // masked key: zero row
       }
     };
     if (my_tiles > 0) {
       load_words(wa, slot_s, word_a, true);
       load_words(wb, slot_s, word_b, true);
-      load_words(wex, slot_s, 64 + lane, lane < 24);
+      load_words(wex, slot_s, 64 + lane, lane < kExtraLanes);
     }
 
     // dequant store addresses (shared-window): latent word w of row r goes to
@@ -562,16 +574,18 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_part0 + 8);
       if (it + 1 < my_tiles) load_words(wb, next_slots, word_b, true);
-      // pass C: rope -> slab 8 (the previous tile's P lived there; PV is done)
-      if (lane >= 8 && lane < 24) {
+      if constexpr (ROPE) {
+        // pass C: rope -> slab 8 (the previous tile's P lived there; PV is done)
+        if (lane >= 8 && lane < 24) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          st_shared_v2(rope_base[i & 7] + (i >> 3) * 1024 + (i & 7) * 128, dequant_rope(wex[i]));
+          for (int i = 0; i < 16; ++i)
+            st_shared_v2(rope_base[i & 7] + (i >> 3) * 1024 + (i & 7) * 128, dequant_rope(wex[i]));
+        }
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_part0 + 16);
       }
-      fence_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_part0 + 16);
-      if (it + 1 < my_tiles) load_words(wex, next_slots, 64 + lane, lane < 24);
+      if (it + 1 < my_tiles) load_words(wex, next_slots, 64 + lane, lane < kExtraLanes);
 
       // ---- a2, second step: page-table entry of the key two tiles ahead
       if (resolve_ahead) {
@@ -851,7 +865,8 @@ __global__ void __launch_bounds__(256) merge_kernel(DecodeArgs a, int n_units) {
 }
 
 // Debug: the decode's index resolution and dequantization (the f16 operand
-// values) written to HBM.  One warp per (b, s, k) row.
+// values) written to HBM.  One warp per (b, s, k) row; 576 columns per row
+// for 352-byte pool rows, 512 for 288-byte (latent-only) rows.
 __global__ void __launch_bounds__(256) debug_gather_kernel(GatherArgs a) {
   const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
@@ -866,25 +881,27 @@ __global__ void __launch_bounds__(256) debug_gather_kernel(GatherArgs a) {
     slot = resolve_slot(a.topk + bs * a.K, k, a.K, l_eff, a.page_table + static_cast<int64_t>(b) * a.pt_stride,
                         a.pt_stride, a.num_slots, a.dev_err);
   slot = __shfl_sync(0xFFFFFFFFu, slot, 0);
+  const int row_bytes = a.rope ? kRowBytes : kRowBytesLatent;
   uint32_t wlo = 0, whi = 0, wex = 0;
   if (slot >= 0) {
-    const uint32_t* row = reinterpret_cast<const uint32_t*>(a.pool + static_cast<int64_t>(slot) * kRowBytes);
+    const uint32_t* row = reinterpret_cast<const uint32_t*>(a.pool + static_cast<int64_t>(slot) * row_bytes);
     wlo = __ldg(row + lane);
     whi = __ldg(row + 32 + lane);
-    wex = lane < 24 ? __ldg(row + 64 + lane) : 0u;
+    wex = lane < (a.rope ? 24 : 8) ? __ldg(row + 64 + lane) : 0u;
   }
   DequantRow d = dequant_row_words(wlo, whi, wex, lane, dequant_scale_selector(lane));
   if (slot < 0) {
     d.lat_lo = d.lat_hi = make_uint4(0, 0, 0, 0);
     d.rope = make_uint2(0, 0);
   }
-  __half* out = static_cast<__half*>(a.rows) + gw * kQk;
+  __half* out = static_cast<__half*>(a.rows) + gw * (a.rope ? kQk : kLatent);
   *reinterpret_cast<uint4*>(out + 8 * lane) = d.lat_lo;
   *reinterpret_cast<uint4*>(out + 256 + 8 * lane) = d.lat_hi;
-  if (lane >= 8 && lane < 24) *reinterpret_cast<uint2*>(out + 512 + 4 * (lane - 8)) = d.rope;
+  if (a.rope && lane >= 8 && lane < 24)
+    *reinterpret_cast<uint2*>(out + 512 + 4 * (lane - 8)) = d.rope;
 }
 
-template <int HG>
+template <int HG, bool ROPE>
 cudaError_t configure_decode() {
   static cudaError_t state = cudaErrorNotReady;   // per process; attributes are per kernel
   if (state == cudaErrorNotReady) {
@@ -892,28 +909,28 @@ cudaError_t configure_decode() {
     // kLaunchRegs registers per thread; with fewer the compute warpgroups'
     // increase could never be granted, so refuse to launch instead.
     cudaFuncAttributes attr;
-    cudaError_t e = cudaFuncGetAttributes(&attr, decode_kernel<HG>);
+    cudaError_t e = cudaFuncGetAttributes(&attr, decode_kernel<HG, ROPE>);
     if (e == cudaSuccess && (attr.numRegs != kLaunchRegs || attr.maxThreadsPerBlock < kThreads))
       e = cudaErrorInvalidConfiguration;
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(decode_kernel<HG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(Layout<HG>::smem_bytes));
+      e = cudaFuncSetAttribute(decode_kernel<HG, ROPE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(Layout<HG, ROPE>::smem_bytes));
     state = e;
   }
   return state;
 }
 
-template <int HG>
+template <int HG, bool ROPE>
 int max_active_clusters_hg(int splits) {
   static int known[kMaxClusterSplits + 1] = {};   // 0 unknown, else 1 + the count
   if (splits < 2 || splits > kMaxClusterSplits) return 0;
   if (known[splits] == 0) {
     int n = 0;
-    if (configure_decode<HG>() == cudaSuccess) {
+    if (configure_decode<HG, ROPE>() == cudaSuccess) {
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(splits);
       cfg.blockDim = dim3(kThreads);
-      cfg.dynamicSmemBytes = Layout<HG>::smem_bytes;
+      cfg.dynamicSmemBytes = Layout<HG, ROPE>::smem_bytes;
       cudaLaunchAttribute attr[1];
       attr[0].id = cudaLaunchAttributeClusterDimension;
       attr[0].val.clusterDim.x = splits;
@@ -921,7 +938,7 @@ int max_active_clusters_hg(int splits) {
       attr[0].val.clusterDim.z = 1;
       cfg.attrs = attr;
       cfg.numAttrs = 1;
-      if (cudaOccupancyMaxActiveClusters(&n, decode_kernel<HG>, &cfg) != cudaSuccess) n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, decode_kernel<HG, ROPE>, &cfg) != cudaSuccess) n = 0;
     }
     (void)cudaGetLastError();
     known[splits] = 1 + (n > 0 ? n : 0);
@@ -929,13 +946,13 @@ int max_active_clusters_hg(int splits) {
   return known[splits] - 1;
 }
 
-template <int HG>
+template <int HG, bool ROPE>
 cudaError_t launch_decode_hg(const DecodeArgs& a, cudaStream_t stream) {
-  const size_t smem = Layout<HG>::smem_bytes;
-  cudaError_t e = configure_decode<HG>();
+  const size_t smem = Layout<HG, ROPE>::smem_bytes;
+  cudaError_t e = configure_decode<HG, ROPE>();
   if (e != cudaSuccess) return e;
   const int units = a.B * a.Sq * (a.H / HG);
-  e = launch_pdl(decode_kernel<HG>, static_cast<unsigned>(units * a.splits), kThreads, smem, stream,
+  e = launch_pdl(decode_kernel<HG, ROPE>, static_cast<unsigned>(units * a.splits), kThreads, smem, stream,
                  a.cluster_merge ? a.splits : 1, a);
   if (e == cudaSuccess && a.after_decode != nullptr) e = cudaEventRecord(a.after_decode, stream);
   if (e != cudaSuccess || a.splits == 1 || a.cluster_merge) return e;
@@ -944,33 +961,49 @@ cudaError_t launch_decode_hg(const DecodeArgs& a, cudaStream_t stream) {
                     units);
 }
 
-}  // namespace
-
-size_t decode_smem_bytes(int HG) {
+template <bool ROPE>
+size_t decode_smem_bytes_r(int HG) {
   switch (HG) {
-    case 16: return Layout<16>::smem_bytes;
-    case 32: return Layout<32>::smem_bytes;
-    case 64: return Layout<64>::smem_bytes;
+    case 16: return Layout<16, ROPE>::smem_bytes;
+    case 32: return Layout<32, ROPE>::smem_bytes;
+    case 64: return Layout<64, ROPE>::smem_bytes;
     default: return 0;
   }
 }
 
-int decode_max_active_clusters(int HG, int splits) {
+template <bool ROPE>
+int decode_max_active_clusters_r(int HG, int splits) {
   switch (HG) {
-    case 16: return max_active_clusters_hg<16>(splits);
-    case 32: return max_active_clusters_hg<32>(splits);
-    case 64: return max_active_clusters_hg<64>(splits);
+    case 16: return max_active_clusters_hg<16, ROPE>(splits);
+    case 32: return max_active_clusters_hg<32, ROPE>(splits);
+    case 64: return max_active_clusters_hg<64, ROPE>(splits);
     default: return 0;
   }
+}
+
+template <bool ROPE>
+cudaError_t launch_decode_r(const DecodeArgs& a, cudaStream_t stream) {
+  switch (a.HG) {
+    case 16: return launch_decode_hg<16, ROPE>(a, stream);
+    case 32: return launch_decode_hg<32, ROPE>(a, stream);
+    case 64: return launch_decode_hg<64, ROPE>(a, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+
+size_t decode_smem_bytes(int HG, bool rope) {
+  return rope ? decode_smem_bytes_r<true>(HG) : decode_smem_bytes_r<false>(HG);
+}
+
+int decode_max_active_clusters(int HG, int splits, bool rope) {
+  return rope ? decode_max_active_clusters_r<true>(HG, splits)
+              : decode_max_active_clusters_r<false>(HG, splits);
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
-  switch (a.HG) {
-    case 16: return launch_decode_hg<16>(a, stream);
-    case 32: return launch_decode_hg<32>(a, stream);
-    case 64: return launch_decode_hg<64>(a, stream);
-    default: return cudaErrorInvalidValue;
-  }
+  return a.rope ? launch_decode_r<true>(a, stream) : launch_decode_r<false>(a, stream);
 }
 
 cudaError_t launch_debug_gather(const GatherArgs& a, cudaStream_t stream) {

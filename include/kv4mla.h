@@ -69,7 +69,8 @@ enum {
 
 enum {
   KV4_ROW_BYTES = 352, KV4_LATENT = 512, KV4_ROPE = 64, KV4_QK_DIM = 576,
-  KV4_BLOCK = 16, KV4_PAGE = 64, KV4_TILE_KEYS = 128
+  KV4_BLOCK = 16, KV4_PAGE = 64, KV4_TILE_KEYS = 128,
+  KV4_ROW_BYTES_LATENT = 288   /* latent-only row (the *_latent entry points) */
 };
 
 /* ---------------------------------------------------------------------------
@@ -151,6 +152,43 @@ kv4_status kv4_debug_gather_dequant(const uint8_t* pool_dev, int64_t num_slots,
                                     const int32_t* seq_lens_dev, int B, int Sq,
                                     void* rows_dev, int32_t* dev_err,
                                     kv4_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Latent-only rows (288 bytes).
+ * Source: README "4-bit KV cache", the GLM-5.3-Flash bullet (a 288-byte
+ * rope-free row).  A row is the first 288 bytes of the 352-byte row above --
+ * bytes [0,256) E2M1 codes, [256,288) the 32 E4M3 scales -- for models whose
+ * cached keys carry no rope part.  QK^T then runs over the 512 latent
+ * columns only, and PV over the same 512.  Arguments, layouts, ownership
+ * and errors are those of the 352-byte calls, except:
+ *   kv4_quantize_write_latent     no rope input; pool uint8 [num_slots, 288]
+ *   kv4_decode_plan_latent        the plan of kv4_sparse_mla_decode_latent
+ *   kv4_sparse_mla_decode_latent  q bf16 [B, Sq, H, 512]; pool [num_slots, 288]
+ *   kv4_debug_gather_dequant_latent  rows f16 [B, Sq, K, 512]
+ * Per byte of pool, 288-byte rows hold 2x the tokens of 576-byte FP8 rows
+ * and 1.22x those of 352-byte rows.
+ * ------------------------------------------------------------------------- */
+kv4_status kv4_quantize_write_latent(const void* latent_dev, int64_t latent_row_stride,
+                                     const int64_t* slot_mapping_dev, int64_t n_tokens,
+                                     uint8_t* pool_dev, int64_t num_slots, int32_t* dev_err,
+                                     kv4_stream_t stream);
+kv4_status kv4_decode_plan_latent(int B, int Sq, int H, int K, int force_splits,
+                                  int* splits, size_t* workspace_bytes);
+kv4_status kv4_sparse_mla_decode_latent(const void* q_dev, const uint8_t* pool_dev,
+                                        int64_t num_slots, const int32_t* page_table_dev,
+                                        int64_t pt_stride, int page_size,
+                                        const int32_t* topk_idx_dev, int K,
+                                        const int32_t* seq_lens_dev, int B, int Sq, int H,
+                                        float sm_scale, void* out_dev, float* lse_dev,
+                                        void* workspace_dev, size_t workspace_bytes,
+                                        int force_splits, int32_t* dev_err,
+                                        kv4_stream_t stream);
+kv4_status kv4_debug_gather_dequant_latent(const uint8_t* pool_dev, int64_t num_slots,
+                                           const int32_t* page_table_dev, int64_t pt_stride,
+                                           int page_size, const int32_t* topk_idx_dev, int K,
+                                           const int32_t* seq_lens_dev, int B, int Sq,
+                                           void* rows_dev, int32_t* dev_err,
+                                           kv4_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * kv4_sparse_mla_decode_noalloc -- the same decode for callers that cannot
