@@ -126,6 +126,12 @@ cudaError_t launch_quantize_write(const QuantizeArgs& a, int num_sms, cudaStream
   int64_t blocks = (warps_needed + 7) / 8;
   const int64_t cap = static_cast<int64_t>(num_sms > 0 ? num_sms : 1) * 16;
   if (blocks > cap) blocks = cap;
+  // Same shared-memory carve-out as the decode kernel, which usually follows
+  // in the stream: the SMs then need no reconfiguration between the two.
+  static const cudaError_t carveout = cudaFuncSetAttribute(
+      quantize_write_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+      cudaSharedmemCarveoutMaxShared);
+  (void)carveout;
   return launch_pdl(quantize_write_kernel, static_cast<unsigned>(blocks), 256, 0, stream, 1, a);
 }
 

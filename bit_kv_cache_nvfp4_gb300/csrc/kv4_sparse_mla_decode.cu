@@ -915,6 +915,10 @@ cudaError_t configure_decode() {
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(decode_kernel<HG, ROPE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                static_cast<int>(Layout<HG, ROPE>::smem_bytes));
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(decode_kernel<HG, ROPE>,
+                               cudaFuncAttributePreferredSharedMemoryCarveout,
+                               cudaSharedmemCarveoutMaxShared);
     state = e;
   }
   return state;
