@@ -405,6 +405,7 @@ def run_gpu(args):
 
     # end to end through the public API, host buffers in and out
     e2e = run_e2e(kv, w, dev, pool, pt, lens, flush, args)
+    cache_write = run_cache_write(kv, dev, flush, args)
     latent = None
     if not args.skip_latent:
         del pool
@@ -466,6 +467,7 @@ def run_gpu(args):
             "cpu_baseline": cpu,
             "e2e": e2e,
             "latent_rows_288B": latent,
+            "cache_write_1M_tokens": cache_write,
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clocks.summary(),
             "wall_s_timed_loop": wall,
@@ -474,6 +476,33 @@ def run_gpu(args):
     if world > 1:
         torch.distributed.destroy_process_group()
     return 0
+
+
+def run_cache_write(kv, dev, flush, args):
+    """Throughput of the cache write alone on 1,048,576 tokens (N(0,1)
+    latent and rope), with amax/6 scales and with MSE-searched scales.
+    Bytes = the bf16 input read (1152 B) + the row written (352 B) per token."""
+    n = 1 << 20
+    lat, rope = wl.sweep_rows("normal", 0, 0, n, device=dev)
+    slots = torch.arange(n, dtype=torch.int64, device=dev)
+    pool = torch.empty((n, 352), dtype=torch.uint8, device=dev)
+    res = {}
+    for name, fn in (("amax", kv.quantize_write), ("mse", kv.quantize_write_mse)):
+        for _ in range(3):
+            fn(lat, rope, slots, pool)
+        ts = []
+        for _ in range(10):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn(lat, rope, slots, pool)
+            b.record()
+            b.synchronize()
+            ts.append(a.elapsed_time(b))
+        t = sorted(ts)[len(ts) // 2] * 1e-3
+        res[name] = {"us": t * 1e6, "gbs": n * (1152 + 352) / t / 1e9}
+    del lat, rope, slots, pool
+    return res
 
 
 def run_latent_rows(kv, w, dev, q, pt, topk, lens, flush, err, args, valid):

@@ -23,7 +23,7 @@ import torch
 __all__ = [
     "Kv4Error", "library_path", "load_library", "quantize_write", "decode_plan",
     "sparse_mla_decode", "debug_gather_dequant", "set_wait_limit", "set_timing_event",
-    "quantize_write_latent", "decode_plan_latent", "sparse_mla_decode_latent",
+    "quantize_write_mse", "quantize_write_latent", "decode_plan_latent", "sparse_mla_decode_latent",
     "debug_gather_dequant_latent", "ROW_BYTES", "ROW_BYTES_LATENT", "LATENT", "ROPE", "QK_DIM", "PAGE", "DEV_BAD_SLOT", "DEV_BAD_PAGE",
     "DEV_TIMEOUT",
 ]
@@ -74,6 +74,8 @@ def load_library():
         lib.kv4_debug_gather_dequant.argtypes = [P, i64, P, i64, i32, P, i32, P, i32, i32, P, P,
                                                  P]
         lib.kv4_debug_gather_dequant.restype = i32
+        lib.kv4_quantize_write_mse.argtypes = lib.kv4_quantize_write.argtypes
+        lib.kv4_quantize_write_mse.restype = i32
         lib.kv4_quantize_write_latent.argtypes = [P, i64, P, i64, P, i64, P, P]
         lib.kv4_quantize_write_latent.restype = i32
         lib.kv4_decode_plan_latent.argtypes = lib.kv4_decode_plan.argtypes
@@ -123,13 +125,24 @@ def quantize_write(latent: torch.Tensor, rope: torch.Tensor, slot_mapping: torch
                    pool: torch.Tensor, dev_err: torch.Tensor | None = None) -> None:
     """Quantize latent bf16 [N,512] and rope bf16 [N,64] into pool uint8
     [num_slots,352] at slot_mapping int64 [N] (negative = skip)."""
+    _quantize("kv4_quantize_write", latent, rope, slot_mapping, pool, dev_err)
+
+
+def quantize_write_mse(latent: torch.Tensor, rope: torch.Tensor, slot_mapping: torch.Tensor,
+                       pool: torch.Tensor, dev_err: torch.Tensor | None = None) -> None:
+    """quantize_write with MSE-searched block scales (kv4_quantize_write_mse);
+    the rows decode with sparse_mla_decode unchanged."""
+    _quantize("kv4_quantize_write_mse", latent, rope, slot_mapping, pool, dev_err)
+
+
+def _quantize(fn, latent, rope, slot_mapping, pool, dev_err):
     lib = load_library()
     n = slot_mapping.shape[0]
     if latent.dim() != 2 or rope.dim() != 2 or latent.shape[0] != n or rope.shape[0] != n:
         raise ValueError("latent [N,512], rope [N,64] and slot_mapping [N] must agree")
     if latent.stride(1) != 1 or rope.stride(1) != 1:
         raise ValueError("latent and rope rows must be contiguous")
-    _check("kv4_quantize_write", lib.kv4_quantize_write(
+    _check(fn, getattr(lib, fn)(
         _dev(latent, "latent", torch.bfloat16, False), latent.stride(0),
         _dev(rope, "rope", torch.bfloat16, False), rope.stride(0),
         _dev(slot_mapping, "slot_mapping", torch.int64), n,

@@ -113,7 +113,7 @@ namespace {
 kv4_status quantize_impl(const void* latent_dev, int64_t latent_row_stride, const void* rope_dev,
                          int64_t rope_row_stride, const int64_t* slot_mapping_dev,
                          int64_t n_tokens, uint8_t* pool_dev, int64_t num_slots,
-                         int32_t* dev_err, kv4_stream_t stream, bool rope) {
+                         int32_t* dev_err, kv4_stream_t stream, bool rope, bool mse = false) {
   if (n_tokens < 0 || num_slots < 0) return KV4_ERR_INVALID_ARG;
   if (n_tokens == 0) return KV4_OK;
   if (!latent_dev || (rope && !rope_dev) || !slot_mapping_dev || !pool_dev)
@@ -131,7 +131,7 @@ kv4_status quantize_impl(const void* latent_dev, int64_t latent_row_stride, cons
   if (st != KV4_OK) return st;
   kv4::QuantizeArgs a{latent_dev, latent_row_stride, rope ? rope_dev : nullptr,
                       rope ? rope_row_stride : 0, slot_mapping_dev, n_tokens, pool_dev,
-                      num_slots, row_bytes, dev_err};
+                      num_slots, row_bytes, dev_err, mse ? 1 : 0};
   return kv4::launch_quantize_write(a, sms, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
              ? KV4_OK
              : KV4_ERR_LAUNCH;
@@ -270,6 +270,16 @@ kv4_status kv4_debug_gather_dequant(const uint8_t* pool_dev, int64_t num_slots,
                                     int32_t* dev_err, kv4_stream_t stream) {
   return gather_impl(pool_dev, num_slots, page_table_dev, pt_stride, page_size, topk_idx_dev, K,
                      seq_lens_dev, B, Sq, rows_dev, dev_err, stream, true);
+}
+
+kv4_status kv4_quantize_write_mse(const void* latent_dev, int64_t latent_row_stride,
+                                  const void* rope_dev, int64_t rope_row_stride,
+                                  const int64_t* slot_mapping_dev, int64_t n_tokens,
+                                  uint8_t* pool_dev, int64_t num_slots, int32_t* dev_err,
+                                  kv4_stream_t stream) {
+  return quantize_impl(latent_dev, latent_row_stride, rope_dev, rope_row_stride,
+                       slot_mapping_dev, n_tokens, pool_dev, num_slots, dev_err, stream, true,
+                       true);
 }
 
 kv4_status kv4_quantize_write_latent(const void* latent_dev, int64_t latent_row_stride,

@@ -21,6 +21,7 @@ struct QuantizeArgs {
   int64_t num_slots;
   int row_bytes;               // 352 (latent + rope) or 288 (latent only; rope unused)
   int32_t* dev_err;
+  int mse;                     // 1: MSE-searched block scales instead of amax/6
 };
 
 struct DecodeArgs {

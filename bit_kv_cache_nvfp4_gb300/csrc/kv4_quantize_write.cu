@@ -13,6 +13,14 @@
 // token).  Rows of 288 bytes (the latent-only layout of the same README
 // section, for models whose keys carry no rope part) are the first 288
 // bytes of the same row: no rope is read or written.
+//
+// With a.mse set, each block's scale is searched instead (README "4-bit KV
+// cache", DeepSeek V4 Pro bullet: "an MSE-searched scale"; the search rule
+// is this project's reading): the candidates are the E4M3 scale bytes
+// c0-8 .. c0+1 around c0 = E4M3(amax/6) (clipped to 0..126); each gives codes
+// E2M1(x/s) and the error sum_i (x_i - dec(code_i) s)^2 in IEEE fp32, in
+// element order with every operation rounded separately; the smallest error
+// wins, the lowest scale byte on ties.
 #include "kv4_device.cuh"
 #include "kv4_launch.h"
 
@@ -53,6 +61,30 @@ __device__ __forceinline__ uint4 ld_stream(const void* p) {
   return v;
 }
 
+// E2M1 magnitude of a 4-bit code's low three bits: 0, 0.5, 1, 1.5, 2, 3, 4, 6
+// (two exponent bits with bias 1, one mantissa bit; exponent 0 subnormal).
+__device__ __forceinline__ float e2m1_value(uint32_t code) {
+  const uint32_t e = (code >> 1) & 3u, m = code & 1u;
+  const float mag = e == 0 ? 0.5f * static_cast<float>(m)
+                           : __uint_as_float((126u + e) << 23) * (1.0f + 0.5f * static_cast<float>(m));
+  return (code & 8u) ? -mag : mag;
+}
+
+// Squared reconstruction error of a block coded as (w0, w1) with scale s,
+// summed in element order with each operation rounded to nearest.
+__device__ __forceinline__ float block_error(const float (&x)[16], uint32_t w0, uint32_t w1,
+                                             float s) {
+  float err = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const uint32_t w = i < 8 ? w0 : w1;
+    const uint32_t code = (w >> (4 * (i & 7))) & 0xFu;
+    const float d = __fsub_rn(x[i], __fmul_rn(e2m1_value(code), s));
+    err = __fadd_rn(err, __fmul_rn(d, d));
+  }
+  return err;
+}
+
 __global__ void __launch_bounds__(256) quantize_write_kernel(QuantizeArgs a) {
   // the previous kernel (e.g. a decode still gathering from the pool) must
   // be complete before any row is written
@@ -84,17 +116,41 @@ __global__ void __launch_bounds__(256) quantize_write_kernel(QuantizeArgs a) {
     float amax = 0.0f;
 #pragma unroll
     for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
-    const uint32_t s8 = f32x2_to_e4m3x2(0.0f, __fdiv_rn(amax, 6.0f)) & 0xFFu;
-    const float s = e4m3_to_float(s8);
+    uint32_t s8 = f32x2_to_e4m3x2(0.0f, __fdiv_rn(amax, 6.0f)) & 0xFFu;
+    // codes of the block for scale byte sb (all zero when it decodes to 0)
+    auto encode = [&](uint32_t sb, uint32_t& w0, uint32_t& w1) {
+      const float s = e4m3_to_float(sb);
+      w0 = w1 = 0;
+      if (s != 0.0f) {
+        float r[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) r[i] = __fdiv_rn(x[i], s);
+        w0 = f32x8_to_e2m1x8(r);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) r[i] = __fdiv_rn(x[8 + i], s);
+        w1 = f32x8_to_e2m1x8(r);
+      }
+      return s;
+    };
     uint32_t c0 = 0, c1 = 0;
-    if (s != 0.0f) {
-      float r[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) r[i] = __fdiv_rn(x[i], s);
-      c0 = f32x8_to_e2m1x8(r);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) r[i] = __fdiv_rn(x[8 + i], s);
-      c1 = f32x8_to_e2m1x8(r);
+    if (!a.mse) {
+      encode(s8, c0, c1);
+    } else {
+      const uint32_t lo = s8 >= 8 ? s8 - 8 : 0, hi = s8 + 1 < 126 ? s8 + 1 : 126;
+      float best = 0.0f;
+      uint32_t best_sb = 0xFFFFFFFFu;
+      for (uint32_t sb = lo; sb <= hi; ++sb) {
+        uint32_t w0, w1;
+        const float s = encode(sb, w0, w1);
+        const float err = block_error(x, w0, w1, s);
+        if (best_sb == 0xFFFFFFFFu || err < best) {
+          best = err;
+          best_sb = sb;
+          c0 = w0;
+          c1 = w1;
+        }
+      }
+      s8 = best_sb;
     }
     uint8_t* row = a.pool + slot * a.row_bytes;
     *reinterpret_cast<uint2*>(row + lane * 8) = make_uint2(c0, c1);

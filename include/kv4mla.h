@@ -93,6 +93,25 @@ kv4_status kv4_quantize_write(const void* latent_dev, int64_t latent_row_stride,
                               int32_t* dev_err, kv4_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * kv4_quantize_write_mse -- kv4_quantize_write with searched block scales.
+ * Source: README "4-bit KV cache", DeepSeek V4 Pro bullet ("an MSE-searched
+ * scale"); the page gives no rule, this is the project's reading.  Same
+ * arguments, row layout and errors as kv4_quantize_write.  Per block: the
+ * candidate scale bytes are c0-8 .. c0+1 (clipped to 0..126) around
+ * c0 = E4M3(amax/6); each candidate s gives codes E2M1(x/s) (fp32 division,
+ * round half to even; s == 0 gives zero codes) and the error
+ * sum_i (x_i - dec(code_i) * s)^2 in IEEE fp32, element order, every
+ * operation rounded to nearest; the smallest error wins, the lowest scale
+ * byte on ties.  The rows decode with kv4_sparse_mla_decode unchanged.
+ * Bit-identical to the CPU oracle.
+ * ------------------------------------------------------------------------- */
+kv4_status kv4_quantize_write_mse(const void* latent_dev, int64_t latent_row_stride,
+                                  const void* rope_dev, int64_t rope_row_stride,
+                                  const int64_t* slot_mapping_dev, int64_t n_tokens,
+                                  uint8_t* pool_dev, int64_t num_slots,
+                                  int32_t* dev_err, kv4_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * kv4_decode_plan -- number of split-K partitions and workspace bytes that
  * kv4_sparse_mla_decode will use for this shape on the current device.
  * force_splits > 0 requests that many partitions (clamped to the number of

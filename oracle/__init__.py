@@ -75,6 +75,10 @@ def _load():
         lib.kv4ref_dequant_row.restype = None
         lib.kv4ref_quantize_write.argtypes = [P, i64, P, i64, P, i64, P, i64]
         lib.kv4ref_quantize_write.restype = i32
+        lib.kv4ref_quantize_row_mse.argtypes = [P, P, P]
+        lib.kv4ref_quantize_row_mse.restype = None
+        lib.kv4ref_quantize_write_mse.argtypes = [P, i64, P, i64, P, i64, P, i64]
+        lib.kv4ref_quantize_write_mse.restype = i32
         lib.kv4ref_resolve_slots.argtypes = [P, i64, i32, P, i32, P, i32, i32, i64, P]
         lib.kv4ref_resolve_slots.restype = i32
         lib.kv4ref_gather_dequant.argtypes = [P, i64, P, i64, i32, P, i32, P, i32, i32, P, P]
@@ -141,6 +145,16 @@ def quantize_row(latent_bits: np.ndarray, rope_bits: np.ndarray) -> np.ndarray:
     return row
 
 
+def quantize_row_mse(latent_bits: np.ndarray, rope_bits: np.ndarray) -> np.ndarray:
+    """The row with MSE-searched block scales (see kv4ref.h)."""
+    lat = _as(latent_bits, np.uint16)
+    rope = _as(rope_bits, np.uint16)
+    assert lat.size == 512 and rope.size == 64
+    row = np.zeros(352, dtype=np.uint8)
+    _load().kv4ref_quantize_row_mse(_ptr(lat), _ptr(rope), _ptr(row))
+    return row
+
+
 def dequant_row(row: np.ndarray) -> np.ndarray:
     row = _as(row, np.uint8)
     assert row.size == 352
@@ -158,6 +172,19 @@ def quantize_write(latent_bits, rope_bits, slot_mapping, pool) -> int:
     assert pool.dtype == np.uint8 and pool.flags["C_CONTIGUOUS"]
     n = slots.shape[0]
     return int(_load().kv4ref_quantize_write(
+        _ptr(lat), lat.shape[1] if lat.ndim == 2 else 512,
+        _ptr(rope), rope.shape[1] if rope.ndim == 2 else 64,
+        _ptr(slots), n, _ptr(pool), pool.shape[0]))
+
+
+def quantize_write_mse(latent_bits, rope_bits, slot_mapping, pool) -> int:
+    """quantize_write with MSE-searched block scales."""
+    lat = _as(latent_bits, np.uint16)
+    rope = _as(rope_bits, np.uint16)
+    slots = _as(slot_mapping, np.int64)
+    assert pool.dtype == np.uint8 and pool.flags["C_CONTIGUOUS"]
+    n = slots.shape[0]
+    return int(_load().kv4ref_quantize_write_mse(
         _ptr(lat), lat.shape[1] if lat.ndim == 2 else 512,
         _ptr(rope), rope.shape[1] if rope.ndim == 2 else 64,
         _ptr(slots), n, _ptr(pool), pool.shape[0]))

@@ -62,6 +62,23 @@ void kv4ref_quantize_row(const uint16_t* latent_bf16, const uint16_t* rope_bf16,
                          uint8_t* row);
 void kv4ref_dequant_row(const uint8_t* row, float* out576);
 
+/* ---- the same row with MSE-searched block scales ------------------------
+ * README "4-bit KV cache", DeepSeek V4 Pro bullet ("an MSE-searched scale");
+ * the page gives no search rule, and this project's reading is: for each
+ * block, c0 = E4M3_RNE(amax/6) as above; the candidate scale bytes are
+ * c0-8 .. c0+1 (clipped to 0..126: one binade below and one step above);
+ * each candidate s gives codes E2M1_RNE(x/s) (s == 0: all zero) and the
+ * error E = sum_i (x_i - dec(code_i)*s)^2, computed in IEEE fp32 in element
+ * order (each difference, square and sum rounded to nearest); the block
+ * takes the candidate with the smallest E, the lowest scale byte on ties.
+ * The rope part is as above. */
+void kv4ref_quantize_row_mse(const uint16_t* latent_bf16, const uint16_t* rope_bf16,
+                             uint8_t* row);
+int kv4ref_quantize_write_mse(const uint16_t* latent_bf16, int64_t latent_stride,
+                              const uint16_t* rope_bf16, int64_t rope_stride,
+                              const int64_t* slot_mapping, int64_t n_tokens,
+                              uint8_t* pool, int64_t num_slots);
+
 /* ---- quantized write into a paged pool [num_slots, 352] -----------------
  * Token t goes to pool[slot_mapping[t]]; slot < 0 is skipped; slot >=
  * num_slots is skipped and reported with KV4REF_ERR_SLOT. */

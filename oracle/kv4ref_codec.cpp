@@ -145,6 +145,66 @@ void kv4ref_dequant_row(const uint8_t* row, float* out576) {
   for (int r = 0; r < 64; ++r) out576[512 + r] = kv4ref_dec_e4m3(row[288 + r]);
 }
 
+void kv4ref_quantize_row_mse(const uint16_t* latent_bf16, const uint16_t* rope_bf16,
+                             uint8_t* row) {
+  uint8_t codes[512];
+  for (int blk = 0; blk < 32; ++blk) {
+    float x[16];
+    float amax = 0.0f;
+    for (int i = 0; i < 16; ++i) {
+      x[i] = bf16_to_float(latent_bf16[blk * 16 + i]);
+      const float a = std::fabs(x[i]);
+      if (a > amax) amax = a;
+    }
+    const int c0 = kv4ref_enc_e4m3(amax / 6.0f);     /* the amax/6 scale byte */
+    const int lo = c0 - 8 < 0 ? 0 : c0 - 8;
+    const int hi = c0 + 1 > 126 ? 126 : c0 + 1;
+    int best_c = -1;
+    float best_err = 0.0f;
+    uint8_t best_codes[16] = {0};
+    for (int c = lo; c <= hi; ++c) {
+      const float s = kv4ref_dec_e4m3(static_cast<uint8_t>(c));
+      uint8_t cand[16];
+      float err = 0.0f;
+      for (int i = 0; i < 16; ++i) {
+        cand[i] = (s == 0.0f) ? 0 : kv4ref_enc_e2m1(x[i] / s);
+        const float d = x[i] - kv4ref_dec_e2m1(cand[i]) * s;   /* product exact */
+        err = err + d * d;
+      }
+      if (best_c < 0 || err < best_err) {
+        best_c = c;
+        best_err = err;
+        for (int i = 0; i < 16; ++i) best_codes[i] = cand[i];
+      }
+    }
+    row[256 + blk] = static_cast<uint8_t>(best_c);
+    for (int i = 0; i < 16; ++i) codes[blk * 16 + i] = best_codes[i];
+  }
+  for (int j = 0; j < 256; ++j)
+    row[j] = static_cast<uint8_t>(codes[2 * j] | (codes[2 * j + 1] << 4));
+  for (int r = 0; r < 64; ++r)
+    row[288 + r] = kv4ref_enc_e4m3(bf16_to_float(rope_bf16[r]));
+}
+
+int kv4ref_quantize_write_mse(const uint16_t* latent_bf16, int64_t latent_stride,
+                              const uint16_t* rope_bf16, int64_t rope_stride,
+                              const int64_t* slot_mapping, int64_t n_tokens,
+                              uint8_t* pool, int64_t num_slots) {
+  if (n_tokens < 0 || num_slots < 0) return KV4REF_ERR_ARG;
+  if (n_tokens > 0 && (!latent_bf16 || !rope_bf16 || !slot_mapping || !pool))
+    return KV4REF_ERR_ARG;
+  if (latent_stride < 512 || rope_stride < 64) return KV4REF_ERR_ARG;
+  int status = KV4REF_OK;
+  for (int64_t t = 0; t < n_tokens; ++t) {
+    const int64_t slot = slot_mapping[t];
+    if (slot < 0) continue;
+    if (slot >= num_slots) { status = KV4REF_ERR_SLOT; continue; }
+    kv4ref_quantize_row_mse(latent_bf16 + t * latent_stride,
+                            rope_bf16 + t * rope_stride, pool + slot * 352);
+  }
+  return status;
+}
+
 int kv4ref_quantize_write(const uint16_t* latent_bf16, int64_t latent_stride,
                           const uint16_t* rope_bf16, int64_t rope_stride,
                           const int64_t* slot_mapping, int64_t n_tokens,
