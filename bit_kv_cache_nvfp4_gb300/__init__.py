@@ -24,7 +24,8 @@ __all__ = [
     "Kv4Error", "library_path", "load_library", "quantize_write", "decode_plan",
     "sparse_mla_decode", "debug_gather_dequant", "set_wait_limit", "set_timing_event",
     "quantize_write_mse", "quantize_write_latent", "decode_plan_latent", "sparse_mla_decode_latent",
-    "debug_gather_dequant_latent", "ROW_BYTES", "ROW_BYTES_LATENT", "LATENT", "ROPE", "QK_DIM", "PAGE", "DEV_BAD_SLOT", "DEV_BAD_PAGE",
+    "debug_gather_dequant_latent", "sparse_mla_decode_partial", "dcp_mask_topk",
+    "merge_partials", "gather_partials", "dcp_sparse_mla_decode", "ROW_BYTES", "ROW_BYTES_LATENT", "LATENT", "ROPE", "QK_DIM", "PAGE", "DEV_BAD_SLOT", "DEV_BAD_PAGE",
     "DEV_TIMEOUT",
 ]
 
@@ -76,6 +77,12 @@ def load_library():
         lib.kv4_debug_gather_dequant.restype = i32
         lib.kv4_quantize_write_mse.argtypes = lib.kv4_quantize_write.argtypes
         lib.kv4_quantize_write_mse.restype = i32
+        lib.kv4_sparse_mla_decode_partial.argtypes = lib.kv4_sparse_mla_decode.argtypes
+        lib.kv4_sparse_mla_decode_partial.restype = i32
+        lib.kv4_dcp_mask_topk.argtypes = [P, P, i64, P, i32, i32, i32, i32, i32, P, P]
+        lib.kv4_dcp_mask_topk.restype = i32
+        lib.kv4_merge_partials.argtypes = [P, P, i32, i64, P, P, P]
+        lib.kv4_merge_partials.restype = i32
         lib.kv4_quantize_write_latent.argtypes = [P, i64, P, i64, P, i64, P, P]
         lib.kv4_quantize_write_latent.restype = i32
         lib.kv4_decode_plan_latent.argtypes = lib.kv4_decode_plan.argtypes
@@ -224,8 +231,81 @@ def sparse_mla_decode_latent(q: torch.Tensor, pool: torch.Tensor, page_table: to
                    force_splits, dev_err)
 
 
+def sparse_mla_decode_partial(q: torch.Tensor, pool: torch.Tensor, page_table: torch.Tensor,
+                              topk_idx: torch.Tensor, seq_lens: torch.Tensor, sm_scale: float,
+                              out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
+                              workspace: torch.Tensor | None = None, force_splits: int = 0,
+                              dev_err: torch.Tensor | None = None):
+    """sparse_mla_decode with an fp32 output: one context-parallel rank's
+    normalized partial (o fp32 [B,Sq,H,512], lse fp32 [B,Sq,H])."""
+    if out is None:
+        B, Sq, H, _ = q.shape
+        out = torch.empty((B, Sq, H, LATENT), dtype=torch.float32, device=q.device)
+    return _decode(False, q, pool, page_table, topk_idx, seq_lens, sm_scale, out, lse, workspace,
+                   force_splits, dev_err, partial=True)
+
+
+def dcp_mask_topk(topk_idx: torch.Tensor, page_table: torch.Tensor, seq_lens: torch.Tensor,
+                  world: int, rank: int) -> torch.Tensor:
+    """The top-k list of context-parallel rank ``rank`` of ``world``: the
+    positions whose physical page p has p % world == rank, -1 elsewhere."""
+    lib = load_library()
+    B, Sq, K = topk_idx.shape
+    out = torch.empty_like(topk_idx)
+    _check("kv4_dcp_mask_topk", lib.kv4_dcp_mask_topk(
+        _dev(topk_idx, "topk_idx", torch.int32), _dev(page_table, "page_table", torch.int32),
+        page_table.shape[1], _dev(seq_lens, "seq_lens", torch.int32), B, Sq, K, int(world),
+        int(rank), _dev(out, "topk_out", torch.int32), _stream(topk_idx.device)))
+    return out
+
+
+def merge_partials(o_parts: torch.Tensor, lse_parts: torch.Tensor):
+    """Log-sum-exp merge of R partials: o_parts fp32 [R, ..., 512], lse_parts
+    fp32 [R, ...] -> (out bf16 [..., 512], lse fp32 [...])."""
+    lib = load_library()
+    R = o_parts.shape[0]
+    shape = tuple(lse_parts.shape[1:])
+    n_rows = lse_parts[0].numel()
+    if tuple(o_parts.shape[1:-1]) != shape or o_parts.shape[-1] != LATENT:
+        raise ValueError("o_parts must be [R, ..., 512] and lse_parts [R, ...]")
+    out = torch.empty(shape + (LATENT,), dtype=torch.bfloat16, device=o_parts.device)
+    lse = torch.empty(shape, dtype=torch.float32, device=o_parts.device)
+    _check("kv4_merge_partials", lib.kv4_merge_partials(
+        _dev(o_parts, "o_parts", torch.float32), _dev(lse_parts, "lse_parts", torch.float32), R,
+        n_rows, _dev(out, "out", torch.bfloat16), _dev(lse, "lse", torch.float32),
+        _stream(o_parts.device)))
+    return out, lse
+
+
+def gather_partials(o: torch.Tensor, lse: torch.Tensor, group=None):
+    """All-gather of every rank's (o, lse) over ``group`` (torch.distributed):
+    returns o_parts [world, *o.shape] and lse_parts [world, *lse.shape]."""
+    import torch.distributed as dist
+    world = dist.get_world_size(group)
+    o_list = [torch.empty_like(o) for _ in range(world)]
+    lse_list = [torch.empty_like(lse) for _ in range(world)]
+    dist.all_gather(o_list, o.contiguous(), group=group)
+    dist.all_gather(lse_list, lse.contiguous(), group=group)
+    return torch.stack(o_list), torch.stack(lse_list)
+
+
+def dcp_sparse_mla_decode(q, pool, page_table, topk_idx, seq_lens, sm_scale, group=None,
+                          dev_err=None):
+    """One decode step with the context split over the ranks of ``group``:
+    each rank decodes the keys on its pages (its pool holds them), the ranks
+    all-gather their fp32 (o, lse), and every rank merges them into the full
+    result (out bf16 [B,Sq,H,512], lse fp32 [B,Sq,H])."""
+    import torch.distributed as dist
+    world, rank = dist.get_world_size(group), dist.get_rank(group)
+    mine = dcp_mask_topk(topk_idx, page_table, seq_lens, world, rank)
+    o, lse = sparse_mla_decode_partial(q, pool, page_table, mine, seq_lens, sm_scale,
+                                       dev_err=dev_err)
+    o_parts, lse_parts = gather_partials(o, lse, group)
+    return merge_partials(o_parts, lse_parts)
+
+
 def _decode(latent_only, q, pool, page_table, topk_idx, seq_lens, sm_scale, out, lse, workspace,
-            force_splits, dev_err):
+            force_splits, dev_err, partial=False):
     lib = load_library()
     B, Sq, H, D = q.shape
     qk, row = (LATENT, ROW_BYTES_LATENT) if latent_only else (QK_DIM, ROW_BYTES)
@@ -239,9 +319,11 @@ def _decode(latent_only, q, pool, page_table, topk_idx, seq_lens, sm_scale, out,
     dev = q.device
     if out is None:
         out = torch.empty((B, Sq, H, LATENT), dtype=torch.bfloat16, device=dev)
+    out_dtype = torch.float32 if partial else torch.bfloat16
     if lse is None:
         lse = torch.empty((B, Sq, H), dtype=torch.float32, device=dev)
-    fn = "kv4_sparse_mla_decode_latent" if latent_only else "kv4_sparse_mla_decode"
+    fn = ("kv4_sparse_mla_decode_latent" if latent_only else
+          "kv4_sparse_mla_decode_partial" if partial else "kv4_sparse_mla_decode")
     splits, ws_bytes = (decode_plan_latent if latent_only else decode_plan)(B, Sq, H, K,
                                                                            force_splits)
     if workspace is None:
@@ -252,7 +334,7 @@ def _decode(latent_only, q, pool, page_table, topk_idx, seq_lens, sm_scale, out,
         _dev(q, "q", torch.bfloat16), _dev(pool, "pool", torch.uint8), pool.shape[0],
         _dev(page_table, "page_table", torch.int32), page_table.shape[1], PAGE,
         _dev(topk_idx, "topk_idx", torch.int32), K, _dev(seq_lens, "seq_lens", torch.int32),
-        B, Sq, H, float(sm_scale), _dev(out, "out", torch.bfloat16),
+        B, Sq, H, float(sm_scale), _dev(out, "out", out_dtype),
         _dev(lse, "lse", torch.float32), ws_ptr, ws_len, force_splits, _err_ptr(dev_err),
         _stream(dev)))
     return out, lse

@@ -19,7 +19,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(HERE, "libkv4mla.so")
-SOURCES = ["kv4_capi.cu", "kv4_quantize_write.cu", "kv4_sparse_mla_decode.cu"]
+SOURCES = ["kv4_capi.cu", "kv4_quantize_write.cu", "kv4_sparse_mla_decode.cu", "kv4_dcp.cu"]
 HEADERS = ["kv4_device.cuh", "kv4_launch.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

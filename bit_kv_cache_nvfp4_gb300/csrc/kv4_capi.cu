@@ -155,7 +155,7 @@ kv4_status decode_impl(const void* q_dev, const uint8_t* pool_dev, int64_t num_s
                        const int32_t* topk_idx_dev, int K, const int32_t* seq_lens_dev, int B,
                        int Sq, int H, float sm_scale, void* out_dev, float* lse_dev,
                        void* workspace_dev, size_t workspace_bytes, int force_splits,
-                       int32_t* dev_err, kv4_stream_t stream, bool rope) {
+                       int32_t* dev_err, kv4_stream_t stream, bool rope, bool out_f32 = false) {
   const kv4_status shape = check_decode_shape(B, Sq, H, K);
   if (shape != KV4_OK) return shape;
   if (page_size != KV4_PAGE) return KV4_ERR_UNSUPPORTED;
@@ -199,6 +199,7 @@ kv4_status decode_impl(const void* q_dev, const uint8_t* pool_dev, int64_t num_s
   a.lse = lse_dev;
   a.cluster_merge = p.cluster_merge ? 1 : 0;
   a.rope = rope ? 1 : 0;
+  a.out_f32 = out_f32 ? 1 : 0;
   if (p.splits > 1 && !p.cluster_merge) {
     a.ws_o = static_cast<float*>(workspace_dev);
     a.ws_lse = a.ws_o + static_cast<size_t>(p.units) * p.splits * p.HG * KV4_LATENT;
@@ -280,6 +281,55 @@ kv4_status kv4_quantize_write_mse(const void* latent_dev, int64_t latent_row_str
   return quantize_impl(latent_dev, latent_row_stride, rope_dev, rope_row_stride,
                        slot_mapping_dev, n_tokens, pool_dev, num_slots, dev_err, stream, true,
                        true);
+}
+
+kv4_status kv4_sparse_mla_decode_partial(const void* q_dev, const uint8_t* pool_dev,
+                                         int64_t num_slots, const int32_t* page_table_dev,
+                                         int64_t pt_stride, int page_size,
+                                         const int32_t* topk_idx_dev, int K,
+                                         const int32_t* seq_lens_dev, int B, int Sq, int H,
+                                         float sm_scale, float* o_dev, float* lse_dev,
+                                         void* workspace_dev, size_t workspace_bytes,
+                                         int force_splits, int32_t* dev_err,
+                                         kv4_stream_t stream) {
+  return decode_impl(q_dev, pool_dev, num_slots, page_table_dev, pt_stride, page_size,
+                     topk_idx_dev, K, seq_lens_dev, B, Sq, H, sm_scale, o_dev, lse_dev,
+                     workspace_dev, workspace_bytes, force_splits, dev_err, stream, true, true);
+}
+
+kv4_status kv4_dcp_mask_topk(const int32_t* topk_idx_dev, const int32_t* page_table_dev,
+                             int64_t pt_stride, const int32_t* seq_lens_dev, int B, int Sq,
+                             int K, int world, int rank, int32_t* topk_out_dev,
+                             kv4_stream_t stream) {
+  if (B < 0 || Sq < 1 || K < 0 || pt_stride < 1 || world < 1 || rank < 0 || rank >= world)
+    return KV4_ERR_INVALID_ARG;
+  if (B == 0 || K == 0) return KV4_OK;
+  if (!topk_idx_dev || !page_table_dev || !seq_lens_dev || !topk_out_dev)
+    return KV4_ERR_INVALID_ARG;
+  int sms = 0;
+  const kv4_status st = device_info(&sms);
+  if (st != KV4_OK) return st;
+  return kv4::launch_dcp_mask_topk(topk_idx_dev, page_table_dev, pt_stride, seq_lens_dev, B, Sq,
+                                   K, world, rank, topk_out_dev,
+                                   reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? KV4_OK
+             : KV4_ERR_LAUNCH;
+}
+
+kv4_status kv4_merge_partials(const float* o_parts_dev, const float* lse_parts_dev, int R,
+                              int64_t n_rows, void* out_dev, float* lse_dev,
+                              kv4_stream_t stream) {
+  if (R < 1 || n_rows < 0) return KV4_ERR_INVALID_ARG;
+  if (n_rows == 0) return KV4_OK;
+  if (!o_parts_dev || !lse_parts_dev || !out_dev || !lse_dev) return KV4_ERR_INVALID_ARG;
+  if (!aligned16(o_parts_dev) || !aligned16(out_dev)) return KV4_ERR_INVALID_ARG;
+  int sms = 0;
+  const kv4_status st = device_info(&sms);
+  if (st != KV4_OK) return st;
+  return kv4::launch_merge_partials(o_parts_dev, lse_parts_dev, R, n_rows, out_dev, lse_dev,
+                                    reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? KV4_OK
+             : KV4_ERR_LAUNCH;
 }
 
 kv4_status kv4_quantize_write_latent(const void* latent_dev, int64_t latent_row_stride,

@@ -1,0 +1,118 @@
+// kv4_dcp.cu -- decode-context parallelism over the NVFP4 pool (numinousmuses
+// "inference-optimizations" README, "Parallelism and disaggregation": each
+// rank attends over the part of the context it holds and the ranks' (o, lse)
+// are merged).
+//
+// Ownership (this project's reading; the page names no rule): physical page p
+// of the pool lives on rank p mod world.  A rank's top-k list keeps the
+// positions whose page it owns and replaces the others by -1 (masked), so
+// the ranks partition every query's keys.  A position outside [0, L_eff)
+// stays masked everywhere; a position whose page-table entry cannot be read
+// (page index past the table or a negative entry) is kept on rank 0 only, so
+// that exactly one rank's decode reports it.  After each rank's decode has
+// written its normalized fp32 o and its lse, and the ranks have exchanged
+// them (an all-gather), merge_partials_kernel combines the R partials of
+// every (query token, head) row by log-sum-exp into the bf16 output.
+#include "kv4_device.cuh"
+#include "kv4_launch.h"
+
+#include <math.h>
+
+namespace kv4 {
+namespace {
+
+__global__ void __launch_bounds__(256) dcp_mask_topk_kernel(const int32_t* topk,
+                                                            const int32_t* page_table,
+                                                            int64_t pt_stride,
+                                                            const int32_t* seq_lens, int B,
+                                                            int Sq, int K, int world, int rank,
+                                                            int32_t* topk_out) {
+  grid_dependency_wait();
+  grid_launch_dependents();
+  const int64_t n = static_cast<int64_t>(B) * Sq * K;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t bs = i / K;
+    const int b = static_cast<int>(bs / Sq), s = static_cast<int>(bs % Sq);
+    const int64_t l_eff = static_cast<int64_t>(seq_lens[b]) - (Sq - 1 - s);
+    const int32_t idx = topk[i];
+    int32_t keep = -1;
+    if (idx >= 0 && idx < l_eff) {
+      const int64_t pi = idx / kPage;
+      const int32_t page = pi < pt_stride ? page_table[static_cast<int64_t>(b) * pt_stride + pi] : -1;
+      if (page < 0) keep = rank == 0 ? idx : -1;             // unreadable: rank 0 reports it
+      else if (page % world == rank) keep = idx;
+    }
+    topk_out[i] = keep;
+  }
+}
+
+// One warp per row: out = sum_r exp(lse_r - m) o_r / sum_r exp(lse_r - m),
+// lse = m + log sum_r exp(lse_r - m), m = max_r lse_r; a partial with
+// lse = -inf has weight 0; no finite lse gives out = 0, lse = -inf.
+__global__ void __launch_bounds__(256) merge_partials_kernel(const float* o_parts,
+                                                             const float* lse_parts, int R,
+                                                             int64_t n_rows,
+                                                             __nv_bfloat16* out, float* lse) {
+  grid_dependency_wait();
+  grid_launch_dependents();
+  const int64_t row = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (row >= n_rows) return;
+  float m = -INFINITY;
+  for (int r = 0; r < R; ++r) m = fmaxf(m, lse_parts[r * n_rows + row]);
+  float4 acc[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+  float wsum = 0.0f;
+  if (m != -INFINITY) {
+    for (int r = 0; r < R; ++r) {
+      const float lr = lse_parts[r * n_rows + row];
+      if (lr == -INFINITY) continue;
+      const float w = expf(lr - m);
+      wsum += w;
+      const float4* o = reinterpret_cast<const float4*>(o_parts + (r * n_rows + row) * kLatent);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float4 v = o[j * 32 + lane];
+        acc[j].x += w * v.x; acc[j].y += w * v.y; acc[j].z += w * v.z; acc[j].w += w * v.w;
+      }
+    }
+  }
+  const float inv = wsum > 0.0f ? 1.0f / wsum : 0.0f;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(acc[j].x * inv, acc[j].y * inv);
+    const __nv_bfloat162 hi = __floats2bfloat162_rn(acc[j].z * inv, acc[j].w * inv);
+    uint2 pk;
+    pk.x = *reinterpret_cast<const uint32_t*>(&lo);
+    pk.y = *reinterpret_cast<const uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(out + row * kLatent + j * 128 + lane * 4) = pk;
+  }
+  if (lane == 0) lse[row] = wsum > 0.0f ? m + logf(wsum) : -INFINITY;
+}
+
+}  // namespace
+
+cudaError_t launch_dcp_mask_topk(const int32_t* topk, const int32_t* page_table,
+                                 int64_t pt_stride, const int32_t* seq_lens, int B, int Sq,
+                                 int K, int world, int rank, int32_t* topk_out,
+                                 cudaStream_t stream) {
+  const int64_t n = static_cast<int64_t>(B) * Sq * K;
+  if (n <= 0) return cudaSuccess;
+  int64_t blocks = (n + 255) / 256;
+  if (blocks > 4096) blocks = 4096;
+  return launch_pdl(dcp_mask_topk_kernel, static_cast<unsigned>(blocks), 256, 0, stream, 1, topk,
+                    page_table, pt_stride, seq_lens, B, Sq, K, world, rank, topk_out);
+}
+
+cudaError_t launch_merge_partials(const float* o_parts, const float* lse_parts, int R,
+                                  int64_t n_rows, void* out_bf16, float* lse,
+                                  cudaStream_t stream) {
+  if (n_rows <= 0) return cudaSuccess;
+  const int64_t blocks = (n_rows + 7) / 8;
+  return launch_pdl(merge_partials_kernel, static_cast<unsigned>(blocks), 256, 0, stream, 1,
+                    o_parts, lse_parts, R, n_rows, static_cast<__nv_bfloat16*>(out_bf16), lse);
+}
+
+}  // namespace kv4

@@ -48,6 +48,7 @@ struct DecodeArgs {
   cudaEvent_t after_decode;    // recorded between the decode and merge kernels (may be null)
   int cluster_merge;           // splits > 1 merged inside a cluster of `splits` blocks
   int rope;                    // 1: 352-byte rows, q of 576 columns; 0: 288-byte rows, q of 512
+  int out_f32;                 // 1: out is fp32 (a context-parallel rank's partial), else bf16
 };
 
 struct GatherArgs {
@@ -94,6 +95,15 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), unsigned grid, unsigned block, 
 }
 
 cudaError_t launch_quantize_write(const QuantizeArgs& a, int num_sms, cudaStream_t stream);
+// Decode-context parallelism: the top-k list of one rank (keys on pages it
+// owns, page % world == rank), and the merge of the ranks' (o, lse).
+cudaError_t launch_dcp_mask_topk(const int32_t* topk, const int32_t* page_table,
+                                 int64_t pt_stride, const int32_t* seq_lens, int B, int Sq,
+                                 int K, int world, int rank, int32_t* topk_out,
+                                 cudaStream_t stream);
+cudaError_t launch_merge_partials(const float* o_parts, const float* lse_parts, int R,
+                                  int64_t n_rows, void* out_bf16, float* lse,
+                                  cudaStream_t stream);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 cudaError_t launch_debug_gather(const GatherArgs& a, cudaStream_t stream);
 size_t decode_smem_bytes(int HG, bool rope);

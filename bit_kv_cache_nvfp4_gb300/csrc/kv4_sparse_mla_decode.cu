@@ -219,6 +219,21 @@ __device__ __forceinline__ void load_scores(uint32_t taddr, uint32_t gap, float 
   }
 }
 
+// Four consecutive output elements: bf16 (rounded to nearest even) or, for
+// the fp32 partial output of a decode-context-parallel rank, fp32.
+__device__ __forceinline__ void store_out4(void* out, int64_t idx, float4 v, bool f32) {
+  if (f32) {
+    *reinterpret_cast<float4*>(static_cast<float*>(out) + idx) = v;
+  } else {
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y);
+    const __nv_bfloat162 hi = __floats2bfloat162_rn(v.z, v.w);
+    uint2 pk;
+    pk.x = *reinterpret_cast<const uint32_t*>(&lo);
+    pk.y = *reinterpret_cast<const uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(out) + idx) = pk;
+  }
+}
+
 // N consecutive floats of shared memory (16-byte aligned) into registers.
 template <int N>
 __device__ __forceinline__ void lds_vec(const float* src, float (&v)[N]) {
@@ -729,6 +744,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
         const float v = o[j] * inv[j];
         if (cmerge) o_x[h * kLatent + d] = v;
         else if (partial) a.ws_o[(part * HG + h) * kLatent + d] = v;
+        else if (a.out_f32) static_cast<float*>(a.out)[(out_head0 + h) * kLatent + d] = v;
         else static_cast<__nv_bfloat16*>(a.out)[(out_head0 + h) * kLatent + d] = __float2bfloat16_rn(v);
       }
     }
@@ -783,7 +799,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
       const float4* theirs = reinterpret_cast<const float4*>(q_s);
       const float* w_mine = xw + rank * HG;
       const float* w_theirs = xw + peer * HG;
-      __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
       for (int i = tid; i < kUnits / 2; i += kComputeThreads) {
         const int u = static_cast<int>(rank) * (kUnits / 2) + i;
         const int h = u / (kLatent / 4);
@@ -793,14 +808,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
         const float4 v0 = rank == 0 ? va : vb, v1 = rank == 0 ? vb : va;
         const float w0 = rank == 0 ? wa : wb, w1 = rank == 0 ? wb : wa;
         const float inv = xinv[h];
-        const __nv_bfloat162 lo = __floats2bfloat162_rn((w0 * v0.x + w1 * v1.x) * inv,
-                                                        (w0 * v0.y + w1 * v1.y) * inv);
-        const __nv_bfloat162 hi = __floats2bfloat162_rn((w0 * v0.z + w1 * v1.z) * inv,
-                                                        (w0 * v0.w + w1 * v1.w) * inv);
-        uint2 pk;
-        pk.x = *reinterpret_cast<const uint32_t*>(&lo);
-        pk.y = *reinterpret_cast<const uint32_t*>(&hi);
-        *reinterpret_cast<uint2*>(out + (out_head0 + h) * kLatent + (u % (kLatent / 4)) * 4) = pk;
+        const float4 m4 = make_float4((w0 * v0.x + w1 * v1.x) * inv, (w0 * v0.y + w1 * v1.y) * inv,
+                                      (w0 * v0.z + w1 * v1.z) * inv, (w0 * v0.w + w1 * v1.w) * inv);
+        store_out4(a.out, (out_head0 + h) * kLatent + (u % (kLatent / 4)) * 4, m4, a.out_f32 != 0);
       }
       cluster_sync();                          // the peer's copy out of this block is done
     }
@@ -850,17 +860,12 @@ __global__ void __launch_bounds__(256) merge_kernel(DecodeArgs a, int n_units) {
     }
   }
   const int64_t row = static_cast<int64_t>(bs) * a.H + g * HG + h;
-  __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + row * kLatent;
   const float inv = wsum > 0.0f ? 1.0f / wsum : 0.0f;
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const __nv_bfloat162 lo = __floats2bfloat162_rn(acc[j].x * inv, acc[j].y * inv);
-    const __nv_bfloat162 hi = __floats2bfloat162_rn(acc[j].z * inv, acc[j].w * inv);
-    uint2 pk;
-    pk.x = *reinterpret_cast<const uint32_t*>(&lo);
-    pk.y = *reinterpret_cast<const uint32_t*>(&hi);
-    *reinterpret_cast<uint2*>(out + j * 128 + lane * 4) = pk;
-  }
+  for (int j = 0; j < 4; ++j)
+    store_out4(a.out, row * kLatent + j * 128 + lane * 4,
+               make_float4(acc[j].x * inv, acc[j].y * inv, acc[j].z * inv, acc[j].w * inv),
+               a.out_f32 != 0);
   if (lane == 0) a.lse[row] = (wsum > 0.0f) ? m + logf(wsum) : -INFINITY;
 }
 

@@ -210,6 +210,47 @@ kv4_status kv4_debug_gather_dequant_latent(const uint8_t* pool_dev, int64_t num_
                                            kv4_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * Decode-context parallelism (DCP).
+ * Source: README "Parallelism and disaggregation" (ranks attend over their
+ * part of the context and merge (o, lse)).  Ownership rule (this project's
+ * reading): physical page p lives on rank p mod world.  One decode step on
+ * `world` ranks is:
+ *   1. kv4_dcp_mask_topk on every rank: topk_out [B,Sq,K] int32 keeps the
+ *      positions whose page the rank owns and is -1 elsewhere.  Positions
+ *      outside [0, L_eff) are -1 on every rank; a position whose page entry
+ *      cannot be read (page index >= pt_stride or a negative entry) is kept
+ *      on rank 0 only, whose decode then reports KV4_DEV_BAD_PAGE.
+ *   2. kv4_sparse_mla_decode_partial on every rank with its topk_out: the
+ *      same decode as kv4_sparse_mla_decode (same arguments, workspace and
+ *      errors), except that o_dev is fp32 [B,Sq,H,512] -- the normalized
+ *      weighted sum over the rank's keys, not rounded to bf16 -- and lse_dev
+ *      that partial's lse (-inf when the rank holds no key of the row).
+ *   3. An all-gather of (o, lse) across the ranks (by the caller, e.g. NCCL)
+ *      into o_parts [R, n_rows, 512] and lse_parts [R, n_rows], where
+ *      n_rows = B*Sq*H.
+ *   4. kv4_merge_partials: out bf16 [n_rows, 512] and lse [n_rows] by
+ *      log-sum-exp over the R partials (a partial with lse = -inf has weight
+ *      0; no finite lse gives out = 0, lse = -inf).  o_parts and out 16-byte
+ *      aligned.
+ * ------------------------------------------------------------------------- */
+kv4_status kv4_dcp_mask_topk(const int32_t* topk_idx_dev, const int32_t* page_table_dev,
+                             int64_t pt_stride, const int32_t* seq_lens_dev, int B, int Sq,
+                             int K, int world, int rank, int32_t* topk_out_dev,
+                             kv4_stream_t stream);
+kv4_status kv4_sparse_mla_decode_partial(const void* q_dev, const uint8_t* pool_dev,
+                                         int64_t num_slots, const int32_t* page_table_dev,
+                                         int64_t pt_stride, int page_size,
+                                         const int32_t* topk_idx_dev, int K,
+                                         const int32_t* seq_lens_dev, int B, int Sq, int H,
+                                         float sm_scale, float* o_dev, float* lse_dev,
+                                         void* workspace_dev, size_t workspace_bytes,
+                                         int force_splits, int32_t* dev_err,
+                                         kv4_stream_t stream);
+kv4_status kv4_merge_partials(const float* o_parts_dev, const float* lse_parts_dev, int R,
+                              int64_t n_rows, void* out_dev, float* lse_dev,
+                              kv4_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * kv4_sparse_mla_decode_noalloc -- the same decode for callers that cannot
  * allocate device memory when they call it (for example a plugin whose host
  * engine hands it only its input and output buffers and owns every byte of

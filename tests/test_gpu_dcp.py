@@ -1,0 +1,76 @@
+"""Decode-context parallelism kernels on one GPU, against the CPU oracle.
+
+The ranks are emulated one after another on the same GPU (nothing waits on
+another rank): for R ranks, kv4_dcp_mask_topk gives every rank its keys,
+kv4_sparse_mla_decode_partial its fp32 (o, lse), and kv4_merge_partials
+combines the stacked partials -- which must agree with the oracle's decode
+over all keys within the decode tolerances.  The mask is checked bit for bit
+against the ownership rule written out in numpy."""
+import numpy as np
+import pytest
+import torch
+
+from gpu_common import assert_close, device_inputs, gpu_pool, need_gpu, oracle_decode, workload
+from test_dcp_cpu import owned_topk
+
+pytestmark = pytest.mark.gpu
+
+
+def kv():
+    import bit_kv_cache_nvfp4_gb300 as m
+    return m
+
+
+@pytest.mark.parametrize("world", [2, 3, 8])
+def test_mask_matches_ownership_rule(world):
+    need_gpu()
+    w = workload("decode")
+    _, pt, topk, lens = device_inputs(w)
+    topk_np = w.topk.numpy().copy()
+    topk_np[0, 0, :7] = -1                              # padding
+    topk_np[1, 0, 3] = int(w.seq_lens[1]) + 5           # past the sequence
+    t = torch.from_numpy(topk_np).cuda()
+    seen = np.zeros(topk_np.shape, dtype=np.int64)
+    for r in range(world):
+        got = kv().dcp_mask_topk(t, pt, lens, world, r).cpu().numpy()
+        ref = owned_topk(topk_np, w.page_table.numpy(), w.seq_lens.numpy(), world, r)
+        assert np.array_equal(got, ref), r
+        seen += got >= 0
+    valid = (topk_np >= 0) & (topk_np < w.seq_lens.numpy()[:, None, None])
+    assert np.array_equal(seen, valid.astype(np.int64))    # a partition of the valid keys
+
+
+@pytest.mark.parametrize("name,world", [("decode", 1), ("decode", 2), ("decode", 4),
+                                        ("decode", 8), ("long", 8)])
+def test_emulated_ranks_match_oracle(name, world):
+    need_gpu()
+    w = workload(name)
+    pool = gpu_pool(w)
+    q, pt, topk, lens = device_inputs(w)
+    m = kv()
+    parts_o, parts_l = [], []
+    for r in range(world):
+        mine = m.dcp_mask_topk(topk, pt, lens, world, r)
+        o, l = m.sparse_mla_decode_partial(q, pool, pt, mine, lens, w.sm_scale)
+        assert o.dtype == torch.float32
+        parts_o.append(o)
+        parts_l.append(l)
+    out, lse = m.merge_partials(torch.stack(parts_o), torch.stack(parts_l))
+    torch.cuda.synchronize()
+    req = [0, 7, 15] if name == "decode" else [0, 41]
+    out_ref, lse_ref = oracle_decode(w, req)
+    mo, ml = assert_close(out[req], lse[req], out_ref, lse_ref, f"{name} world={world}")
+    print(f"{name} DCP world={world}: max|out err| {mo:.3g}  max|lse err| {ml:.3g}")
+
+
+def test_merge_of_empty_partials():
+    need_gpu()
+    o = torch.randn(3, 5, 512, device="cuda")
+    l = torch.full((3, 5), float("-inf"), device="cuda")
+    l[1, 2] = 0.5                                           # one finite partial in row 2
+    out, lse = kv().merge_partials(o, l)
+    torch.cuda.synchronize()
+    assert torch.all(torch.isneginf(lse[[0, 1, 3, 4]]))
+    assert torch.all(out[[0, 1, 3, 4]] == 0)
+    assert abs(float(lse[2]) - 0.5) < 1e-6
+    assert torch.equal(out[2], o[1, 2].to(torch.bfloat16))
