@@ -9,8 +9,9 @@
 // to even, saturating, sign kept).  A zero scale gives zero codes.  Lanes
 // 0..7 also convert 8 rope values each to E4M3.  The row is written with
 // coalesced stores: codes as 32 x 8 bytes, scales as 8 x 4 bytes, rope as
-// 8 x 8 bytes.  The kernel is HBM-bound (1152 bytes read, 352 written per
-// token).  Rows of 288 bytes (the latent-only layout of the same README
+// 8 x 8 bytes.  Each warp loads its next token while it codes the current
+// one.  Bytes: 1152 read, 352 written per token; at 1M tokens the IEEE
+// divisions (17 per lane and token) rather than HBM bound the kernel.  Rows of 288 bytes (the latent-only layout of the same README
 // section, for models whose keys carry no rope part) are the first 288
 // bytes of the same row: no rope is read or written.
 //
@@ -96,16 +97,34 @@ __global__ void __launch_bounds__(256) quantize_write_kernel(QuantizeArgs a) {
   const __nv_bfloat16* latent = static_cast<const __nv_bfloat16*>(a.latent);
   const __nv_bfloat16* rope = static_cast<const __nv_bfloat16*>(a.rope);
 
+  // The loads of a warp's next token are issued before the current token is
+  // processed (slot, latent and rope of a token are independent loads), so
+  // every warp keeps one token's reads in flight while it computes.
+  struct TokenLoads {
+    int64_t slot;
+    uint4 v0, v1, rv;
+  };
+  auto load = [&](int64_t tt, TokenLoads& l) {
+    l.slot = __ldg(a.slots + tt);
+    const __nv_bfloat16* src = latent + tt * a.latent_stride + lane * 16;
+    l.v0 = ld_stream(src);
+    l.v1 = ld_stream(src + 8);
+    l.rv = (rope != nullptr && lane < 8) ? ld_stream(rope + tt * a.rope_stride + lane * 8)
+                                         : make_uint4(0, 0, 0, 0);
+  };
+  TokenLoads next{};
+  if (warp0 < a.n_tokens) load(warp0, next);
   for (int64_t t = warp0; t < a.n_tokens; t += nwarps) {
-    const int64_t slot = __ldg(a.slots + t);
+    const TokenLoads cur = next;
+    if (t + nwarps < a.n_tokens) load(t + nwarps, next);
+    const int64_t slot = cur.slot;
     if (slot < 0) continue;                               // warp-uniform
     if (slot >= a.num_slots) {
       if (lane == 0) flag_error(a.dev_err, kDevBadSlot);
       continue;
     }
-    const __nv_bfloat16* src = latent + t * a.latent_stride + lane * 16;
-    const uint4 v0 = ld_stream(src);
-    const uint4 v1 = ld_stream(src + 8);
+    const uint4 v0 = cur.v0;
+    const uint4 v1 = cur.v1;
     const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
     float x[16];
 #pragma unroll
@@ -164,7 +183,7 @@ __global__ void __launch_bounds__(256) quantize_write_kernel(QuantizeArgs a) {
       *reinterpret_cast<uint32_t*>(row + 256 + lane * 4) = b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
     }
     if (lane < 8 && rope != nullptr) {
-      const uint4 rv = ld_stream(rope + t * a.rope_stride + lane * 8);
+      const uint4 rv = cur.rv;
       const uint32_t lo = f32x2_to_e4m3x2(bf16_high(rv.x), bf16_low(rv.x)) |
                           (f32x2_to_e4m3x2(bf16_high(rv.y), bf16_low(rv.y)) << 16);
       const uint32_t hi = f32x2_to_e4m3x2(bf16_high(rv.z), bf16_low(rv.z)) |
@@ -180,7 +199,16 @@ cudaError_t launch_quantize_write(const QuantizeArgs& a, int num_sms, cudaStream
   if (a.n_tokens <= 0) return cudaSuccess;
   const int64_t warps_needed = a.n_tokens;
   int64_t blocks = (warps_needed + 7) / 8;
-  const int64_t cap = static_cast<int64_t>(num_sms > 0 ? num_sms : 1) * 16;
+  // at most one wave of resident blocks; each warp then walks its tokens
+  static int per_sm = 0;
+  if (per_sm == 0) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, quantize_write_kernel, 256, 0) !=
+            cudaSuccess ||
+        per_sm < 1)
+      per_sm = 1;
+    (void)cudaGetLastError();
+  }
+  const int64_t cap = static_cast<int64_t>(num_sms > 0 ? num_sms : 1) * per_sm;
   if (blocks > cap) blocks = cap;
   // Same shared-memory carve-out as the decode kernel, which usually follows
   // in the stream: the SMs then need no reconfiguration between the two.
