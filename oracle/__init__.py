@@ -75,6 +75,12 @@ def _load():
         lib.kv4ref_dequant_row.restype = None
         lib.kv4ref_quantize_write.argtypes = [P, i64, P, i64, P, i64, P, i64]
         lib.kv4ref_quantize_write.restype = i32
+        lib.kv4ref_quantize_write_fp8.argtypes = [P, i64, P, i64, P, i64, P, i64]
+        lib.kv4ref_quantize_write_fp8.restype = i32
+        lib.kv4ref_dequant_row_fp8.argtypes = [P, P]
+        lib.kv4ref_dequant_row_fp8.restype = None
+        lib.kv4ref_fp8_scratch.argtypes = [P, i64, P, i64, i32, P, i32, P, i32, i32, P]
+        lib.kv4ref_fp8_scratch.restype = i32
         lib.kv4ref_quantize_row_mse.argtypes = [P, P, P]
         lib.kv4ref_quantize_row_mse.restype = None
         lib.kv4ref_quantize_write_mse.argtypes = [P, i64, P, i64, P, i64, P, i64]
@@ -86,6 +92,8 @@ def _load():
         lib.kv4ref_sparse_mla_decode.argtypes = [P, P, i64, P, i64, i32, P, i32, P,
                                                  i32, i32, i32, f32, i32, P, P]
         lib.kv4ref_sparse_mla_decode.restype = i32
+        lib.kv4ref_sparse_mla_decode_fp8.argtypes = lib.kv4ref_sparse_mla_decode.argtypes
+        lib.kv4ref_sparse_mla_decode_fp8.restype = i32
         lib.kv4ref_merge.argtypes = [P, P, i32, i32, i32, P, P]
         lib.kv4ref_merge.restype = None
         _lib = lib
@@ -216,8 +224,9 @@ def gather_dequant(pool, page_table, topk_idx, seq_lens, page_size=64):
 
 
 def sparse_mla_decode(q_bits, pool, page_table, topk_idx, seq_lens, sm_scale,
-                      splits=1, page_size=64):
-    """q_bits uint16[B,Sq,H,576] -> (status, out fp32[B,Sq,H,512], lse fp32[B,Sq,H])."""
+                      splits=1, page_size=64, fp8_rows=False):
+    """q_bits uint16[B,Sq,H,576] -> (status, out fp32[B,Sq,H,512], lse fp32[B,Sq,H]).
+    pool rows: 352-byte NVFP4, or 576-byte FP8 with fp8_rows=True."""
     q = _as(q_bits, np.uint16)
     pool = _as(pool, np.uint8)
     pt = _as(page_table, np.int32)
@@ -228,11 +237,45 @@ def sparse_mla_decode(q_bits, pool, page_table, topk_idx, seq_lens, sm_scale,
     K = topk.shape[2]
     out = np.empty((B, Sq, H, 512), dtype=np.float32)
     lse = np.empty((B, Sq, H), dtype=np.float32)
-    st = _load().kv4ref_sparse_mla_decode(_ptr(q), _ptr(pool), pool.shape[0], _ptr(pt),
-                                          pt.shape[1], page_size, _ptr(topk), K, _ptr(sl),
-                                          B, Sq, H, float(sm_scale), int(splits),
-                                          _ptr(out), _ptr(lse))
+    fn = _load().kv4ref_sparse_mla_decode_fp8 if fp8_rows else _load().kv4ref_sparse_mla_decode
+    st = fn(_ptr(q), _ptr(pool), pool.shape[0], _ptr(pt), pt.shape[1], page_size, _ptr(topk), K,
+            _ptr(sl), B, Sq, H, float(sm_scale), int(splits), _ptr(out), _ptr(lse))
     return st, out, lse
+
+
+def quantize_write_fp8(latent_bits, rope_bits, slot_mapping, pool) -> int:
+    """576-byte FP8 rows (E4M3 of every latent and rope value) into pool
+    uint8[num_slots,576]."""
+    lat = _as(latent_bits, np.uint16)
+    rope = _as(rope_bits, np.uint16)
+    slots = _as(slot_mapping, np.int64)
+    assert pool.dtype == np.uint8 and pool.flags["C_CONTIGUOUS"] and pool.shape[1] == 576
+    return int(_load().kv4ref_quantize_write_fp8(
+        _ptr(lat), lat.shape[1] if lat.ndim == 2 else 512,
+        _ptr(rope), rope.shape[1] if rope.ndim == 2 else 64,
+        _ptr(slots), slots.shape[0], _ptr(pool), pool.shape[0]))
+
+
+def dequant_row_fp8(row: np.ndarray) -> np.ndarray:
+    row = _as(row, np.uint8)
+    assert row.size == 576
+    out = np.zeros(576, dtype=np.float32)
+    _load().kv4ref_dequant_row_fp8(_ptr(row), _ptr(out))
+    return out
+
+
+def fp8_scratch(pool, page_table, topk_idx, seq_lens, page_size=64):
+    """(status, scratch uint8[B*Sq*K, 576]): the FP8 copy of the rows the keys
+    select (zero rows for masked keys)."""
+    pool = _as(pool, np.uint8)
+    pt = _as(page_table, np.int32)
+    topk = _as(topk_idx, np.int32)
+    sl = _as(seq_lens, np.int32)
+    B, Sq, K = topk.shape
+    scratch = np.empty((B * Sq * K, 576), dtype=np.uint8)
+    st = _load().kv4ref_fp8_scratch(_ptr(pool), pool.shape[0], _ptr(pt), pt.shape[1], page_size,
+                                    _ptr(topk), K, _ptr(sl), B, Sq, _ptr(scratch))
+    return st, scratch
 
 
 def merge(o_parts, lse_parts):

@@ -118,6 +118,34 @@ int kv4ref_sparse_mla_decode(const uint16_t* q_bf16, const uint8_t* pool,
                              float sm_scale, int splits, float* out,
                              float* lse);
 
+/* ---- FP8 rows (the comparison paths) --------------------------------------
+ * README "4-bit KV cache": the 352-byte row "replaces the 576-byte FP8 row",
+ * and kv4mla is compared with a path that builds "an FP8 scratch copy".  The
+ * FP8 row is read here as 576 E4M3 bytes -- latent 0..511 then rope 0..63,
+ * each E4M3_RNE_satfinite(x) with no scale (the page gives no scale).
+ *   kv4ref_quantize_write_fp8   bf16 latent/rope -> pool [num_slots, 576]
+ *   kv4ref_dequant_row_fp8      576 bytes -> 576 floats
+ *   kv4ref_fp8_scratch          for every (b, s, k): the NVFP4 row the key
+ *                               selects, dequantized and cast to E4M3 (the
+ *                               FP8 scratch copy), into scratch
+ *                               [B*Sq*K, 576]; masked keys give zero rows
+ *   kv4ref_sparse_mla_decode_fp8  kv4ref_sparse_mla_decode over a pool of
+ *                               576-byte FP8 rows */
+int kv4ref_quantize_write_fp8(const uint16_t* latent_bf16, int64_t latent_stride,
+                              const uint16_t* rope_bf16, int64_t rope_stride,
+                              const int64_t* slot_mapping, int64_t n_tokens,
+                              uint8_t* pool, int64_t num_slots);
+void kv4ref_dequant_row_fp8(const uint8_t* row, float* out576);
+int kv4ref_fp8_scratch(const uint8_t* pool, int64_t num_slots, const int32_t* page_table,
+                       int64_t pt_stride, int page_size, const int32_t* topk_idx, int K,
+                       const int32_t* seq_lens, int B, int Sq, uint8_t* scratch);
+int kv4ref_sparse_mla_decode_fp8(const uint16_t* q_bf16, const uint8_t* pool,
+                                 int64_t num_slots, const int32_t* page_table,
+                                 int64_t pt_stride, int page_size,
+                                 const int32_t* topk_idx, int K,
+                                 const int32_t* seq_lens, int B, int Sq, int H,
+                                 float sm_scale, int splits, float* out, float* lse);
+
 /* ---- log-sum-exp merge of S partials -------------------------------------
  * o_parts [S, n, D] (each normalized), lse_parts [S, n] -> out [n, D],
  * lse [n].  Partials with lse = -inf carry weight 0. */

@@ -66,6 +66,65 @@ float attend_one_head(const float* q576, const std::vector<const float*>& rows,
 
 }  // namespace
 
+namespace {
+
+/* The decode over rows of either layout: row_bytes 352 (NVFP4) or 576
+ * (FP8), dequantized by the matching row decoder. */
+int decode_rows(const uint16_t* q_bf16, const uint8_t* pool, int64_t num_slots,
+                const int32_t* page_table, int64_t pt_stride, int page_size,
+                const int32_t* topk_idx, int K, const int32_t* seq_lens, int B, int Sq,
+                int H, float sm_scale, int splits, float* out, float* lse, int row_bytes,
+                void (*dequant)(const uint8_t*, float*)) {
+  if (!q_bf16 || !pool || !page_table || !topk_idx || !seq_lens || !out ||
+      !lse || B < 0 || Sq < 1 || H < 1 || K < 0 || splits < 1)
+    return KV4REF_ERR_ARG;
+  const int64_t n_keys = static_cast<int64_t>(B) * Sq * K;
+  std::vector<int64_t> slots(static_cast<size_t>(n_keys));
+  const int status =
+      kv4ref_resolve_slots(page_table, pt_stride, page_size, topk_idx, K,
+                           seq_lens, B, Sq, num_slots, slots.data());
+  if (status == KV4REF_ERR_ARG) return status;
+
+  const int chunk = (K + splits - 1) / (splits > 0 ? splits : 1);
+  std::vector<float> kv(static_cast<size_t>(K) * kQkDim);
+  std::vector<float> q(kQkDim);
+  std::vector<float> o_parts(static_cast<size_t>(splits) * kVDim);
+  std::vector<float> lse_parts(static_cast<size_t>(splits));
+  for (int b = 0; b < B; ++b) {
+    for (int s = 0; s < Sq; ++s) {
+      const int64_t base = (static_cast<int64_t>(b) * Sq + s) * K;
+      for (int k = 0; k < K; ++k)
+        if (slots[base + k] >= 0)
+          dequant(pool + slots[base + k] * row_bytes,
+                  kv.data() + static_cast<size_t>(k) * kQkDim);
+      for (int h = 0; h < H; ++h) {
+        const int64_t qh = (static_cast<int64_t>(b) * Sq + s) * H + h;
+        for (int d = 0; d < kQkDim; ++d) q[d] = bf16_to_float(q_bf16[qh * kQkDim + d]);
+        for (int part = 0; part < splits; ++part) {
+          std::vector<const float*> rows;
+          const int k0 = part * chunk;
+          const int k1 = (k0 + chunk < K) ? k0 + chunk : K;
+          for (int k = k0; k < k1; ++k)
+            if (slots[base + k] >= 0)
+              rows.push_back(kv.data() + static_cast<size_t>(k) * kQkDim);
+          lse_parts[part] = attend_one_head(q.data(), rows, sm_scale,
+                                            o_parts.data() + part * kVDim);
+        }
+        if (splits == 1) {
+          std::memcpy(out + qh * kVDim, o_parts.data(), kVDim * sizeof(float));
+          lse[qh] = lse_parts[0];
+        } else {
+          kv4ref_merge(o_parts.data(), lse_parts.data(), splits, 1, kVDim,
+                       out + qh * kVDim, lse + qh);
+        }
+      }
+    }
+  }
+  return status;
+}
+
+}  // namespace
+
 extern "C" {
 
 int kv4ref_resolve_slots(const int32_t* page_table, int64_t pt_stride,
@@ -157,50 +216,41 @@ int kv4ref_sparse_mla_decode(const uint16_t* q_bf16, const uint8_t* pool,
                              const int32_t* seq_lens, int B, int Sq, int H,
                              float sm_scale, int splits, float* out,
                              float* lse) {
-  if (!q_bf16 || !pool || !page_table || !topk_idx || !seq_lens || !out ||
-      !lse || B < 0 || Sq < 1 || H < 1 || K < 0 || splits < 1)
-    return KV4REF_ERR_ARG;
-  const int64_t n_keys = static_cast<int64_t>(B) * Sq * K;
-  std::vector<int64_t> slots(static_cast<size_t>(n_keys));
-  const int status =
-      kv4ref_resolve_slots(page_table, pt_stride, page_size, topk_idx, K,
-                           seq_lens, B, Sq, num_slots, slots.data());
-  if (status == KV4REF_ERR_ARG) return status;
+  return decode_rows(q_bf16, pool, num_slots, page_table, pt_stride, page_size, topk_idx, K,
+                     seq_lens, B, Sq, H, sm_scale, splits, out, lse, kRowBytes,
+                     kv4ref_dequant_row);
+}
 
-  const int chunk = (K + splits - 1) / (splits > 0 ? splits : 1);
-  std::vector<float> kv(static_cast<size_t>(K) * kQkDim);
-  std::vector<float> q(kQkDim);
-  std::vector<float> o_parts(static_cast<size_t>(splits) * kVDim);
-  std::vector<float> lse_parts(static_cast<size_t>(splits));
-  for (int b = 0; b < B; ++b) {
-    for (int s = 0; s < Sq; ++s) {
-      const int64_t base = (static_cast<int64_t>(b) * Sq + s) * K;
-      for (int k = 0; k < K; ++k)
-        if (slots[base + k] >= 0)
-          kv4ref_dequant_row(pool + slots[base + k] * kRowBytes,
-                             kv.data() + static_cast<size_t>(k) * kQkDim);
-      for (int h = 0; h < H; ++h) {
-        const int64_t qh = (static_cast<int64_t>(b) * Sq + s) * H + h;
-        for (int d = 0; d < kQkDim; ++d) q[d] = bf16_to_float(q_bf16[qh * kQkDim + d]);
-        for (int part = 0; part < splits; ++part) {
-          std::vector<const float*> rows;
-          const int k0 = part * chunk;
-          const int k1 = (k0 + chunk < K) ? k0 + chunk : K;
-          for (int k = k0; k < k1; ++k)
-            if (slots[base + k] >= 0)
-              rows.push_back(kv.data() + static_cast<size_t>(k) * kQkDim);
-          lse_parts[part] = attend_one_head(q.data(), rows, sm_scale,
-                                            o_parts.data() + part * kVDim);
-        }
-        if (splits == 1) {
-          std::memcpy(out + qh * kVDim, o_parts.data(), kVDim * sizeof(float));
-          lse[qh] = lse_parts[0];
-        } else {
-          kv4ref_merge(o_parts.data(), lse_parts.data(), splits, 1, kVDim,
-                       out + qh * kVDim, lse + qh);
-        }
-      }
+int kv4ref_sparse_mla_decode_fp8(const uint16_t* q_bf16, const uint8_t* pool,
+                                 int64_t num_slots, const int32_t* page_table,
+                                 int64_t pt_stride, int page_size,
+                                 const int32_t* topk_idx, int K,
+                                 const int32_t* seq_lens, int B, int Sq, int H,
+                                 float sm_scale, int splits, float* out, float* lse) {
+  return decode_rows(q_bf16, pool, num_slots, page_table, pt_stride, page_size, topk_idx, K,
+                     seq_lens, B, Sq, H, sm_scale, splits, out, lse, 576,
+                     kv4ref_dequant_row_fp8);
+}
+
+int kv4ref_fp8_scratch(const uint8_t* pool, int64_t num_slots, const int32_t* page_table,
+                       int64_t pt_stride, int page_size, const int32_t* topk_idx, int K,
+                       const int32_t* seq_lens, int B, int Sq, uint8_t* scratch) {
+  if (!pool || !page_table || !topk_idx || !seq_lens || !scratch || B < 0 || Sq < 1 || K < 0)
+    return KV4REF_ERR_ARG;
+  const int64_t n = static_cast<int64_t>(B) * Sq * K;
+  std::vector<int64_t> slots(static_cast<size_t>(n));
+  const int status = kv4ref_resolve_slots(page_table, pt_stride, page_size, topk_idx, K,
+                                          seq_lens, B, Sq, num_slots, slots.data());
+  if (status == KV4REF_ERR_ARG) return status;
+  float row[kQkDim];
+  for (int64_t i = 0; i < n; ++i) {
+    uint8_t* dst = scratch + i * 576;
+    if (slots[i] < 0) {
+      std::memset(dst, 0, 576);
+      continue;
     }
+    kv4ref_dequant_row(pool + slots[i] * kRowBytes, row);
+    for (int d = 0; d < kQkDim; ++d) dst[d] = kv4ref_enc_e4m3(row[d]);
   }
   return status;
 }

@@ -205,6 +205,32 @@ int kv4ref_quantize_write_mse(const uint16_t* latent_bf16, int64_t latent_stride
   return status;
 }
 
+int kv4ref_quantize_write_fp8(const uint16_t* latent_bf16, int64_t latent_stride,
+                              const uint16_t* rope_bf16, int64_t rope_stride,
+                              const int64_t* slot_mapping, int64_t n_tokens,
+                              uint8_t* pool, int64_t num_slots) {
+  if (n_tokens < 0 || num_slots < 0) return KV4REF_ERR_ARG;
+  if (n_tokens > 0 && (!latent_bf16 || !rope_bf16 || !slot_mapping || !pool))
+    return KV4REF_ERR_ARG;
+  if (latent_stride < 512 || rope_stride < 64) return KV4REF_ERR_ARG;
+  int status = KV4REF_OK;
+  for (int64_t t = 0; t < n_tokens; ++t) {
+    const int64_t slot = slot_mapping[t];
+    if (slot < 0) continue;
+    if (slot >= num_slots) { status = KV4REF_ERR_SLOT; continue; }
+    uint8_t* row = pool + slot * 576;
+    for (int d = 0; d < 512; ++d)
+      row[d] = kv4ref_enc_e4m3(bf16_to_float(latent_bf16[t * latent_stride + d]));
+    for (int r = 0; r < 64; ++r)
+      row[512 + r] = kv4ref_enc_e4m3(bf16_to_float(rope_bf16[t * rope_stride + r]));
+  }
+  return status;
+}
+
+void kv4ref_dequant_row_fp8(const uint8_t* row, float* out576) {
+  for (int d = 0; d < 576; ++d) out576[d] = kv4ref_dec_e4m3(row[d]);
+}
+
 int kv4ref_quantize_write(const uint16_t* latent_bf16, int64_t latent_stride,
                           const uint16_t* rope_bf16, int64_t rope_stride,
                           const int64_t* slot_mapping, int64_t n_tokens,
