@@ -406,11 +406,17 @@ def run_gpu(args):
     # end to end through the public API, host buffers in and out
     e2e = run_e2e(kv, w, dev, pool, pt, lens, flush, args)
     cache_write = run_cache_write(kv, dev, flush, args)
-    latent = None
-    if not args.skip_latent:
+    latent = fp8 = None
+    if not args.skip_variants:
+        scratch = run_scratch_path(kv, w, dev, pool, q, pt, topk, lens, flush, args)
         del pool
         torch.cuda.empty_cache()
         latent = run_latent_rows(kv, w, dev, q, pt, topk, lens, flush, err, args, valid)
+        fp8 = run_fp8_rows(kv, w, dev, q, pt, topk, lens, flush, args)
+        fp8.update(scratch)
+        fp8["nvfp4_decode_us"] = dec_ms_avg * 1e3
+        fp8["nvfp4_vs_scratch_path"] = fp8["scratch_path_us"] / (dec_ms_avg * 1e3)
+        fp8["nvfp4_vs_fp8_rows"] = fp8["fp8_rows_decode_us"] / (dec_ms_avg * 1e3)
 
     peak_gbs, peak_tflops, peak_kind = measured_peaks()
     achieved_gbs = alg_bytes / (dec_ms_avg * 1e-3) / 1e9
@@ -467,6 +473,7 @@ def run_gpu(args):
             "cpu_baseline": cpu,
             "e2e": e2e,
             "latent_rows_288B": latent,
+            "fp8_comparison": fp8,
             "cache_write_1M_tokens": cache_write,
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clocks.summary(),
@@ -476,6 +483,65 @@ def run_gpu(args):
     if world > 1:
         torch.distributed.destroy_process_group()
     return 0
+
+
+def _time_loop(fn, flush, stream, steps, warmup):
+    """Average device time of fn() over `steps` calls, L2 flushed before each."""
+    for _ in range(warmup):
+        flush.zero_()
+        fn()
+    e0 = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    e1 = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for i in range(steps):
+        flush.zero_()
+        e0[i].record(stream)
+        fn()
+        e1[i].record(stream)
+    torch.cuda.synchronize()
+    return sum(a.elapsed_time(b) for a, b in zip(e0, e1)) / steps
+
+
+def run_scratch_path(kv, w, dev, pool, q, pt, topk, lens, flush, args):
+    """The comparison path of the README's kv4mla bullet: copy the selected
+    NVFP4 rows into an FP8 scratch buffer in HBM (dequantize, cast to E4M3),
+    then run the decode over the scratch rows."""
+    scratch = kv.fp8_scratch(pool, pt, topk, lens)
+    s_pt, s_topk, s_lens = kv.scratch_index(topk, lens)
+    qs = q.reshape(w.B * w.Sq, 1, w.H, 576).contiguous()
+    out = torch.empty((w.B * w.Sq, 1, w.H, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((w.B * w.Sq, 1, w.H), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def convert():
+        kv.fp8_scratch(pool, pt, topk, lens, scratch=scratch)
+
+    def path():
+        convert()
+        kv.sparse_mla_decode_fp8(qs, scratch, s_pt, s_topk, s_lens, w.sm_scale, out=out, lse=lse)
+
+    t_conv = _time_loop(convert, flush, stream, args.steps, args.warmup)
+    t_path = _time_loop(path, flush, stream, args.steps, args.warmup)
+    return {"scratch_bytes": scratch.numel(), "scratch_convert_us": t_conv * 1e3,
+            "scratch_path_us": t_path * 1e3}
+
+
+def run_fp8_rows(kv, w, dev, q, pt, topk, lens, flush, args):
+    """The decode over a pool of 576-byte FP8 rows (the row the NVFP4 row
+    replaces), same workload and indices."""
+    pool = torch.zeros((w.num_slots, 576), dtype=torch.uint8, device=dev)
+    for lat, rope, slots in wl.iter_pool_chunks(w, chunk=1 << 18, device=dev):
+        kv.quantize_write_fp8(lat, rope, slots, pool)
+    out = torch.empty((w.B, w.Sq, w.H, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((w.B, w.Sq, w.H), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    t = _time_loop(lambda: kv.sparse_mla_decode_fp8(q, pool, pt, topk, lens, w.sm_scale,
+                                                    out=out, lse=lse),
+                   flush, stream, args.steps, args.warmup)
+    del pool
+    torch.cuda.empty_cache()
+    return {"fp8_pool_bytes": w.num_slots * 576, "fp8_rows_decode_us": t * 1e3,
+            "note": "decode-only device times (cluster merge or merge kernel included); "
+                    "scratch_path = scratch copy + FP8 decode over it"}
 
 
 def run_cache_write(kv, dev, flush, args):
@@ -620,8 +686,8 @@ def main(argv=None):
     p.add_argument("--skip-cpu", action="store_true")
     p.add_argument("--sessions", type=int, default=64,
                    help="sessions of the long-context workload per rank (smaller: profiling)")
-    p.add_argument("--skip-latent", action="store_true",
-                   help="skip the 288-byte latent-only row measurement")
+    p.add_argument("--skip-variants", action="store_true",
+                   help="skip the 288-byte row and FP8 comparison measurements")
     p.add_argument("--splits", type=int, default=0,
                    help="force the split-K count (0: the library's plan)")
     args = p.parse_args(argv)

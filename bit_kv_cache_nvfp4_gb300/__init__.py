@@ -23,7 +23,8 @@ import torch
 __all__ = [
     "Kv4Error", "library_path", "load_library", "quantize_write", "decode_plan",
     "sparse_mla_decode", "debug_gather_dequant", "set_wait_limit", "set_timing_event",
-    "quantize_write_mse", "quantize_write_latent", "decode_plan_latent", "sparse_mla_decode_latent",
+    "quantize_write_mse", "quantize_write_fp8", "decode_plan_fp8", "sparse_mla_decode_fp8",
+    "fp8_scratch", "scratch_index", "ROW_BYTES_FP8", "quantize_write_latent", "decode_plan_latent", "sparse_mla_decode_latent",
     "debug_gather_dequant_latent", "sparse_mla_decode_partial", "dcp_mask_topk",
     "merge_partials", "gather_partials", "dcp_sparse_mla_decode", "ROW_BYTES", "ROW_BYTES_LATENT", "LATENT", "ROPE", "QK_DIM", "PAGE", "DEV_BAD_SLOT", "DEV_BAD_PAGE",
     "DEV_TIMEOUT",
@@ -31,6 +32,7 @@ __all__ = [
 
 ROW_BYTES, LATENT, ROPE, QK_DIM, PAGE, TILE_KEYS = 352, 512, 64, 576, 64, 128
 ROW_BYTES_LATENT = 288
+ROW_BYTES_FP8 = 576
 DEV_BAD_SLOT, DEV_BAD_PAGE, DEV_TIMEOUT = 1, 2, 4
 _STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported shape or page size",
            3: "device is not compute capability 10.3", 4: "kernel launch failed",
@@ -75,6 +77,14 @@ def load_library():
         lib.kv4_debug_gather_dequant.argtypes = [P, i64, P, i64, i32, P, i32, P, i32, i32, P, P,
                                                  P]
         lib.kv4_debug_gather_dequant.restype = i32
+        lib.kv4_quantize_write_fp8.argtypes = lib.kv4_quantize_write.argtypes
+        lib.kv4_quantize_write_fp8.restype = i32
+        lib.kv4_decode_plan_fp8.argtypes = lib.kv4_decode_plan.argtypes
+        lib.kv4_decode_plan_fp8.restype = i32
+        lib.kv4_sparse_mla_decode_fp8.argtypes = lib.kv4_sparse_mla_decode.argtypes
+        lib.kv4_sparse_mla_decode_fp8.restype = i32
+        lib.kv4_fp8_scratch.argtypes = lib.kv4_debug_gather_dequant.argtypes
+        lib.kv4_fp8_scratch.restype = i32
         lib.kv4_quantize_write_mse.argtypes = lib.kv4_quantize_write.argtypes
         lib.kv4_quantize_write_mse.restype = i32
         lib.kv4_sparse_mla_decode_partial.argtypes = lib.kv4_sparse_mla_decode.argtypes
@@ -142,6 +152,15 @@ def quantize_write_mse(latent: torch.Tensor, rope: torch.Tensor, slot_mapping: t
     _quantize("kv4_quantize_write_mse", latent, rope, slot_mapping, pool, dev_err)
 
 
+def quantize_write_fp8(latent: torch.Tensor, rope: torch.Tensor, slot_mapping: torch.Tensor,
+                       pool: torch.Tensor, dev_err: torch.Tensor | None = None) -> None:
+    """576-byte FP8 rows (E4M3 of every latent and rope value) into pool
+    uint8 [num_slots,576] -- the row the NVFP4 row replaces, for comparison."""
+    if pool.dim() != 2 or pool.shape[1] != ROW_BYTES_FP8:
+        raise ValueError("pool must be [num_slots, 576]")
+    _quantize("kv4_quantize_write_fp8", latent, rope, slot_mapping, pool, dev_err)
+
+
 def _quantize(fn, latent, rope, slot_mapping, pool, dev_err):
     lib = load_library()
     n = slot_mapping.shape[0]
@@ -189,6 +208,11 @@ def decode_plan(B: int, Sq: int, H: int, K: int, force_splits: int = 0):
     return _plan("kv4_decode_plan", B, Sq, H, K, force_splits)
 
 
+def decode_plan_fp8(B: int, Sq: int, H: int, K: int, force_splits: int = 0):
+    """(splits, workspace_bytes) of sparse_mla_decode_fp8 on the current device."""
+    return _plan("kv4_decode_plan_fp8", B, Sq, H, K, force_splits)
+
+
 def decode_plan_latent(B: int, Sq: int, H: int, K: int, force_splits: int = 0):
     """(splits, workspace_bytes) of sparse_mla_decode_latent on the current device."""
     return _plan("kv4_decode_plan_latent", B, Sq, H, K, force_splits)
@@ -216,7 +240,7 @@ def sparse_mla_decode(q: torch.Tensor, pool: torch.Tensor, page_table: torch.Ten
     [B,pt_stride]; topk_idx int32 [B,Sq,K] (logical positions, -1 = pad);
     seq_lens int32 [B].  Returns (out bf16 [B,Sq,H,512], lse fp32 [B,Sq,H]).
     """
-    return _decode(False, q, pool, page_table, topk_idx, seq_lens, sm_scale, out, lse, workspace,
+    return _decode("nvfp4", q, pool, page_table, topk_idx, seq_lens, sm_scale, out, lse, workspace,
                    force_splits, dev_err)
 
 
@@ -227,8 +251,58 @@ def sparse_mla_decode_latent(q: torch.Tensor, pool: torch.Tensor, page_table: to
                              dev_err: torch.Tensor | None = None):
     """The same decode over latent-only rows: q bf16 [B,Sq,H,512], pool uint8
     [num_slots,288]; QK^T over the 512 latent columns."""
-    return _decode(True, q, pool, page_table, topk_idx, seq_lens, sm_scale, out, lse, workspace,
+    return _decode("latent", q, pool, page_table, topk_idx, seq_lens, sm_scale, out, lse,
+                   workspace, force_splits, dev_err)
+
+
+def sparse_mla_decode_fp8(q: torch.Tensor, pool: torch.Tensor, page_table: torch.Tensor,
+                          topk_idx: torch.Tensor, seq_lens: torch.Tensor, sm_scale: float,
+                          out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
+                          workspace: torch.Tensor | None = None, force_splits: int = 0,
+                          dev_err: torch.Tensor | None = None):
+    """The decode over 576-byte FP8 rows (q bf16 [B,Sq,H,576]; pool uint8
+    [num_slots,576]) -- the comparison path of the NVFP4 decode."""
+    return _decode("fp8", q, pool, page_table, topk_idx, seq_lens, sm_scale, out, lse, workspace,
                    force_splits, dev_err)
+
+
+def fp8_scratch(pool: torch.Tensor, page_table: torch.Tensor, topk_idx: torch.Tensor,
+                seq_lens: torch.Tensor, scratch: torch.Tensor | None = None,
+                dev_err: torch.Tensor | None = None) -> torch.Tensor:
+    """The FP8 scratch copy of the NVFP4 rows the keys select: uint8
+    [B*Sq*K, 576] (E4M3 of the dequantized values; masked keys give zero rows)."""
+    lib = load_library()
+    B, Sq, K = topk_idx.shape
+    if scratch is None:
+        scratch = torch.empty((B * Sq * K, ROW_BYTES_FP8), dtype=torch.uint8, device=pool.device)
+    _check("kv4_fp8_scratch", lib.kv4_fp8_scratch(
+        _dev(pool, "pool", torch.uint8), pool.shape[0],
+        _dev(page_table, "page_table", torch.int32), page_table.shape[1], PAGE,
+        _dev(topk_idx, "topk_idx", torch.int32), K, _dev(seq_lens, "seq_lens", torch.int32),
+        B, Sq, _dev(scratch, "scratch", torch.uint8), _err_ptr(dev_err), _stream(pool.device)))
+    return scratch
+
+
+def scratch_index(topk_idx: torch.Tensor, seq_lens: torch.Tensor):
+    """Indexing that makes a scratch copy (row (b*Sq + s)*K + k for key k of
+    token s of request b) look like a paged pool: (page_table, topk, seq_lens)
+    for a decode of B*Sq one-token requests whose K positions are 0..K-1,
+    masked where the original key is masked.  K must be a multiple of 64."""
+    B, Sq, K = topk_idx.shape
+    if K % PAGE:
+        raise ValueError("the scratch path needs K to be a multiple of 64")
+    dev = topk_idx.device
+    n = B * Sq
+    pages = K // PAGE
+    page_table = (torch.arange(n, device=dev, dtype=torch.int32)[:, None] * pages +
+                  torch.arange(pages, device=dev, dtype=torch.int32)[None, :])
+    pos = torch.arange(K, device=dev, dtype=torch.int32)
+    s_idx = torch.arange(Sq, device=dev)
+    l_eff = seq_lens.to(torch.int64)[:, None] - (Sq - 1 - s_idx)[None, :]          # [B, Sq]
+    valid = (topk_idx >= 0) & (topk_idx.to(torch.int64) < l_eff[..., None])
+    topk = torch.where(valid, pos, torch.full_like(pos, -1)).reshape(n, 1, K).contiguous()
+    lens = torch.full((n,), K, dtype=torch.int32, device=dev)
+    return page_table.contiguous(), topk, lens
 
 
 def sparse_mla_decode_partial(q: torch.Tensor, pool: torch.Tensor, page_table: torch.Tensor,
@@ -241,7 +315,7 @@ def sparse_mla_decode_partial(q: torch.Tensor, pool: torch.Tensor, page_table: t
     if out is None:
         B, Sq, H, _ = q.shape
         out = torch.empty((B, Sq, H, LATENT), dtype=torch.float32, device=q.device)
-    return _decode(False, q, pool, page_table, topk_idx, seq_lens, sm_scale, out, lse, workspace,
+    return _decode("nvfp4", q, pool, page_table, topk_idx, seq_lens, sm_scale, out, lse, workspace,
                    force_splits, dev_err, partial=True)
 
 
@@ -304,11 +378,14 @@ def dcp_sparse_mla_decode(q, pool, page_table, topk_idx, seq_lens, sm_scale, gro
     return merge_partials(o_parts, lse_parts)
 
 
-def _decode(latent_only, q, pool, page_table, topk_idx, seq_lens, sm_scale, out, lse, workspace,
+def _decode(fmt, q, pool, page_table, topk_idx, seq_lens, sm_scale, out, lse, workspace,
             force_splits, dev_err, partial=False):
+    """fmt: "nvfp4" (352-byte rows), "latent" (288-byte rows) or "fp8" (576)."""
     lib = load_library()
     B, Sq, H, D = q.shape
-    qk, row = (LATENT, ROW_BYTES_LATENT) if latent_only else (QK_DIM, ROW_BYTES)
+    fp8, latent_only = fmt == "fp8", fmt == "latent"
+    qk, row = ((LATENT, ROW_BYTES_LATENT) if latent_only else
+               (QK_DIM, ROW_BYTES_FP8) if fp8 else (QK_DIM, ROW_BYTES))
     if D != qk:
         raise ValueError(f"q must be [B, Sq, H, {qk}]")
     if pool.dim() != 2 or pool.shape[1] != row:
@@ -323,9 +400,10 @@ def _decode(latent_only, q, pool, page_table, topk_idx, seq_lens, sm_scale, out,
     if lse is None:
         lse = torch.empty((B, Sq, H), dtype=torch.float32, device=dev)
     fn = ("kv4_sparse_mla_decode_latent" if latent_only else
+          "kv4_sparse_mla_decode_fp8" if fp8 else
           "kv4_sparse_mla_decode_partial" if partial else "kv4_sparse_mla_decode")
-    splits, ws_bytes = (decode_plan_latent if latent_only else decode_plan)(B, Sq, H, K,
-                                                                           force_splits)
+    plan = decode_plan_latent if latent_only else decode_plan_fp8 if fp8 else decode_plan
+    splits, ws_bytes = plan(B, Sq, H, K, force_splits)
     if workspace is None:
         workspace = _workspace(dev, ws_bytes)
     ws_ptr = None if workspace is None else _dev(workspace, "workspace", workspace.dtype)

@@ -62,7 +62,7 @@ struct Plan {
 // to the smaller S.  One block runs per SM.  The fixed cost (prologue: Q
 // load and conversion, first dependent loads; epilogue: output or partial
 // writes) is about two tiles of work.
-Plan make_plan(int B, int Sq, int H, int K, int force_splits, int sms, bool rope) {
+Plan make_plan(int B, int Sq, int H, int K, int force_splits, int sms, int fmt) {
   Plan p{};
   p.HG = heads_per_block(H);
   p.units = B * Sq * (H / p.HG);
@@ -89,7 +89,7 @@ Plan make_plan(int B, int Sq, int H, int K, int force_splits, int sms, bool rope
   // the device at once; otherwise the partials go to the workspace for
   // merge_kernel.
   p.cluster_merge = p.splits > 1 && p.splits <= kv4::kMaxClusterSplits &&
-                    p.units <= kv4::decode_max_active_clusters(p.HG, p.splits, rope);
+                    p.units <= kv4::decode_max_active_clusters(p.HG, p.splits, fmt);
   p.ws_bytes = (p.splits > 1 && !p.cluster_merge)
                    ? static_cast<size_t>(p.units) * p.splits * p.HG * (KV4_LATENT + 1) *
                          sizeof(float)
@@ -108,8 +108,9 @@ kv4_status check_decode_shape(int B, int Sq, int H, int K) {
 
 namespace {
 
-// The entry points below share these bodies; `rope` selects the 352-byte row
-// (latent + rope) or the 288-byte latent-only row.
+// The entry points below share these bodies.  For the cache write, `rope`
+// selects the 352-byte row (latent + rope) or the 288-byte latent-only row;
+// for the decode, `fmt` is the row format (kv4_launch.h).
 kv4_status quantize_impl(const void* latent_dev, int64_t latent_row_stride, const void* rope_dev,
                          int64_t rope_row_stride, const int64_t* slot_mapping_dev,
                          int64_t n_tokens, uint8_t* pool_dev, int64_t num_slots,
@@ -131,20 +132,20 @@ kv4_status quantize_impl(const void* latent_dev, int64_t latent_row_stride, cons
   if (st != KV4_OK) return st;
   kv4::QuantizeArgs a{latent_dev, latent_row_stride, rope ? rope_dev : nullptr,
                       rope ? rope_row_stride : 0, slot_mapping_dev, n_tokens, pool_dev,
-                      num_slots, row_bytes, dev_err, mse ? 1 : 0};
+                      num_slots, row_bytes, dev_err, mse ? 1 : 0, 0};
   return kv4::launch_quantize_write(a, sms, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
              ? KV4_OK
              : KV4_ERR_LAUNCH;
 }
 
 kv4_status plan_impl(int B, int Sq, int H, int K, int force_splits, int* splits,
-                     size_t* workspace_bytes, bool rope) {
+                     size_t* workspace_bytes, int fmt) {
   const kv4_status shape = check_decode_shape(B, Sq, H, K);
   if (shape != KV4_OK) return shape;
   int sms = 0;
   const kv4_status st = device_info(&sms);
   if (st != KV4_OK) return st;
-  const Plan p = make_plan(B, Sq, H, K, force_splits, sms, rope);
+  const Plan p = make_plan(B, Sq, H, K, force_splits, sms, fmt);
   if (splits) *splits = p.splits;
   if (workspace_bytes) *workspace_bytes = p.ws_bytes;
   return KV4_OK;
@@ -155,7 +156,7 @@ kv4_status decode_impl(const void* q_dev, const uint8_t* pool_dev, int64_t num_s
                        const int32_t* topk_idx_dev, int K, const int32_t* seq_lens_dev, int B,
                        int Sq, int H, float sm_scale, void* out_dev, float* lse_dev,
                        void* workspace_dev, size_t workspace_bytes, int force_splits,
-                       int32_t* dev_err, kv4_stream_t stream, bool rope, bool out_f32 = false) {
+                       int32_t* dev_err, kv4_stream_t stream, int fmt, bool out_f32 = false) {
   const kv4_status shape = check_decode_shape(B, Sq, H, K);
   if (shape != KV4_OK) return shape;
   if (page_size != KV4_PAGE) return KV4_ERR_UNSUPPORTED;
@@ -174,7 +175,7 @@ kv4_status decode_impl(const void* q_dev, const uint8_t* pool_dev, int64_t num_s
   int sms = 0;
   const kv4_status st = device_info(&sms);
   if (st != KV4_OK) return st;
-  const Plan p = make_plan(B, Sq, H, K, force_splits, sms, rope);
+  const Plan p = make_plan(B, Sq, H, K, force_splits, sms, fmt);
   if (p.ws_bytes > 0 &&
       (workspace_dev == nullptr || workspace_bytes < p.ws_bytes || !aligned16(workspace_dev)))
     return KV4_ERR_WORKSPACE;
@@ -198,7 +199,7 @@ kv4_status decode_impl(const void* q_dev, const uint8_t* pool_dev, int64_t num_s
   a.out = out_dev;
   a.lse = lse_dev;
   a.cluster_merge = p.cluster_merge ? 1 : 0;
-  a.rope = rope ? 1 : 0;
+  a.fmt = fmt;
   a.out_f32 = out_f32 ? 1 : 0;
   if (p.splits > 1 && !p.cluster_merge) {
     a.ws_o = static_cast<float*>(workspace_dev);
@@ -250,7 +251,7 @@ kv4_status kv4_quantize_write(const void* latent_dev, int64_t latent_row_stride,
 
 kv4_status kv4_decode_plan(int B, int Sq, int H, int K, int force_splits, int* splits,
                            size_t* workspace_bytes) {
-  return plan_impl(B, Sq, H, K, force_splits, splits, workspace_bytes, true);
+  return plan_impl(B, Sq, H, K, force_splits, splits, workspace_bytes, kv4::kFmtNvfp4);
 }
 
 kv4_status kv4_sparse_mla_decode(const void* q_dev, const uint8_t* pool_dev, int64_t num_slots,
@@ -261,7 +262,8 @@ kv4_status kv4_sparse_mla_decode(const void* q_dev, const uint8_t* pool_dev, int
                                  int force_splits, int32_t* dev_err, kv4_stream_t stream) {
   return decode_impl(q_dev, pool_dev, num_slots, page_table_dev, pt_stride, page_size,
                      topk_idx_dev, K, seq_lens_dev, B, Sq, H, sm_scale, out_dev, lse_dev,
-                     workspace_dev, workspace_bytes, force_splits, dev_err, stream, true);
+                     workspace_dev, workspace_bytes, force_splits, dev_err, stream,
+                     kv4::kFmtNvfp4);
 }
 
 kv4_status kv4_debug_gather_dequant(const uint8_t* pool_dev, int64_t num_slots,
@@ -294,7 +296,8 @@ kv4_status kv4_sparse_mla_decode_partial(const void* q_dev, const uint8_t* pool_
                                          kv4_stream_t stream) {
   return decode_impl(q_dev, pool_dev, num_slots, page_table_dev, pt_stride, page_size,
                      topk_idx_dev, K, seq_lens_dev, B, Sq, H, sm_scale, o_dev, lse_dev,
-                     workspace_dev, workspace_bytes, force_splits, dev_err, stream, true, true);
+                     workspace_dev, workspace_bytes, force_splits, dev_err, stream,
+                     kv4::kFmtNvfp4, true);
 }
 
 kv4_status kv4_dcp_mask_topk(const int32_t* topk_idx_dev, const int32_t* page_table_dev,
@@ -332,6 +335,74 @@ kv4_status kv4_merge_partials(const float* o_parts_dev, const float* lse_parts_d
              : KV4_ERR_LAUNCH;
 }
 
+kv4_status kv4_quantize_write_fp8(const void* latent_dev, int64_t latent_row_stride,
+                                  const void* rope_dev, int64_t rope_row_stride,
+                                  const int64_t* slot_mapping_dev, int64_t n_tokens,
+                                  uint8_t* pool_dev, int64_t num_slots, int32_t* dev_err,
+                                  kv4_stream_t stream) {
+  if (n_tokens < 0 || num_slots < 0) return KV4_ERR_INVALID_ARG;
+  if (n_tokens == 0) return KV4_OK;
+  if (!latent_dev || !rope_dev || !slot_mapping_dev || !pool_dev) return KV4_ERR_INVALID_ARG;
+  if (latent_row_stride < KV4_LATENT || latent_row_stride % 8 != 0 ||
+      rope_row_stride < KV4_ROPE || rope_row_stride % 8 != 0)
+    return KV4_ERR_INVALID_ARG;
+  if (!aligned16(latent_dev) || !aligned16(rope_dev) || !aligned16(pool_dev) ||
+      (reinterpret_cast<uintptr_t>(slot_mapping_dev) & 7u) != 0)
+    return KV4_ERR_INVALID_ARG;
+  if (num_slots > INT64_MAX / KV4_ROW_BYTES_FP8) return KV4_ERR_INVALID_ARG;
+  int sms = 0;
+  const kv4_status st = device_info(&sms);
+  if (st != KV4_OK) return st;
+  kv4::QuantizeArgs a{latent_dev, latent_row_stride, rope_dev,     rope_row_stride, slot_mapping_dev,
+                      n_tokens,   pool_dev,          num_slots,    KV4_ROW_BYTES_FP8, dev_err,
+                      0,          1};
+  return kv4::launch_quantize_write(a, sms, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? KV4_OK
+             : KV4_ERR_LAUNCH;
+}
+
+kv4_status kv4_decode_plan_fp8(int B, int Sq, int H, int K, int force_splits, int* splits,
+                               size_t* workspace_bytes) {
+  return plan_impl(B, Sq, H, K, force_splits, splits, workspace_bytes, kv4::kFmtFp8);
+}
+
+kv4_status kv4_sparse_mla_decode_fp8(const void* q_dev, const uint8_t* pool_dev,
+                                     int64_t num_slots, const int32_t* page_table_dev,
+                                     int64_t pt_stride, int page_size,
+                                     const int32_t* topk_idx_dev, int K,
+                                     const int32_t* seq_lens_dev, int B, int Sq, int H,
+                                     float sm_scale, void* out_dev, float* lse_dev,
+                                     void* workspace_dev, size_t workspace_bytes,
+                                     int force_splits, int32_t* dev_err, kv4_stream_t stream) {
+  return decode_impl(q_dev, pool_dev, num_slots, page_table_dev, pt_stride, page_size,
+                     topk_idx_dev, K, seq_lens_dev, B, Sq, H, sm_scale, out_dev, lse_dev,
+                     workspace_dev, workspace_bytes, force_splits, dev_err, stream,
+                     kv4::kFmtFp8);
+}
+
+kv4_status kv4_fp8_scratch(const uint8_t* pool_dev, int64_t num_slots,
+                           const int32_t* page_table_dev, int64_t pt_stride, int page_size,
+                           const int32_t* topk_idx_dev, int K, const int32_t* seq_lens_dev,
+                           int B, int Sq, uint8_t* scratch_dev, int32_t* dev_err,
+                           kv4_stream_t stream) {
+  if (B < 0 || Sq < 1 || K < 0) return KV4_ERR_INVALID_ARG;
+  if (page_size != KV4_PAGE) return KV4_ERR_UNSUPPORTED;
+  if (B == 0 || K == 0) return KV4_OK;
+  if (!pool_dev || !page_table_dev || !topk_idx_dev || !seq_lens_dev || !scratch_dev)
+    return KV4_ERR_INVALID_ARG;
+  if (num_slots < 0 || num_slots > INT32_MAX || pt_stride < 1 || pt_stride > INT32_MAX)
+    return KV4_ERR_INVALID_ARG;
+  if (!aligned16(pool_dev) || !aligned16(scratch_dev)) return KV4_ERR_INVALID_ARG;
+  int sms = 0;
+  const kv4_status st = device_info(&sms);
+  if (st != KV4_OK) return st;
+  kv4::GatherArgs a{pool_dev, num_slots,    page_table_dev, pt_stride, topk_idx_dev, K,
+                    seq_lens_dev, B,         Sq,             scratch_dev, 1,          dev_err};
+  return kv4::launch_fp8_scratch(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? KV4_OK
+             : KV4_ERR_LAUNCH;
+}
+
 kv4_status kv4_quantize_write_latent(const void* latent_dev, int64_t latent_row_stride,
                                      const int64_t* slot_mapping_dev, int64_t n_tokens,
                                      uint8_t* pool_dev, int64_t num_slots, int32_t* dev_err,
@@ -342,7 +413,7 @@ kv4_status kv4_quantize_write_latent(const void* latent_dev, int64_t latent_row_
 
 kv4_status kv4_decode_plan_latent(int B, int Sq, int H, int K, int force_splits, int* splits,
                                   size_t* workspace_bytes) {
-  return plan_impl(B, Sq, H, K, force_splits, splits, workspace_bytes, false);
+  return plan_impl(B, Sq, H, K, force_splits, splits, workspace_bytes, kv4::kFmtNvfp4Latent);
 }
 
 kv4_status kv4_sparse_mla_decode_latent(const void* q_dev, const uint8_t* pool_dev,
@@ -356,7 +427,8 @@ kv4_status kv4_sparse_mla_decode_latent(const void* q_dev, const uint8_t* pool_d
                                         kv4_stream_t stream) {
   return decode_impl(q_dev, pool_dev, num_slots, page_table_dev, pt_stride, page_size,
                      topk_idx_dev, K, seq_lens_dev, B, Sq, H, sm_scale, out_dev, lse_dev,
-                     workspace_dev, workspace_bytes, force_splits, dev_err, stream, false);
+                     workspace_dev, workspace_bytes, force_splits, dev_err, stream,
+                     kv4::kFmtNvfp4Latent);
 }
 
 kv4_status kv4_debug_gather_dequant_latent(const uint8_t* pool_dev, int64_t num_slots,
@@ -422,7 +494,7 @@ kv4_status kv4_sparse_mla_decode_noalloc(const void* q_dev, const uint8_t* pool_
   int sms = 0;
   kv4_status st = device_info(&sms);
   if (st != KV4_OK) return st;
-  const Plan p = make_plan(B, Sq, H, K, force_splits, sms, true);
+  const Plan p = make_plan(B, Sq, H, K, force_splits, sms, kv4::kFmtNvfp4);
   if (p.ws_bytes > kStaticScratchBytes) return KV4_ERR_SCRATCH_LIMIT;
   void* scratch = nullptr;
   st = static_scratch(&scratch);

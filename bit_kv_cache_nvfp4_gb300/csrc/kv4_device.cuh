@@ -18,6 +18,7 @@ namespace kv4 {
 
 constexpr int kRowBytes = 352;
 constexpr int kRowBytesLatent = 288;   // latent-only row: codes + scales, no rope
+constexpr int kRowBytesFp8 = 576;      // E4M3 latent + rope (the comparison row)
 constexpr int kLatent = 512;
 constexpr int kRope = 64;
 constexpr int kQk = 576;
@@ -431,6 +432,17 @@ __device__ __forceinline__ uint32_t f16x2_mul(uint32_t a, uint32_t b) {
 //   lat_lo: latent 8l..8l+7, lat_hi: latent 256+8l..256+8l+7,
 //   rope:   rope 4(l-8)..4(l-8)+3 (lanes 8..23 only).
 // Every lane of the warp must call this (it shuffles).
+// Two f16 values (f16x2, element 0 in the low half) -> two E4M3 bytes
+// (element 0 in the low byte), round half to even, saturating at 448.  Via
+// fp32, which holds every f16 value exactly.
+__device__ __forceinline__ uint32_t f16x2_to_e4m3x2(uint32_t h2) {
+  const __half2 h = *reinterpret_cast<const __half2*>(&h2);
+  const float lo = __low2float(h), hi = __high2float(h);
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
 struct DequantRow {
   uint4 lat_lo, lat_hi;
   uint2 rope;

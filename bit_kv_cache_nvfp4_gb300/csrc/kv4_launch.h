@@ -10,6 +10,12 @@
 
 namespace kv4 {
 
+// Row formats of the pool:
+//   kFmtNvfp4        352 B: E2M1 latent codes, E4M3 scales, E4M3 rope; q of 576
+//   kFmtNvfp4Latent  288 B: the same without rope; q of 512
+//   kFmtFp8          576 B: E4M3 latent and rope (the comparison row); q of 576
+enum RowFormat : int { kFmtNvfp4 = 0, kFmtNvfp4Latent = 1, kFmtFp8 = 2 };
+
 struct QuantizeArgs {
   const void* latent;
   int64_t latent_stride;
@@ -22,6 +28,7 @@ struct QuantizeArgs {
   int row_bytes;               // 352 (latent + rope) or 288 (latent only; rope unused)
   int32_t* dev_err;
   int mse;                     // 1: MSE-searched block scales instead of amax/6
+  int fp8;                     // 1: 576-byte FP8 rows (E4M3 of every value; row_bytes 576)
 };
 
 struct DecodeArgs {
@@ -47,7 +54,7 @@ struct DecodeArgs {
   int fault_site;
   cudaEvent_t after_decode;    // recorded between the decode and merge kernels (may be null)
   int cluster_merge;           // splits > 1 merged inside a cluster of `splits` blocks
-  int rope;                    // 1: 352-byte rows, q of 576 columns; 0: 288-byte rows, q of 512
+  int fmt;                     // row format: kFmtNvfp4, kFmtNvfp4Latent or kFmtFp8
   int out_f32;                 // 1: out is fp32 (a context-parallel rank's partial), else bf16
 };
 
@@ -106,12 +113,15 @@ cudaError_t launch_merge_partials(const float* o_parts, const float* lse_parts, 
                                   cudaStream_t stream);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 cudaError_t launch_debug_gather(const GatherArgs& a, cudaStream_t stream);
-size_t decode_smem_bytes(int HG, bool rope);
+// The FP8 scratch copy of the rows the keys select: a.rows is uint8
+// [B*Sq*K, 576] (E4M3 of the dequantized NVFP4 values; masked keys 0).
+cudaError_t launch_fp8_scratch(const GatherArgs& a, cudaStream_t stream);
+size_t decode_smem_bytes(int HG, int fmt);
 // How many clusters of `splits` blocks of the HG variant can be resident at
 // once on this device (0: such clusters cannot run).  A unit split in two
 // runs as a cluster of two blocks that merge through distributed shared
 // memory; more splits merge through the workspace.
-int decode_max_active_clusters(int HG, int splits, bool rope);
+int decode_max_active_clusters(int HG, int splits, int fmt);
 constexpr int kMaxClusterSplits = 2;
 
 }  // namespace kv4

@@ -13,7 +13,9 @@
 // one.  Bytes: 1152 read, 352 written per token; at 1M tokens the IEEE
 // divisions (17 per lane and token) rather than HBM bound the kernel.  Rows of 288 bytes (the latent-only layout of the same README
 // section, for models whose keys carry no rope part) are the first 288
-// bytes of the same row: no rope is read or written.
+// bytes of the same row: no rope is read or written.  With a.fp8 the row is
+// the 576-byte FP8 row the NVFP4 row replaces (E4M3 of every latent and rope
+// value, no scale), for the comparison paths.
 //
 // With a.mse set, each block's scale is searched instead (README "4-bit KV
 // cache", DeepSeek V4 Pro bullet: "an MSE-searched scale"; the search rule
@@ -126,6 +128,25 @@ __global__ void __launch_bounds__(256) quantize_write_kernel(QuantizeArgs a) {
     const uint4 v0 = cur.v0;
     const uint4 v1 = cur.v1;
     const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    if (a.fp8) {
+      // 576-byte FP8 row: every latent and rope value as E4M3 (no scale)
+      uint8_t* row = a.pool + slot * a.row_bytes;
+      uint32_t b[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        b[i] = f32x2_to_e4m3x2(bf16_high(w[2 * i]), bf16_low(w[2 * i])) |
+               (f32x2_to_e4m3x2(bf16_high(w[2 * i + 1]), bf16_low(w[2 * i + 1])) << 16);
+      *reinterpret_cast<uint4*>(row + lane * 16) = make_uint4(b[0], b[1], b[2], b[3]);
+      if (lane < 8) {
+        const uint4 rv = cur.rv;
+        const uint32_t lo = f32x2_to_e4m3x2(bf16_high(rv.x), bf16_low(rv.x)) |
+                            (f32x2_to_e4m3x2(bf16_high(rv.y), bf16_low(rv.y)) << 16);
+        const uint32_t hi = f32x2_to_e4m3x2(bf16_high(rv.z), bf16_low(rv.z)) |
+                            (f32x2_to_e4m3x2(bf16_high(rv.w), bf16_low(rv.w)) << 16);
+        *reinterpret_cast<uint2*>(row + 512 + lane * 8) = make_uint2(lo, hi);
+      }
+      continue;
+    }
     float x[16];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {

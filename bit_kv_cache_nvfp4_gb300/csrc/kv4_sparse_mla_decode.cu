@@ -43,6 +43,8 @@
 
 #include <math.h>
 
+#include <type_traits>
+
 namespace kv4 {
 namespace {
 
@@ -67,13 +69,15 @@ static_assert(kPvIssuers == 2 || kPvIssuers == 4, "PV issuers");
 constexpr int kBarCompute = 3;            // named barrier of the 256 compute threads (1, 2: softmax groups)
 constexpr float kRaiseThreshold = 8.0f;   // log2 units: p <= 256 between raises
 
-// ROPE: rows of 352 B (latent + rope, QK over 576 columns) or of 288 B
-// (latent only, QK over the 512 latent columns).
-template <int HG, bool ROPE>
+// FMT: the pool's row format (kv4_launch.h): 352-byte NVFP4 rows (QK over
+// 576 columns), 288-byte latent-only NVFP4 rows (QK over the 512 latent
+// columns) or 576-byte FP8 rows (QK over 576 columns).
+template <int HG, int FMT>
 struct Layout {
   static constexpr int HPT = HG / 2;                                  // heads per softmax group
-  static constexpr int QK = ROPE ? kQk : kLatent;                     // columns of QK^T
-  static constexpr int row_bytes = ROPE ? kRowBytes : kRowBytesLatent;
+  static constexpr int QK = FMT == kFmtNvfp4Latent ? kLatent : kQk;   // columns of QK^T
+  static constexpr int row_bytes =
+      FMT == kFmtNvfp4 ? kRowBytes : (FMT == kFmtNvfp4Latent ? kRowBytesLatent : kRowBytesFp8);
   static constexpr uint32_t q_slabs = QK / 64;                        // 64-column slabs of Q
   static constexpr uint32_t q_bytes = q_slabs * HG * 128u;            // Q
   static constexpr uint32_t kv_off = (q_bytes + 1023u) & ~1023u;
@@ -266,9 +270,11 @@ __device__ __forceinline__ void tmem_scale_cols(uint32_t taddr, const float* alp
   }
 }
 
-template <int HG, bool ROPE>
+template <int HG, int FMT>
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
-  using L = Layout<HG, ROPE>;
+  using L = Layout<HG, FMT>;
+  constexpr bool ROPE = FMT != kFmtNvfp4Latent;     // rows carry a rope part
+  constexpr bool FP8 = FMT == kFmtFp8;
   constexpr int HPT = L::HPT;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -502,31 +508,61 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
     //   wa(l) = l < 16 ? l : l + 16,   wb(l) = wa(l) + 16.
     // Each group is reloaded for the next tile right after the pass that
     // consumed it, so the gather is spread over the whole tile.
-    constexpr int kExtraLanes = ROPE ? 24 : 8;        // lanes loading words 64 + l
+    // An NVFP4 row's latent word w (8 codes) and an FP8 row's 8-byte latent
+    // unit w (8 E4M3 values) both become the f16 unit of columns 8w..8w+7.
+    // The extra word of lane l is word 64 + l of an NVFP4 row (scales, rope)
+    // and word 120 + l of an FP8 row (rope only, lanes 8..23).
+    using LatWord = std::conditional_t<FP8, uint2, uint32_t>;
+    constexpr int kExtraWord0 = FP8 ? 120 : 64;
+    const bool extra_lane = FP8 ? (lane >= 8 && lane < 24) : (lane < (ROPE ? 24 : 8));
     const int word_a = lane < 16 ? lane : lane + 16;
     const int word_b = word_a + 16;
-    uint32_t wa[16], wb[16], wex[16];
+    LatWord wa[16], wb[16];
+    uint32_t wex[16];
     // one word of each of this warp's 16 rows of the tile whose slots are
     // at `slots` (the slots are re-read from shared memory for every group,
     // so that they hold no registers across the tile)
-    auto load_words = [&](uint32_t (&w)[16], const int32_t* slots, int word, bool active) {
-      int32_t sv[16];
+    auto read_slots = [&](const int32_t* slots, int32_t (&sv)[16]) {
 #pragma unroll
       for (int i = 0; i < 16; i += 4) {
         const int4 t = *reinterpret_cast<const int4*>(slots + warp * 16 + i);
         sv[i] = t.x; sv[i + 1] = t.y; sv[i + 2] = t.z; sv[i + 3] = t.w;
       }
+    };
+    auto load_latent = [&](LatWord (&w)[16], const int32_t* slots, int word) {
+      int32_t sv[16];
+      read_slots(slots, sv);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const uint8_t* row = a.pool + static_cast<int64_t>(sv[i]) * L::row_bytes;
+        if constexpr (FP8)
+          w[i] = sv[i] >= 0 ? __ldg(reinterpret_cast<const uint2*>(row) + word) : make_uint2(0, 0);
+        else
+          w[i] = sv[i] >= 0 ? __ldg(reinterpret_cast<const uint32_t*>(row) + word) : 0u;
+      }                                                    // masked key: zero row
+    };
+    auto load_extra = [&](uint32_t (&w)[16], const int32_t* slots) {
+      int32_t sv[16];
+      read_slots(slots, sv);
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         const uint32_t* row =
             reinterpret_cast<const uint32_t*>(a.pool + static_cast<int64_t>(sv[i]) * L::row_bytes);
-        w[i] = (sv[i] >= 0 && active) ? __ldg(row + word) : 0u;    // masked key: zero row
+        w[i] = (sv[i] >= 0 && extra_lane) ? __ldg(row + kExtraWord0 + lane) : 0u;
+      }
+    };
+    auto dequant_latent = [&](const LatWord& w, uint32_t w_ex, int word) -> uint4 {
+      if constexpr (FP8) {
+        const uint2 lo = dequant_rope(w.x), hi = dequant_rope(w.y);
+        return make_uint4(lo.x, lo.y, hi.x, hi.y);
+      } else {
+        return dequant_latent_word(w, w_ex, word);
       }
     };
     if (my_tiles > 0) {
-      load_words(wa, slot_s, word_a, true);
-      load_words(wb, slot_s, word_b, true);
-      load_words(wex, slot_s, 64 + lane, lane < kExtraLanes);
+      load_latent(wa, slot_s, word_a);
+      load_latent(wb, slot_s, word_b);
+      load_extra(wex, slot_s);
     }
 
     // dequant store addresses (shared-window): latent word w of row r goes to
@@ -569,11 +605,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
 #pragma unroll
       for (int i = 0; i < 16; ++i)
         st_shared_v4(a_base[i & 7] + (i >> 3) * 1024 + (i & 7) * 128,
-                     dequant_latent_word(wa[i], wex[i], word_a));
+                     dequant_latent(wa[i], wex[i], word_a));
       fence_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_part0);
-      if (it + 1 < my_tiles) load_words(wa, next_slots, word_a, true);   // next tile
+      if (it + 1 < my_tiles) load_latent(wa, next_slots, word_a);        // next tile
       // pass B: slabs 2,3 and 6,7 (PV slabs 1 and 3; PV is then complete)
       if (it > 0) {
         wait(bar_pv0 + 8, par ^ 1);
@@ -584,11 +620,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
 #pragma unroll
       for (int i = 0; i < 16; ++i)
         st_shared_v4(b_base[i & 7] + (i >> 3) * 1024 + (i & 7) * 128,
-                     dequant_latent_word(wb[i], wex[i], word_b));
+                     dequant_latent(wb[i], wex[i], word_b));
       fence_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_part0 + 8);
-      if (it + 1 < my_tiles) load_words(wb, next_slots, word_b, true);
+      if (it + 1 < my_tiles) load_latent(wb, next_slots, word_b);
       if constexpr (ROPE) {
         // pass C: rope -> slab 8 (the previous tile's P lived there; PV is done)
         if (lane >= 8 && lane < 24) {
@@ -600,7 +636,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_part0 + 16);
       }
-      if (it + 1 < my_tiles) load_words(wex, next_slots, 64 + lane, lane < kExtraLanes);
+      if (it + 1 < my_tiles) load_extra(wex, next_slots);
 
       // ---- a2, second step: page-table entry of the key two tiles ahead
       if (resolve_ahead) {
@@ -906,7 +942,53 @@ __global__ void __launch_bounds__(256) debug_gather_kernel(GatherArgs a) {
     *reinterpret_cast<uint2*>(out + 512 + 4 * (lane - 8)) = d.rope;
 }
 
-template <int HG, bool ROPE>
+// The FP8 scratch copy (the comparison path the README's kv4mla bullet
+// measures against): for every (b, s, k), the NVFP4 row the key selects,
+// dequantized as in the decode and cast to E4M3, into a 576-byte row of
+// a.rows; masked keys give zero rows.  One warp per (b, s, k) row.
+__global__ void __launch_bounds__(256) fp8_scratch_kernel(GatherArgs a) {
+  grid_dependency_wait();
+  grid_launch_dependents();
+  const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  const int64_t n = static_cast<int64_t>(a.B) * a.Sq * a.K;
+  if (gw >= n) return;
+  const int k = static_cast<int>(gw % a.K);
+  const int64_t bs = gw / a.K;
+  const int b = static_cast<int>(bs / a.Sq), s = static_cast<int>(bs % a.Sq);
+  const int64_t l_eff = static_cast<int64_t>(__ldg(a.seq_lens + b)) - (a.Sq - 1 - s);
+  int32_t slot = 0;
+  if (lane == 0)
+    slot = resolve_slot(a.topk + bs * a.K, k, a.K, l_eff,
+                        a.page_table + static_cast<int64_t>(b) * a.pt_stride, a.pt_stride,
+                        a.num_slots, a.dev_err);
+  slot = __shfl_sync(0xFFFFFFFFu, slot, 0);
+  uint32_t wlo = 0, whi = 0, wex = 0;
+  if (slot >= 0) {
+    const uint32_t* row =
+        reinterpret_cast<const uint32_t*>(a.pool + static_cast<int64_t>(slot) * kRowBytes);
+    wlo = __ldg(row + lane);
+    whi = __ldg(row + 32 + lane);
+    wex = lane < 24 ? __ldg(row + 64 + lane) : 0u;
+  }
+  const DequantRow d = dequant_row_words(wlo, whi, wex, lane, dequant_scale_selector(lane));
+  auto e4m3x8 = [](const uint4& h) {                     // 8 f16 -> 8 E4M3 bytes
+    return make_uint2(f16x2_to_e4m3x2(h.x) | (f16x2_to_e4m3x2(h.y) << 16),
+                      f16x2_to_e4m3x2(h.z) | (f16x2_to_e4m3x2(h.w) << 16));
+  };
+  uint2 lo = e4m3x8(d.lat_lo), hi = e4m3x8(d.lat_hi);
+  uint32_t rope = f16x2_to_e4m3x2(d.rope.x) | (f16x2_to_e4m3x2(d.rope.y) << 16);
+  if (slot < 0) {
+    lo = hi = make_uint2(0, 0);
+    rope = 0;
+  }
+  uint8_t* out = static_cast<uint8_t*>(a.rows) + gw * kRowBytesFp8;
+  *reinterpret_cast<uint2*>(out + 8 * lane) = lo;
+  *reinterpret_cast<uint2*>(out + 256 + 8 * lane) = hi;
+  if (lane >= 8 && lane < 24) *reinterpret_cast<uint32_t*>(out + 512 + 4 * (lane - 8)) = rope;
+}
+
+template <int HG, int FMT>
 cudaError_t configure_decode() {
   static cudaError_t state = cudaErrorNotReady;   // per process; attributes are per kernel
   if (state == cudaErrorNotReady) {
@@ -914,14 +996,14 @@ cudaError_t configure_decode() {
     // kLaunchRegs registers per thread; with fewer the compute warpgroups'
     // increase could never be granted, so refuse to launch instead.
     cudaFuncAttributes attr;
-    cudaError_t e = cudaFuncGetAttributes(&attr, decode_kernel<HG, ROPE>);
+    cudaError_t e = cudaFuncGetAttributes(&attr, decode_kernel<HG, FMT>);
     if (e == cudaSuccess && (attr.numRegs != kLaunchRegs || attr.maxThreadsPerBlock < kThreads))
       e = cudaErrorInvalidConfiguration;
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(decode_kernel<HG, ROPE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(Layout<HG, ROPE>::smem_bytes));
+      e = cudaFuncSetAttribute(decode_kernel<HG, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(Layout<HG, FMT>::smem_bytes));
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(decode_kernel<HG, ROPE>,
+      e = cudaFuncSetAttribute(decode_kernel<HG, FMT>,
                                cudaFuncAttributePreferredSharedMemoryCarveout,
                                cudaSharedmemCarveoutMaxShared);
     state = e;
@@ -929,17 +1011,17 @@ cudaError_t configure_decode() {
   return state;
 }
 
-template <int HG, bool ROPE>
+template <int HG, int FMT>
 int max_active_clusters_hg(int splits) {
   static int known[kMaxClusterSplits + 1] = {};   // 0 unknown, else 1 + the count
   if (splits < 2 || splits > kMaxClusterSplits) return 0;
   if (known[splits] == 0) {
     int n = 0;
-    if (configure_decode<HG, ROPE>() == cudaSuccess) {
+    if (configure_decode<HG, FMT>() == cudaSuccess) {
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(splits);
       cfg.blockDim = dim3(kThreads);
-      cfg.dynamicSmemBytes = Layout<HG, ROPE>::smem_bytes;
+      cfg.dynamicSmemBytes = Layout<HG, FMT>::smem_bytes;
       cudaLaunchAttribute attr[1];
       attr[0].id = cudaLaunchAttributeClusterDimension;
       attr[0].val.clusterDim.x = splits;
@@ -947,7 +1029,7 @@ int max_active_clusters_hg(int splits) {
       attr[0].val.clusterDim.z = 1;
       cfg.attrs = attr;
       cfg.numAttrs = 1;
-      if (cudaOccupancyMaxActiveClusters(&n, decode_kernel<HG, ROPE>, &cfg) != cudaSuccess) n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, decode_kernel<HG, FMT>, &cfg) != cudaSuccess) n = 0;
     }
     (void)cudaGetLastError();
     known[splits] = 1 + (n > 0 ? n : 0);
@@ -955,13 +1037,13 @@ int max_active_clusters_hg(int splits) {
   return known[splits] - 1;
 }
 
-template <int HG, bool ROPE>
+template <int HG, int FMT>
 cudaError_t launch_decode_hg(const DecodeArgs& a, cudaStream_t stream) {
-  const size_t smem = Layout<HG, ROPE>::smem_bytes;
-  cudaError_t e = configure_decode<HG, ROPE>();
+  const size_t smem = Layout<HG, FMT>::smem_bytes;
+  cudaError_t e = configure_decode<HG, FMT>();
   if (e != cudaSuccess) return e;
   const int units = a.B * a.Sq * (a.H / HG);
-  e = launch_pdl(decode_kernel<HG, ROPE>, static_cast<unsigned>(units * a.splits), kThreads, smem, stream,
+  e = launch_pdl(decode_kernel<HG, FMT>, static_cast<unsigned>(units * a.splits), kThreads, smem, stream,
                  a.cluster_merge ? a.splits : 1, a);
   if (e == cudaSuccess && a.after_decode != nullptr) e = cudaEventRecord(a.after_decode, stream);
   if (e != cudaSuccess || a.splits == 1 || a.cluster_merge) return e;
@@ -970,49 +1052,70 @@ cudaError_t launch_decode_hg(const DecodeArgs& a, cudaStream_t stream) {
                     units);
 }
 
-template <bool ROPE>
+template <int FMT>
 size_t decode_smem_bytes_r(int HG) {
   switch (HG) {
-    case 16: return Layout<16, ROPE>::smem_bytes;
-    case 32: return Layout<32, ROPE>::smem_bytes;
-    case 64: return Layout<64, ROPE>::smem_bytes;
+    case 16: return Layout<16, FMT>::smem_bytes;
+    case 32: return Layout<32, FMT>::smem_bytes;
+    case 64: return Layout<64, FMT>::smem_bytes;
     default: return 0;
   }
 }
 
-template <bool ROPE>
+template <int FMT>
 int decode_max_active_clusters_r(int HG, int splits) {
   switch (HG) {
-    case 16: return max_active_clusters_hg<16, ROPE>(splits);
-    case 32: return max_active_clusters_hg<32, ROPE>(splits);
-    case 64: return max_active_clusters_hg<64, ROPE>(splits);
+    case 16: return max_active_clusters_hg<16, FMT>(splits);
+    case 32: return max_active_clusters_hg<32, FMT>(splits);
+    case 64: return max_active_clusters_hg<64, FMT>(splits);
     default: return 0;
   }
 }
 
-template <bool ROPE>
+template <int FMT>
 cudaError_t launch_decode_r(const DecodeArgs& a, cudaStream_t stream) {
   switch (a.HG) {
-    case 16: return launch_decode_hg<16, ROPE>(a, stream);
-    case 32: return launch_decode_hg<32, ROPE>(a, stream);
-    case 64: return launch_decode_hg<64, ROPE>(a, stream);
+    case 16: return launch_decode_hg<16, FMT>(a, stream);
+    case 32: return launch_decode_hg<32, FMT>(a, stream);
+    case 64: return launch_decode_hg<64, FMT>(a, stream);
     default: return cudaErrorInvalidValue;
   }
 }
 
 }  // namespace
 
-size_t decode_smem_bytes(int HG, bool rope) {
-  return rope ? decode_smem_bytes_r<true>(HG) : decode_smem_bytes_r<false>(HG);
+size_t decode_smem_bytes(int HG, int fmt) {
+  switch (fmt) {
+    case kFmtNvfp4: return decode_smem_bytes_r<kFmtNvfp4>(HG);
+    case kFmtNvfp4Latent: return decode_smem_bytes_r<kFmtNvfp4Latent>(HG);
+    case kFmtFp8: return decode_smem_bytes_r<kFmtFp8>(HG);
+    default: return 0;
+  }
 }
 
-int decode_max_active_clusters(int HG, int splits, bool rope) {
-  return rope ? decode_max_active_clusters_r<true>(HG, splits)
-              : decode_max_active_clusters_r<false>(HG, splits);
+int decode_max_active_clusters(int HG, int splits, int fmt) {
+  switch (fmt) {
+    case kFmtNvfp4: return decode_max_active_clusters_r<kFmtNvfp4>(HG, splits);
+    case kFmtNvfp4Latent: return decode_max_active_clusters_r<kFmtNvfp4Latent>(HG, splits);
+    case kFmtFp8: return decode_max_active_clusters_r<kFmtFp8>(HG, splits);
+    default: return 0;
+  }
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
-  return a.rope ? launch_decode_r<true>(a, stream) : launch_decode_r<false>(a, stream);
+  switch (a.fmt) {
+    case kFmtNvfp4: return launch_decode_r<kFmtNvfp4>(a, stream);
+    case kFmtNvfp4Latent: return launch_decode_r<kFmtNvfp4Latent>(a, stream);
+    case kFmtFp8: return launch_decode_r<kFmtFp8>(a, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_fp8_scratch(const GatherArgs& a, cudaStream_t stream) {
+  const int64_t rows = static_cast<int64_t>(a.B) * a.Sq * a.K;
+  if (rows <= 0) return cudaSuccess;
+  return launch_pdl(fp8_scratch_kernel, static_cast<unsigned>((rows + 7) / 8), 256, 0, stream, 1,
+                    a);
 }
 
 cudaError_t launch_debug_gather(const GatherArgs& a, cudaStream_t stream) {

@@ -70,7 +70,8 @@ enum {
 enum {
   KV4_ROW_BYTES = 352, KV4_LATENT = 512, KV4_ROPE = 64, KV4_QK_DIM = 576,
   KV4_BLOCK = 16, KV4_PAGE = 64, KV4_TILE_KEYS = 128,
-  KV4_ROW_BYTES_LATENT = 288   /* latent-only row (the *_latent entry points) */
+  KV4_ROW_BYTES_LATENT = 288,  /* latent-only row (the *_latent entry points) */
+  KV4_ROW_BYTES_FP8 = 576      /* FP8 comparison row (the *_fp8 entry points)  */
 };
 
 /* ---------------------------------------------------------------------------
