@@ -84,7 +84,7 @@ struct Layout {
   static constexpr uint32_t kv_bytes = 9u * kChunkBytes;              // K/V tile
   static constexpr uint32_t ctl_off = kv_off + kv_bytes;
   // control block
-  static constexpr uint32_t bar_off = ctl_off;                        // uint64 x 11
+  static constexpr uint32_t bar_off = ctl_off;                        // uint64 x 12
   static constexpr uint32_t tmem_off = ctl_off + 96;                  // uint32
   static constexpr uint32_t slot_off = ctl_off + 112;                 // int32 [3][128]
   static constexpr uint32_t mref_off = slot_off + 3 * 128 * 4;        // float [HG]
@@ -302,7 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
   // mbarriers: QK done (all four issuers commit), PV done per 128-column
   // slab of O (slabs 0-1 from issuer 0, 2-3 from issuer 1), tile parts
   // written by the 8 compute warps (latent group a, latent group b, rope), P
-  // written, and the test hook's one.
+  // written, the test hook's one, the cluster merge's and Q staged.
   const uint32_t bars = smem_addr(smem + L::bar_off);
   const uint32_t bar_qk = bars;
   const uint32_t bar_pv0 = bars + 8;              // + 8 * slab: PV slab (128 columns) done
@@ -310,6 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
   const uint32_t bar_p = bars + 64;
   const uint32_t bar_fault = bars + 72;
   const uint32_t bar_merge = bars + 80;           // cluster merge: the peer's data arrived
+  const uint32_t bar_q = bars + 88;               // Q copied into the K/V region
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::tmem_off);
   int32_t* slot_s = reinterpret_cast<int32_t*>(smem + L::slot_off);
   float* m_ref = reinterpret_cast<float*>(smem + L::mref_off);
@@ -319,35 +320,67 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
   float* qscale = reinterpret_cast<float*>(smem + L::qscale_off);
 
   // ---- prologue ------------------------------------------------------------
+  bool timed_out = false;
+  auto wait = [&](uint32_t bar, uint32_t parity) {
+    if (!mbar_wait_bounded(bar, parity, a.timeout_ns)) timed_out = true;
+  };
+  const uint32_t kv_addr = smem_addr(kv_s);
+  constexpr int kQThread = 32 * (kComputeWarps + 1);   // inits the barriers, copies Q
   if (warp == kComputeWarps) tmem_alloc(smem_addr(tmem_slot), L::tmem_cols);
-  if (tid == 32 * (kComputeWarps + 1)) {
+  if (tid == kQThread) {
     mbar_init(bar_qk, 4);
     for (int p = 0; p < 4; ++p) mbar_init(bar_pv0 + 8 * p, 1);
     for (int p = 0; p < 3; ++p) mbar_init(bar_part0 + 8 * p, kComputeWarps);
     mbar_init(bar_p, 1);
     mbar_init(bar_fault, 1);
     mbar_init(bar_merge, 1);
+    mbar_init(bar_q, 1);
     fence_mbar_init();
   }
   // everything above touches no global memory and may overlap the end of
   // the previous kernel of the stream (which may have produced any input)
   grid_dependency_wait();
   grid_launch_dependents();
+  // The HG x QK bf16 rows of Q (contiguous) into the K/V region, which holds
+  // no tile yet, by one bulk copy; they are converted below.
+  constexpr uint32_t kQBytes = HG * L::QK * 2;
+  static_assert(kQBytes <= L::kv_bytes, "Q staging fits the K/V region");
+  if (tid == kQThread) {
+    mbar_arrive_expect_tx(bar_q, kQBytes);
+    bulk_copy_g2s(kv_addr,
+                  static_cast<const __nv_bfloat16*>(a.q) + (static_cast<int64_t>(bs) * a.H + g * HG) * L::QK,
+                  kQBytes, bar_q);
+  }
   const int64_t l_eff = static_cast<int64_t>(__ldg(a.seq_lens + b)) - (a.Sq - 1 - s);
   if (tid < HG) m_ref[tid] = -INFINITY;
-  // slots of the first two tiles (a ring of three tiles, filled two ahead);
-  // started first so that their dependent loads overlap the Q conversion
-  int32_t pro_idx = -1, pro_page = -1, pro_pi = -1;
-  const int pro_t = tid >> 7, pro_r = tid & 127;
-  const int pro_k = (tile_begin + pro_t) * kTileKeys + pro_r;
-  const bool pro_on = tid < kComputeThreads && pro_t < my_tiles;
-  if (pro_on && pro_k < a.K) pro_idx = __ldg(topk_row + pro_k);
-  // Q rows of this head group -> f16, 128-byte-swizzled K-major operand.
-  // Each head is scaled by 2^-e_h (exact) so that its largest magnitude lies
-  // in [2^14, 2^15): every bf16 element then converts to f16 without loss
-  // (apart from elements below 2^-24 of the head's maximum); 2^e_h is folded
-  // into the head's score scale.  TPH threads own a head (its QK/8 16-byte
-  // units interleaved among them) and reduce its maximum with shuffles.
+  // Slots of the first two tiles (a ring of three tiles, filled two ahead):
+  // top-k entry, page-table entry, slot -- one row per thread -- and each
+  // row is started on its way into L2 (its bytes span at most four 128-byte
+  // lines) while Q arrives and is converted.
+  {
+    const int pro_t = tid >> 7, pro_r = tid & 127;
+    const int pro_k = (tile_begin + pro_t) * kTileKeys + pro_r;
+    if (tid < kComputeThreads && pro_t < my_tiles) {
+      const int32_t idx = pro_k < a.K ? __ldg(topk_row + pro_k) : -1;
+      const int32_t pi = slot_page_index(idx, l_eff, a.pt_stride, a.dev_err);
+      const int32_t sl = pi >= 0 ? slot_from_page(__ldg(pt_row + pi), idx, a.num_slots, a.dev_err) : -1;
+      slot_s[pro_t * 128 + pro_r] = sl;
+      if (sl >= 0) {
+        const uint8_t* row = a.pool + static_cast<int64_t>(sl) * L::row_bytes;
+        prefetch_l2_line(row);
+        prefetch_l2_line(row + 128);
+        prefetch_l2_line(row + 256);
+        prefetch_l2_line(row + L::row_bytes - 1);
+      }
+    }
+  }
+  // Q -> f16, 128-byte-swizzled K-major operand.  Each head is scaled by
+  // 2^-e_h (exact) so that its largest magnitude lies in [2^14, 2^15): every
+  // bf16 element then converts to f16 without loss (apart from elements
+  // below 2^-24 of the head's maximum); 2^e_h is folded into the head's
+  // score scale.  TPH threads own a head (its QK/8 16-byte units interleaved
+  // among them, the order rotated by head so that a warp's reads of the
+  // staged rows spread over all banks) and reduce its maximum with shuffles.
   {
     constexpr int UNITS = L::QK / 8;               // 16-byte units of a head
     constexpr int TPH = HG == 64 ? 4 : 8;          // threads per head
@@ -355,21 +388,18 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
     static_assert(UNITS % TPH == 0, "units per thread");
     const int h = tid / TPH, part = tid % TPH;
     const bool active = h < HG;                    // HG = 16 uses 128 threads
-    const uint4* qsrc = reinterpret_cast<const uint4*>(
-        static_cast<const __nv_bfloat16*>(a.q) + (static_cast<int64_t>(bs) * a.H + g * HG) * L::QK);
+    const uint4* qst = reinterpret_cast<const uint4*>(kv_s);
     uint4 qv[UPT];
     uint32_t m = 0;
+    if (active) wait(bar_q, 0);
 #pragma unroll
     for (int j = 0; j < UPT; ++j) {
-      qv[j] = active ? __ldg(qsrc + h * UNITS + part + j * TPH) : make_uint4(0, 0, 0, 0);
+      const int gu = part + ((j + h) % UPT) * TPH;   // 16-byte unit of head h
+      qv[j] = active ? qst[h * UNITS + gu] : make_uint4(0, 0, 0, 0);
       const uint32_t w[4] = {qv[j].x, qv[j].y, qv[j].z, qv[j].w};
 #pragma unroll
       for (int k = 0; k < 4; ++k)
         m = max(m, max((w[k] << 16) & 0x7FFFFFFFu, w[k] & 0x7FFF0000u));   // |bf16| as fp32 bits
-    }
-    if (pro_on) {                                  // second step of the slot lookup
-      pro_pi = slot_page_index(pro_idx, l_eff, a.pt_stride, a.dev_err);
-      if (pro_pi >= 0) pro_page = __ldg(pt_row + pro_pi);
     }
 #pragma unroll
     for (int off = 1; off < TPH; off <<= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
@@ -380,7 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
     if (active) {
 #pragma unroll
       for (int j = 0; j < UPT; ++j) {
-        const int gu = part + j * TPH;             // 16-byte unit of head h
+        const int gu = part + ((j + h) % UPT) * TPH;
         const uint32_t w[4] = {qv[j].x, qv[j].y, qv[j].z, qv[j].w};
         uint32_t o[4];
 #pragma unroll
@@ -394,19 +424,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
       }
     }
   }
-  if (pro_on)
-    slot_s[pro_t * 128 + pro_r] =
-        pro_pi >= 0 ? slot_from_page(pro_page, pro_idx, a.num_slots, a.dev_err) : -1;
   fence_async_smem();
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
-  bool timed_out = false;
-  auto wait = [&](uint32_t bar, uint32_t parity) {
-    if (!mbar_wait_bounded(bar, parity, a.timeout_ns)) timed_out = true;
-  };
-  const uint32_t kv_addr = smem_addr(kv_s);
 
   if (warp >= kComputeWarps) {
     // ==== MMA issue warpgroup: lane 0 of each of its warps is an issuer ====
@@ -536,9 +558,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
       for (int i = 0; i < 16; ++i) {
         const uint8_t* row = a.pool + static_cast<int64_t>(sv[i]) * L::row_bytes;
         if constexpr (FP8)
-          w[i] = sv[i] >= 0 ? __ldg(reinterpret_cast<const uint2*>(row) + word) : make_uint2(0, 0);
+          w[i] = sv[i] >= 0 ? ldg_stream_u64(reinterpret_cast<const uint2*>(row) + word)
+                            : make_uint2(0, 0);
         else
-          w[i] = sv[i] >= 0 ? __ldg(reinterpret_cast<const uint32_t*>(row) + word) : 0u;
+          w[i] = sv[i] >= 0 ? ldg_stream_u32(reinterpret_cast<const uint32_t*>(row) + word) : 0u;
       }                                                    // masked key: zero row
     };
     auto load_extra = [&](uint32_t (&w)[16], const int32_t* slots) {
@@ -548,7 +571,20 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
       for (int i = 0; i < 16; ++i) {
         const uint32_t* row =
             reinterpret_cast<const uint32_t*>(a.pool + static_cast<int64_t>(sv[i]) * L::row_bytes);
-        w[i] = (sv[i] >= 0 && extra_lane) ? __ldg(row + kExtraWord0 + lane) : 0u;
+        w[i] = (sv[i] >= 0 && extra_lane) ? ldg_stream_u32(row + kExtraWord0 + lane) : 0u;
+      }
+    };
+    // Start this warp's 16 rows of a tile (slots at `slots`, just written by
+    // its lanes 0..15) on their way into L2, so that the register gather one
+    // tile later finds them there: lane l asks for line (l & 3) of rows l/4
+    // and 8 + l/4 (a row's bytes span at most four 128-byte lines).
+    auto prefetch_rows = [&](const int32_t* slots) {
+      __syncwarp();
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int32_t sl = slots[warp * 16 + 8 * k + (lane >> 2)];
+        const uint32_t off = (lane & 3) == 3 ? L::row_bytes - 1 : 128u * (lane & 3);
+        if (sl >= 0) prefetch_l2_line(a.pool + static_cast<int64_t>(sl) * L::row_bytes + off);
       }
     };
     auto dequant_latent = [&](const LatWord& w, uint32_t w_ex, int word) -> uint4 {
@@ -722,6 +758,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
         if (resolve_ahead)
           slot_s[((it + 2) % 3) * 128 + warp * 16 + lane] =
               pi_ahead >= 0 ? slot_from_page(page_ahead, idx_ahead, a.num_slots, a.dev_err) : -1;
+        if (it + 2 < my_tiles) prefetch_rows(slot_s + ((it + 2) % 3) * 128);
         fence_async_smem();
         tc_fence_before_sync();
       }
