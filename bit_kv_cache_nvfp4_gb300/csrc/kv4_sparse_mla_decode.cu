@@ -103,6 +103,9 @@ struct Layout {
   // (free after the last QK): half of HG x 512 fp32 fits in Q's 8 or 9 slabs
   // of HG x 128 B.
   static_assert(HG * kLatent * 4 / 2 <= q_bytes, "peer slice must fit in the Q region");
+  // the merge stages the outgoing half (fp32) and then its own merged half
+  // (bf16 or fp32) in the K/V region
+  static_assert(HG * kLatent * 4 / 2 * 2 <= kv_bytes, "merge staging fits the K/V region");
   static_assert(xlse_off % 16 == 0 && xlse_in_off % 16 == 0, "bulk-copy operands are 16-byte aligned");
   static constexpr uint32_t smem_bytes = end + 1024;                  // + alignment slack
   // tensor memory: O^T slabs at columns [0, 4HG); S^T as four partial sums
@@ -775,13 +778,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
     }
 
     // ---- a8: epilogue ----
-    // Normalized partial (o, lse) of this split: into this block's shared
-    // memory when the splits of the unit form a cluster (the K/V tile is
-    // free once the last PV is done), else into the workspace; with one
-    // split, straight to out / lse.
+    // Normalized partial (o, lse) of this split: merged inside the cluster
+    // when the splits of the unit form one (below), else into the workspace;
+    // with one split, straight to out / lse.
     const bool cmerge = a.cluster_merge != 0;
     const bool partial = a.splits > 1;
-    float* o_x = reinterpret_cast<float*>(kv_s);
     float* xlse = reinterpret_cast<float*>(smem + L::xlse_off);
     const int64_t out_head0 = static_cast<int64_t>(bs) * a.H + g * HG;   // first head row
     const int64_t part = static_cast<int64_t>(unit) * a.splits + split;
@@ -801,6 +802,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
     }
 #pragma unroll
     for (int mb = 0; mb < 4; ++mb) {
+      if (cmerge) break;
       const int d = mb * 128 + r_key;
       float o[HPT];
       if (my_tiles > 0) {
@@ -815,8 +817,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
       for (int j = 0; j < HPT; ++j) {
         const int h = h0 + j;
         const float v = o[j] * inv[j];
-        if (cmerge) o_x[h * kLatent + d] = v;
-        else if (partial) a.ws_o[(part * HG + h) * kLatent + d] = v;
+        if (partial) a.ws_o[(part * HG + h) * kLatent + d] = v;
         else if (a.out_f32) static_cast<float*>(a.out)[(out_head0 + h) * kLatent + d] = v;
         else static_cast<__nv_bfloat16*>(a.out)[(out_head0 + h) * kLatent + d] = __float2bfloat16_rn(v);
       }
@@ -830,31 +831,77 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
     }
 
     // ---- a9 inside a cluster of the unit's two splits: block r produces
-    // half of the output elements, out = (w_0 o_0 + w_1 o_1) / (w_0 + w_1)
-    // with w_i = exp(lse_i - max lse), lse = max lse + log(w_0 + w_1).  Each
-    // block pushes the peer's half of its normalized partial (and its lse)
-    // into the peer's shared memory with one bulk copy, then merges its own
-    // half locally.  (The issue warpgroup meets the same two cluster
-    // barriers in its branch.)
+    // output columns [256 r, 256 r + 256) (O slabs 2r, 2r+1), out =
+    // (w_0 o_0 + w_1 o_1) / (w_0 + w_1) with w_i = exp(lse_i - max lse) and
+    // lse = max lse + log(w_0 + w_1), o_i the normalized partials.
+    //   1. each thread normalizes its column of the peer's two slabs (from
+    //      TMEM) into a staging area of this block's K/V region: a
+    //      (slab, column) row of HG fp32 values, its 16-byte units
+    //      XOR-swizzled by the column so that a warp's accesses spread over
+    //      all banks;
+    //   2. after a cluster barrier (the peer's Q region is free once its last
+    //      QK is done), one bulk copy moves the staged half and this block's
+    //      lse into the peer; meanwhile the threads read their own half from
+    //      TMEM;
+    //   3. once the peer's half has arrived, the merged values go through a
+    //      second staging area (head-major rows) so that the output leaves in
+    //      16-byte stores;
+    //   4. a last cluster barrier keeps the staged half alive until the
+    //      peer's copy of it has landed.
+    // (The issue warpgroup meets the same two cluster barriers.)
     if (cmerge) {
-      constexpr int kUnits = HG * kLatent / 4;                // float4 units of o
-      constexpr uint32_t kHalfBytes = kUnits / 2 * 16;
+      constexpr int U = HG / 4;                              // 16-byte units of a row
+      constexpr uint32_t kHalfBytes = HG * kLatent * 4 / 2;
       const uint32_t rank = cluster_ctarank();
       const uint32_t peer = rank ^ 1u;
       float* xlse_in = reinterpret_cast<float*>(smem + L::xlse_in_off);
       float* xw = reinterpret_cast<float*>(smem + L::xw_off);
       float* xinv = reinterpret_cast<float*>(smem + L::xinv_off);
+      uint8_t* stage_out = kv_s;                             // outgoing half, fp32
+      uint8_t* stage_res = kv_s + kHalfBytes;                // this block's merged rows
+      auto row_unit = [&](int s2, int u) -> uint32_t {       // byte offset of a staged unit
+        return static_cast<uint32_t>(((s2 * 128 + r_key) * U + (u ^ (r_key % U))) * 16);
+      };
+      float inv[HPT];
+      lds_vec<HPT>(lsum + HG + h0, inv);
+#pragma unroll
+      for (int s2 = 0; s2 < 2; ++s2) {
+        float v[HPT];
+        if (my_tiles > 0) {
+          tmem_load_cols<HPT>(lane_base + L::col_o + (2 * peer + s2) * HG + h0, v);
+        } else {
+#pragma unroll
+          for (int j = 0; j < HPT; ++j) v[j] = 0.0f;
+        }
+#pragma unroll
+        for (int k = 0; k < HPT / 4; ++k)
+          *reinterpret_cast<float4*>(stage_out + row_unit(s2, h0 / 4 + k)) =
+              make_float4(v[4 * k] * inv[4 * k], v[4 * k + 1] * inv[4 * k + 1],
+                          v[4 * k + 2] * inv[4 * k + 2], v[4 * k + 3] * inv[4 * k + 3]);
+      }
       if (tid == 0) mbar_arrive_expect_tx(bar_merge, kHalfBytes + HG * 4);
-      fence_async_smem();                      // o_x / xlse are read by the async proxy
-      cluster_sync();                          // both partials written, both barriers armed
+      fence_async_smem();                      // the staged half is read by the async proxy
+      cluster_sync();                          // both halves staged, both merge barriers armed
       if (tid == 0) {
         const uint32_t peer_bar = cluster_map(bar_merge, peer);
-        bulk_copy_to_cluster(cluster_map(smem_addr(q_s), peer), smem_addr(o_x) + peer * kHalfBytes,
-                             kHalfBytes, peer_bar);
+        bulk_copy_to_cluster(cluster_map(smem_addr(q_s), peer), smem_addr(stage_out), kHalfBytes,
+                             peer_bar);
         bulk_copy_to_cluster(cluster_map(smem_addr(xlse_in), peer), smem_addr(xlse), HG * 4,
                              peer_bar);
       }
-      wait(bar_merge, 0);
+      float mine[2][HPT];
+#pragma unroll
+      for (int s2 = 0; s2 < 2; ++s2) {
+        if (my_tiles > 0) {
+          tmem_load_cols<HPT>(lane_base + L::col_o + (2 * rank + s2) * HG + h0, mine[s2]);
+        } else {
+#pragma unroll
+          for (int j = 0; j < HPT; ++j) mine[s2][j] = 0.0f;
+        }
+#pragma unroll
+        for (int j = 0; j < HPT; ++j) mine[s2][j] *= inv[j];
+      }
+      wait(bar_merge, 0);                      // the peer's half and lse are here
       if (tid < HG) {
         const float l0 = rank == 0 ? xlse[tid] : xlse_in[tid];
         const float l1 = rank == 0 ? xlse_in[tid] : xlse[tid];
@@ -868,24 +915,46 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
         if (rank == 0) a.lse[out_head0 + tid] = wsum > 0.0f ? m + logf(wsum) : -INFINITY;
       }
       named_sync(kBarCompute, kComputeThreads);
-      const float4* mine = reinterpret_cast<const float4*>(o_x) + rank * (kUnits / 2);
-      const float4* theirs = reinterpret_cast<const float4*>(q_s);
-      const float* w_mine = xw + rank * HG;
-      const float* w_theirs = xw + peer * HG;
-      for (int i = tid; i < kUnits / 2; i += kComputeThreads) {
-        const int u = static_cast<int>(rank) * (kUnits / 2) + i;
-        const int h = u / (kLatent / 4);
-        const float4 va = mine[i], vb = theirs[i];
-        const float wa = w_mine[h], wb = w_theirs[h];
-        // summed in split order, as the merge kernel does
-        const float4 v0 = rank == 0 ? va : vb, v1 = rank == 0 ? vb : va;
-        const float w0 = rank == 0 ? wa : wb, w1 = rank == 0 ? wb : wa;
-        const float inv = xinv[h];
-        const float4 m4 = make_float4((w0 * v0.x + w1 * v1.x) * inv, (w0 * v0.y + w1 * v1.y) * inv,
-                                      (w0 * v0.z + w1 * v1.z) * inv, (w0 * v0.w + w1 * v1.w) * inv);
-        store_out4(a.out, (out_head0 + h) * kLatent + (u % (kLatent / 4)) * 4, m4, a.out_f32 != 0);
-      }
-      cluster_sync();                          // the peer's copy out of this block is done
+      // merged rows -> stage_res (head-major, 256 columns; lanes store
+      // consecutive columns of one head: no bank conflicts), then 16-byte
+      // units to out[head, 256 rank + ...]
+      auto merge_and_store = [&](auto* res) {
+        using T = std::remove_pointer_t<decltype(res)>;
+        float w0[HPT], w1[HPT], xi[HPT];
+        lds_vec<HPT>(xw + h0, w0);
+        lds_vec<HPT>(xw + HG + h0, w1);
+        lds_vec<HPT>(xinv + h0, xi);
+#pragma unroll
+        for (int s2 = 0; s2 < 2; ++s2) {
+          const int c = s2 * 128 + r_key;                  // column within this block's half
+#pragma unroll
+          for (int k = 0; k < HPT / 4; ++k) {
+            const float4 t = *reinterpret_cast<const float4*>(q_s + row_unit(s2, h0 / 4 + k));
+            const float theirs[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int j = 4 * k + i;
+              // summed in split order, as the merge kernel does
+              const float v0 = rank == 0 ? mine[s2][j] : theirs[i];
+              const float v1 = rank == 0 ? theirs[i] : mine[s2][j];
+              const float v = (w0[j] * v0 + w1[j] * v1) * xi[j];
+              if constexpr (std::is_same_v<T, float>) res[(h0 + j) * 256 + c] = v;
+              else res[(h0 + j) * 256 + c] = __float2bfloat16_rn(v);
+            }
+          }
+        }
+        named_sync(kBarCompute, kComputeThreads);
+        constexpr int kUnitsPerRow = 256 * static_cast<int>(sizeof(T)) / 16;
+        const uint4* src = reinterpret_cast<const uint4*>(res);
+        for (int i = tid; i < HG * kUnitsPerRow; i += kComputeThreads) {
+          const int h = i / kUnitsPerRow, u = i % kUnitsPerRow;
+          T* dst = static_cast<T*>(a.out) + (out_head0 + h) * kLatent + 256 * static_cast<int64_t>(rank);
+          reinterpret_cast<uint4*>(dst)[u] = src[i];
+        }
+      };
+      if (a.out_f32) merge_and_store(reinterpret_cast<float*>(stage_res));
+      else merge_and_store(reinterpret_cast<__nv_bfloat16*>(stage_res));
+      cluster_sync();                          // the peer's copy of the staged half has landed
     }
   }  // compute warpgroups
   if (timed_out) flag_error(a.dev_err, kDevTimeout);

@@ -137,7 +137,8 @@ kv4_status kv4_decode_plan(int B, int Sq, int H, int K, int force_splits,
  *   H              16, 32, 64, or a multiple of 64 up to 256
  *   sm_scale       softmax scale applied to q.k
  *   out_dev        bf16 [B, Sq, H, 512]: softmax-weighted sum of the latent
- *                  part of the selected rows (0 if no key is valid)
+ *                  part of the selected rows (0 if no key is valid),
+ *                  16-byte aligned
  *   lse_dev        fp32 [B, Sq, H]: natural-log log-sum-exp of the scaled
  *                  scores (-inf if no key is valid)
  *   workspace_dev  device scratch of at least the bytes kv4_decode_plan

@@ -78,3 +78,13 @@ def test_binding_fails_loudly_without_cuda_tensors():
         kv.quantize_write(torch.zeros(1, 512, dtype=torch.bfloat16),
                           torch.zeros(1, 64, dtype=torch.bfloat16),
                           torch.zeros(1, dtype=torch.int64), torch.zeros(64, 352, dtype=torch.uint8))
+
+
+def test_binding_constants_match_header():
+    """The binding's layout constants are the header's enum values."""
+    import bit_kv_cache_nvfp4_gb300 as kv
+    text = re.sub(r"/\*.*?\*/", "", open(os.path.join(ROOT, "include", "kv4mla.h")).read(), flags=re.S)
+    values = {k: int(v) for k, v in re.findall(r"\bKV4_([A-Z0-9_]+)\s*=\s*(\d+)", text)}
+    for name in ("ROW_BYTES", "LATENT", "ROPE", "QK_DIM", "PAGE", "TILE_KEYS", "ROW_BYTES_LATENT",
+                 "ROW_BYTES_FP8"):
+        assert getattr(kv, name) == values[name], name

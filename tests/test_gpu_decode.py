@@ -152,10 +152,10 @@ def test_heads_and_ragged_k(H, K):
     assert_close(out, lse, out_ref, lse_ref, f"H={H} K={K}")
 
 
-# up to 8 splits merge inside a thread-block cluster (distributed shared
+# two splits merge inside a thread-block cluster (distributed shared
 # memory); more go through the workspace and the merge kernel
-@pytest.mark.parametrize("K,S", [(1000, 1), (1000, 2), (1000, 3), (1000, 5), (1000, 8),
-                                 (2000, 9), (2000, 16)])
+@pytest.mark.parametrize("K,S", [(1000, 1), (1000, 2), (1000, 3), (1000, 4), (1000, 5),
+                                 (1000, 8), (2000, 9), (2000, 16)])
 def test_forced_splits(K, S):
     need_gpu()
     p = small_problem(L=3000, B=2, Sq=1, H=64, K=K, seed=77)
@@ -259,29 +259,34 @@ def test_invalid_arguments_raise():
     assert e.value.status == 1
 
 
-def test_determinism_and_graph_replay():
+@pytest.mark.parametrize("S", [0, 2])
+def test_determinism_and_graph_replay(S):
+    """Planned splits (merge kernel) and 2 forced splits (merged inside a
+    thread-block cluster)."""
     need_gpu()
     w = workload("decode")
     pool = gpu_pool(w)
     q, pt, topk, lens = device_inputs(w)
     m = kv()
-    out_a, lse_a = m.sparse_mla_decode(q, pool, pt, topk, lens, w.sm_scale)
-    out_b, lse_b = m.sparse_mla_decode(q, pool, pt, topk, lens, w.sm_scale)
+    out_a, lse_a = m.sparse_mla_decode(q, pool, pt, topk, lens, w.sm_scale, force_splits=S)
+    out_b, lse_b = m.sparse_mla_decode(q, pool, pt, topk, lens, w.sm_scale, force_splits=S)
     torch.cuda.synchronize()
     assert torch.equal(out_a.view(torch.int16), out_b.view(torch.int16))
     assert torch.equal(lse_a, lse_b)
     out = torch.empty_like(out_a)
     lse = torch.empty_like(lse_a)
-    splits, ws_bytes = m.decode_plan(w.B, w.Sq, w.H, w.K)
+    splits, ws_bytes = m.decode_plan(w.B, w.Sq, w.H, w.K, S)
     ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device="cuda")
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(s):
-        m.sparse_mla_decode(q, pool, pt, topk, lens, w.sm_scale, out=out, lse=lse, workspace=ws)
+        m.sparse_mla_decode(q, pool, pt, topk, lens, w.sm_scale, out=out, lse=lse, workspace=ws,
+                            force_splits=S)
     torch.cuda.current_stream().wait_stream(s)
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
-        m.sparse_mla_decode(q, pool, pt, topk, lens, w.sm_scale, out=out, lse=lse, workspace=ws)
+        m.sparse_mla_decode(q, pool, pt, topk, lens, w.sm_scale, out=out, lse=lse, workspace=ws,
+                            force_splits=S)
     for _ in range(3):
         out.zero_()
         g.replay()
