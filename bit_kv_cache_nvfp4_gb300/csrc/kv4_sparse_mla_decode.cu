@@ -354,6 +354,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
                   static_cast<const __nv_bfloat16*>(a.q) + (static_cast<int64_t>(bs) * a.H + g * HG) * L::QK,
                   kQBytes, bar_q);
   }
+  // The request's page-table row into L2 (up to 32 KB, one 128-byte line
+  // per thread), so that the slot lookups below and two tiles ahead find
+  // their second dependent load there.
+  {
+    const int64_t pt_lines = (a.pt_stride * 4 + 127) / 128;
+    if (tid < pt_lines) prefetch_l2_line(reinterpret_cast<const uint8_t*>(pt_row) + tid * 128);
+  }
   const int64_t l_eff = static_cast<int64_t>(__ldg(a.seq_lens + b)) - (a.Sq - 1 - s);
   if (tid < HG) m_ref[tid] = -INFINITY;
   // Slots of the first two tiles (a ring of three tiles, filled two ahead):
