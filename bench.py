@@ -340,9 +340,11 @@ def run_gpu(args):
     stream = torch.cuda.current_stream(dev)
 
     def step():
-        kv.quantize_write(new_lat, new_rope, new_slots, pool, err)
-        kv.sparse_mla_decode(q, pool, pt, topk, lens, w.sm_scale, out=out, lse=lse, workspace=ws,
-                             dev_err=err, force_splits=args.splits)
+        # the cache write of the step's new tokens, then the decode (one call;
+        # the decode's prologue overlaps the write)
+        kv.quantize_write_and_decode(new_lat, new_rope, new_slots, pool, q, pt, topk, lens,
+                                     w.sm_scale, out=out, lse=lse, workspace=ws, dev_err=err,
+                                     force_splits=args.splits)
 
     valid = valid_key_count(w)
     kv_bytes = valid * 352
@@ -652,8 +654,8 @@ def run_e2e(kv, w, dev, pool, pt, lens, flush, args):
         nl_d.copy_(nl_h, non_blocking=True)
         nr_d.copy_(nr_h, non_blocking=True)
         ns_d.copy_(ns_h, non_blocking=True)
-        kv.quantize_write(nl_d, nr_d, ns_d, pool)
-        out, lse = kv.sparse_mla_decode(q_d, pool, pt, topk_d, lens, w.sm_scale)
+        out, lse = kv.quantize_write_and_decode(nl_d, nr_d, ns_d, pool, q_d, pt, topk_d, lens,
+                                                w.sm_scale)
         out_h.copy_(out, non_blocking=True)
         lse_h.copy_(lse, non_blocking=True)
 

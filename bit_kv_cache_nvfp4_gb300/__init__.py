@@ -24,7 +24,7 @@ __all__ = [
     "Kv4Error", "library_path", "load_library", "quantize_write", "decode_plan",
     "sparse_mla_decode", "debug_gather_dequant", "set_wait_limit", "set_timing_event",
     "quantize_write_mse", "quantize_write_fp8", "decode_plan_fp8", "sparse_mla_decode_fp8",
-    "fp8_scratch", "scratch_index", "ROW_BYTES_FP8", "quantize_write_latent", "decode_plan_latent", "sparse_mla_decode_latent",
+    "fp8_scratch", "scratch_index", "ROW_BYTES_FP8", "quantize_write_and_decode", "quantize_write_latent", "decode_plan_latent", "sparse_mla_decode_latent",
     "debug_gather_dequant_latent", "sparse_mla_decode_partial", "dcp_mask_topk",
     "merge_partials", "gather_partials", "dcp_sparse_mla_decode", "ROW_BYTES", "ROW_BYTES_LATENT", "LATENT", "ROPE", "QK_DIM", "PAGE", "DEV_BAD_SLOT", "DEV_BAD_PAGE",
     "DEV_TIMEOUT",
@@ -101,6 +101,10 @@ def load_library():
         lib.kv4_sparse_mla_decode_latent.restype = i32
         lib.kv4_debug_gather_dequant_latent.argtypes = lib.kv4_debug_gather_dequant.argtypes
         lib.kv4_debug_gather_dequant_latent.restype = i32
+        lib.kv4_quantize_write_and_decode.argtypes = (lib.kv4_quantize_write.argtypes[:8] +
+                                                      lib.kv4_sparse_mla_decode.argtypes[:1] +
+                                                      lib.kv4_sparse_mla_decode.argtypes[3:])
+        lib.kv4_quantize_write_and_decode.restype = i32
         lib.kv4_set_wait_limit.argtypes = [i64, i32]
         lib.kv4_set_wait_limit.restype = i32
         lib.kv4_set_timing_event.argtypes = [P]
@@ -413,6 +417,55 @@ def _decode(fmt, q, pool, page_table, topk_idx, seq_lens, sm_scale, out, lse, wo
         _dev(page_table, "page_table", torch.int32), page_table.shape[1], PAGE,
         _dev(topk_idx, "topk_idx", torch.int32), K, _dev(seq_lens, "seq_lens", torch.int32),
         B, Sq, H, float(sm_scale), _dev(out, "out", out_dtype),
+        _dev(lse, "lse", torch.float32), ws_ptr, ws_len, force_splits, _err_ptr(dev_err),
+        _stream(dev)))
+    return out, lse
+
+
+def quantize_write_and_decode(latent: torch.Tensor, rope: torch.Tensor,
+                              slot_mapping: torch.Tensor, pool: torch.Tensor, q: torch.Tensor,
+                              page_table: torch.Tensor, topk_idx: torch.Tensor,
+                              seq_lens: torch.Tensor, sm_scale: float,
+                              out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
+                              workspace: torch.Tensor | None = None, force_splits: int = 0,
+                              dev_err: torch.Tensor | None = None):
+    """One decode step (kv4_quantize_write_and_decode): quantize_write of the
+    step's new tokens, then sparse_mla_decode, with the same results; the
+    decode's reads of q, page_table, topk_idx and seq_lens overlap the write."""
+    lib = load_library()
+    n = slot_mapping.shape[0]
+    if latent.dim() != 2 or rope.dim() != 2 or latent.shape[0] != n or rope.shape[0] != n:
+        raise ValueError("latent [N,512], rope [N,64] and slot_mapping [N] must agree")
+    if latent.stride(1) != 1 or rope.stride(1) != 1:
+        raise ValueError("latent and rope rows must be contiguous")
+    B, Sq, H, D = q.shape
+    if D != QK_DIM:
+        raise ValueError(f"q must be [B, Sq, H, {QK_DIM}]")
+    if pool.dim() != 2 or pool.shape[1] != ROW_BYTES:
+        raise ValueError(f"pool must be [num_slots, {ROW_BYTES}]")
+    K = topk_idx.shape[2]
+    if tuple(topk_idx.shape[:2]) != (B, Sq) or seq_lens.shape[0] != B or page_table.shape[0] != B:
+        raise ValueError("topk_idx [B,Sq,K], seq_lens [B] and page_table [B,*] must agree with q")
+    dev = q.device
+    if out is None:
+        out = torch.empty((B, Sq, H, LATENT), dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((B, Sq, H), dtype=torch.float32, device=dev)
+    splits, ws_bytes = decode_plan(B, Sq, H, K, force_splits)
+    if workspace is None:
+        workspace = _workspace(dev, ws_bytes)
+    ws_ptr = None if workspace is None else _dev(workspace, "workspace", workspace.dtype)
+    ws_len = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    fn = "kv4_quantize_write_and_decode"
+    _check(fn, lib.kv4_quantize_write_and_decode(
+        _dev(latent, "latent", torch.bfloat16, False), latent.stride(0),
+        _dev(rope, "rope", torch.bfloat16, False), rope.stride(0),
+        _dev(slot_mapping, "slot_mapping", torch.int64), n,
+        _dev(pool, "pool", torch.uint8), pool.shape[0],
+        _dev(q, "q", torch.bfloat16),
+        _dev(page_table, "page_table", torch.int32), page_table.shape[1], PAGE,
+        _dev(topk_idx, "topk_idx", torch.int32), K, _dev(seq_lens, "seq_lens", torch.int32),
+        B, Sq, H, float(sm_scale), _dev(out, "out", torch.bfloat16),
         _dev(lse, "lse", torch.float32), ws_ptr, ws_len, force_splits, _err_ptr(dev_err),
         _stream(dev)))
     return out, lse

@@ -156,7 +156,8 @@ kv4_status decode_impl(const void* q_dev, const uint8_t* pool_dev, int64_t num_s
                        const int32_t* topk_idx_dev, int K, const int32_t* seq_lens_dev, int B,
                        int Sq, int H, float sm_scale, void* out_dev, float* lse_dev,
                        void* workspace_dev, size_t workspace_bytes, int force_splits,
-                       int32_t* dev_err, kv4_stream_t stream, int fmt, bool out_f32 = false) {
+                       int32_t* dev_err, kv4_stream_t stream, int fmt, bool out_f32 = false,
+                       bool early_inputs = false, bool launch = true) {
   const kv4_status shape = check_decode_shape(B, Sq, H, K);
   if (shape != KV4_OK) return shape;
   if (page_size != KV4_PAGE) return KV4_ERR_UNSUPPORTED;
@@ -201,6 +202,7 @@ kv4_status decode_impl(const void* q_dev, const uint8_t* pool_dev, int64_t num_s
   a.cluster_merge = p.cluster_merge ? 1 : 0;
   a.fmt = fmt;
   a.out_f32 = out_f32 ? 1 : 0;
+  a.early_inputs = early_inputs ? 1 : 0;
   if (p.splits > 1 && !p.cluster_merge) {
     a.ws_o = static_cast<float*>(workspace_dev);
     a.ws_lse = a.ws_o + static_cast<size_t>(p.units) * p.splits * p.HG * KV4_LATENT;
@@ -209,6 +211,7 @@ kv4_status decode_impl(const void* q_dev, const uint8_t* pool_dev, int64_t num_s
   a.timeout_ns = static_cast<uint64_t>(g_timeout_ns.load());
   a.fault_site = g_fault_site.load();
   a.after_decode = static_cast<cudaEvent_t>(g_timing_event.load());
+  if (!launch) return KV4_OK;                  // arguments checked only
   return kv4::launch_decode(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
              ? KV4_OK
              : KV4_ERR_LAUNCH;
@@ -264,6 +267,29 @@ kv4_status kv4_sparse_mla_decode(const void* q_dev, const uint8_t* pool_dev, int
                      topk_idx_dev, K, seq_lens_dev, B, Sq, H, sm_scale, out_dev, lse_dev,
                      workspace_dev, workspace_bytes, force_splits, dev_err, stream,
                      kv4::kFmtNvfp4);
+}
+
+kv4_status kv4_quantize_write_and_decode(
+    const void* latent_dev, int64_t latent_row_stride, const void* rope_dev,
+    int64_t rope_row_stride, const int64_t* slot_mapping_dev, int64_t n_tokens, uint8_t* pool_dev,
+    int64_t num_slots, const void* q_dev, const int32_t* page_table_dev, int64_t pt_stride,
+    int page_size, const int32_t* topk_idx_dev, int K, const int32_t* seq_lens_dev, int B, int Sq,
+    int H, float sm_scale, void* out_dev, float* lse_dev, void* workspace_dev,
+    size_t workspace_bytes, int force_splits, int32_t* dev_err, kv4_stream_t stream) {
+  // the decode's arguments are checked before anything is launched
+  const kv4_status d = decode_impl(q_dev, pool_dev, num_slots, page_table_dev, pt_stride,
+                                   page_size, topk_idx_dev, K, seq_lens_dev, B, Sq, H, sm_scale,
+                                   out_dev, lse_dev, workspace_dev, workspace_bytes, force_splits,
+                                   dev_err, stream, kv4::kFmtNvfp4, false, false, false);
+  if (d != KV4_OK) return d;
+  const kv4_status w = quantize_impl(latent_dev, latent_row_stride, rope_dev, rope_row_stride,
+                                     slot_mapping_dev, n_tokens, pool_dev, num_slots, dev_err,
+                                     stream, true);
+  if (w != KV4_OK) return w;
+  return decode_impl(q_dev, pool_dev, num_slots, page_table_dev, pt_stride, page_size,
+                     topk_idx_dev, K, seq_lens_dev, B, Sq, H, sm_scale, out_dev, lse_dev,
+                     workspace_dev, workspace_bytes, force_splits, dev_err, stream,
+                     kv4::kFmtNvfp4, false, n_tokens > 0);
 }
 
 kv4_status kv4_debug_gather_dequant(const uint8_t* pool_dev, int64_t num_slots,

@@ -56,6 +56,8 @@ struct DecodeArgs {
   int cluster_merge;           // splits > 1 merged inside a cluster of `splits` blocks
   int fmt;                     // row format: kFmtNvfp4, kFmtNvfp4Latent or kFmtFp8
   int out_f32;                 // 1: out is fp32 (a context-parallel rank's partial), else bf16
+  int early_inputs;            // 1: q, page table, top-k and lengths may be read before the
+                               //    previous kernel (this call's cache write) has finished
 };
 
 struct GatherArgs {

@@ -340,9 +340,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
     mbar_init(bar_q, 1);
     fence_mbar_init();
   }
-  // everything above touches no global memory and may overlap the end of
-  // the previous kernel of the stream (which may have produced any input)
-  grid_dependency_wait();
+  // Everything above touches no global memory and may overlap the end of
+  // the previous kernel of the stream, which may have produced any input.
+  // When that kernel is known to be this call's own cache write (which
+  // writes only the pool), the prologue below -- Q, top-k, page-table and
+  // length reads, L2 prefetches -- overlaps it too, and each compute thread
+  // waits just before its first read of pool rows.
+  if (!a.early_inputs) grid_dependency_wait();
   grid_launch_dependents();
   // The HG x QK bf16 rows of Q (contiguous) into the K/V region, which holds
   // no tile yet, by one bulk copy; they are converted below.
@@ -605,6 +609,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
         return dequant_latent_word(w, w_ex, word);
       }
     };
+    if (a.early_inputs) grid_dependency_wait();   // the pool rows are written
     if (my_tiles > 0) {
       load_latent(wa, slot_s, word_a);
       load_latent(wb, slot_s, word_b);

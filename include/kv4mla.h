@@ -160,6 +160,32 @@ kv4_status kv4_sparse_mla_decode(const void* q_dev, const uint8_t* pool_dev,
                                  kv4_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * kv4_quantize_write_and_decode -- one decode step: kv4_quantize_write of the
+ * step's new tokens, then kv4_sparse_mla_decode over the pool, on `stream`.
+ * Source: the write (README "4-bit KV cache", kv4mla bullet) followed by the
+ * decode it feeds; the two are the step's hot path.
+ * Arguments: those of kv4_quantize_write (latent_dev .. num_slots) followed
+ * by those of kv4_sparse_mla_decode (q_dev .. stream), with the same
+ * meanings, layouts and ownership; pool_dev and num_slots are shared.
+ * Results are bit-identical to the two calls made one after the other.  The
+ * difference: the decode kernel starts while the write is still running and
+ * reads q, the page table, the top-k list and seq_lens at once; only its
+ * reads of pool rows wait for the write.  So q_dev, page_table_dev,
+ * topk_idx_dev and seq_lens_dev must not overlap the pool or the write's
+ * inputs (they are otherwise as in kv4_sparse_mla_decode: ready in stream
+ * order).  Every argument of both parts is checked before anything is
+ * launched; errors are those of the two calls.
+ * ------------------------------------------------------------------------- */
+kv4_status kv4_quantize_write_and_decode(
+    const void* latent_dev, int64_t latent_row_stride, const void* rope_dev,
+    int64_t rope_row_stride, const int64_t* slot_mapping_dev, int64_t n_tokens,
+    uint8_t* pool_dev, int64_t num_slots, const void* q_dev, const int32_t* page_table_dev,
+    int64_t pt_stride, int page_size, const int32_t* topk_idx_dev, int K,
+    const int32_t* seq_lens_dev, int B, int Sq, int H, float sm_scale, void* out_dev,
+    float* lse_dev, void* workspace_dev, size_t workspace_bytes, int force_splits,
+    int32_t* dev_err, kv4_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * kv4_debug_gather_dequant -- the decode's own index resolution and
  * dequantization, written out: rows_dev f16 [B, Sq, K, 576] receives the
  * dequantized selected rows, i.e. the tensor-core operand values (every

@@ -309,3 +309,41 @@ def test_bounded_wait_reports_timeout():
     assert_close(out, lse, out_ref, lse_ref, "after timeout")
     out, lse, out_ref, lse_ref, st = run_both(p)
     assert_close(out, lse, out_ref, lse_ref, "after reset")
+
+
+@pytest.mark.parametrize("S", [0, 2])
+def test_write_and_decode_matches_two_calls(S):
+    """kv4_quantize_write_and_decode, whose decode reads q, the page table,
+    the top-k list and the lengths while the write is still running, gives
+    the pool bytes and the results of quantize_write then sparse_mla_decode.
+    The new tokens' slots are zeroed first and every query selects its
+    newest position, so a decode that read a row before the write landed
+    would differ."""
+    need_gpu()
+    w = workload("decode")
+    base = gpu_pool(w)
+    q, pt, topk, lens = device_inputs(w)
+    topk = topk.clone()
+    topk[:, :, 0] = (lens - 1).view(-1, 1).to(torch.int32)      # the newest token
+    m = kv()
+    lat, rope, slots = wl.newest_tokens(w, device="cuda")
+    results = []
+    for fused in (False, True):
+        pool = base.clone()
+        pool[slots] = 0
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        if fused:
+            out, lse = m.quantize_write_and_decode(lat, rope, slots, pool, q, pt, topk, lens,
+                                                   w.sm_scale, force_splits=S, dev_err=err)
+        else:
+            m.quantize_write(lat, rope, slots, pool, err)
+            out, lse = m.sparse_mla_decode(q, pool, pt, topk, lens, w.sm_scale, force_splits=S,
+                                           dev_err=err)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        results.append((pool, out, lse))
+    (pa, oa, la), (pb, ob, lb) = results
+    assert torch.equal(pa, pb)
+    assert torch.equal(pa, base)                    # the write restored the zeroed rows
+    assert torch.equal(oa.view(torch.int16), ob.view(torch.int16))
+    assert torch.equal(la, lb)
