@@ -781,18 +781,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
       named_sync(kBarCompute, kComputeThreads);
       if (tid == 0) mbar_arrive(bar_p);
     }
-    // the last PV must be complete before O is read or TMEM is freed
-    if (my_tiles > 0) {
-      const uint32_t last = (my_tiles - 1) & 1;
-      for (int p = 0; p < 4; ++p) wait(bar_pv0 + 8 * p, last);
-      __syncwarp();
-      tc_fence_after_sync();
-    }
-
     // ---- a8: epilogue ----
     // Normalized partial (o, lse) of this split: merged inside the cluster
     // when the splits of the unit form one (below), else into the workspace;
-    // with one split, straight to out / lse.
+    // with one split, straight to out / lse.  l and lse need only the softmax
+    // state, so they are computed while the last PV still runs.
     const bool cmerge = a.cluster_merge != 0;
     const bool partial = a.splits > 1;
     float* xlse = reinterpret_cast<float*>(smem + L::xlse_off);
@@ -812,6 +805,20 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
       else if (partial) a.ws_lse[part * HG + h] = lse;
       else a.lse[out_head0 + h] = lse;
     }
+    if (cmerge) {
+      // first half of the merge's first cluster barrier: this block's Q region
+      // is free (its last QK is done) and its merge barrier is armed
+      if (tid == 0) mbar_arrive_expect_tx(bar_merge, HG * kLatent * 4 / 2 + HG * 4);
+      cluster_arrive();
+    }
+    // the last PV must be complete before O is read or TMEM is freed
+    if (my_tiles > 0) {
+      const uint32_t last = (my_tiles - 1) & 1;
+      for (int p = 0; p < 4; ++p) wait(bar_pv0 + 8 * p, last);
+      __syncwarp();
+      tc_fence_after_sync();
+    }
+
 #pragma unroll
     for (int mb = 0; mb < 4; ++mb) {
       if (cmerge) break;
@@ -852,9 +859,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
     //      XOR-swizzled by the column so that a warp's accesses spread over
     //      all banks;
     //   2. after a cluster barrier (the peer's Q region is free once its last
-    //      QK is done), one bulk copy moves the staged half and this block's
-    //      lse into the peer; meanwhile the threads read their own half from
-    //      TMEM;
+    //      QK is done; each block arrived on it before waiting for its last
+    //      PV), one bulk copy moves the staged half and this block's lse into
+    //      the peer; meanwhile the threads read their own half from TMEM;
     //   3. once the peer's half has arrived, the merged values go through a
     //      second staging area (head-major rows) so that the output leaves in
     //      16-byte stores;
@@ -891,9 +898,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
               make_float4(v[4 * k] * inv[4 * k], v[4 * k + 1] * inv[4 * k + 1],
                           v[4 * k + 2] * inv[4 * k + 2], v[4 * k + 3] * inv[4 * k + 3]);
       }
-      if (tid == 0) mbar_arrive_expect_tx(bar_merge, kHalfBytes + HG * 4);
       fence_async_smem();                      // the staged half is read by the async proxy
-      cluster_sync();                          // both halves staged, both merge barriers armed
+      cluster_wait();                          // the peer's Q region is free, its barrier armed
       if (tid == 0) {
         const uint32_t peer_bar = cluster_map(bar_merge, peer);
         bulk_copy_to_cluster(cluster_map(smem_addr(q_s), peer), smem_addr(stage_out), kHalfBytes,
