@@ -899,13 +899,20 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
                           v[4 * k + 2] * inv[4 * k + 2], v[4 * k + 3] * inv[4 * k + 3]);
       }
       fence_async_smem();                      // the staged half is read by the async proxy
+      named_sync(kBarCompute, kComputeThreads);  // every thread's part is staged
       cluster_wait();                          // the peer's Q region is free, its barrier armed
-      if (tid == 0) {
+      // the staged half leaves in kMergeCopies bulk copies issued by as many
+      // threads (lane 0 of consecutive warps), so that they run side by side
+      constexpr int kMergeCopies = 8;
+      static_assert(kHalfBytes % (kMergeCopies * 16) == 0, "copy chunks of whole 16-byte units");
+      constexpr uint32_t kChunk = kHalfBytes / kMergeCopies;
+      if (lane == 0 && warp < kMergeCopies) {
         const uint32_t peer_bar = cluster_map(bar_merge, peer);
-        bulk_copy_to_cluster(cluster_map(smem_addr(q_s), peer), smem_addr(stage_out), kHalfBytes,
-                             peer_bar);
-        bulk_copy_to_cluster(cluster_map(smem_addr(xlse_in), peer), smem_addr(xlse), HG * 4,
-                             peer_bar);
+        bulk_copy_to_cluster(cluster_map(smem_addr(q_s) + warp * kChunk, peer),
+                             smem_addr(stage_out) + warp * kChunk, kChunk, peer_bar);
+        if (warp == 0)
+          bulk_copy_to_cluster(cluster_map(smem_addr(xlse_in), peer), smem_addr(xlse), HG * 4,
+                               peer_bar);
       }
       float mine[2][HPT];
 #pragma unroll
