@@ -88,3 +88,26 @@ def test_binding_constants_match_header():
     for name in ("ROW_BYTES", "LATENT", "ROPE", "QK_DIM", "PAGE", "TILE_KEYS", "ROW_BYTES_LATENT",
                  "ROW_BYTES_FP8"):
         assert getattr(kv, name) == values[name], name
+
+
+def test_write_and_decode_checks_both_parts_first(lib):
+    """kv4_quantize_write_and_decode refuses a bad decode argument before it
+    launches the write, and a bad write argument before anything else."""
+    P, i64, i32, f = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float
+    fn = lib.kv4_quantize_write_and_decode
+    fn.argtypes = [P, i64, P, i64, P, i64, P, i64,
+                   P, P, i64, i32, P, i32, P, i32, i32, i32, f, P, P, P, ctypes.c_size_t, i32, P,
+                   P]
+    fn.restype = i32
+    buf = ctypes.create_string_buffer(1 << 12)
+    ptr = ctypes.cast(buf, P)
+    # a page size other than 64 (decode) -> unsupported, with a valid-looking write
+    assert fn(ptr, 512, ptr, 64, ptr, 4, ptr, 64,
+              ptr, ptr, 1, 32, ptr, 8, ptr, 1, 1, 16, 0.1, ptr, ptr, None, 0, 0, None, None) == 2
+    # an unsupported head count (decode) -> unsupported
+    assert fn(ptr, 512, ptr, 64, ptr, 4, ptr, 64,
+              ptr, ptr, 1, 64, ptr, 8, ptr, 1, 1, 48, 0.1, ptr, ptr, None, 0, 0, None, None) == 2
+    # null decode outputs -> invalid argument
+    assert fn(ptr, 512, ptr, 64, ptr, 4, ptr, 64,
+              ptr, ptr, 1, 64, ptr, 8, ptr, 1, 1, 16, 0.1, None, None, None, 0, 0, None,
+              None) == 1
