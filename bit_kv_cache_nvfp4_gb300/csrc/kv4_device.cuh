@@ -194,20 +194,6 @@ __device__ __forceinline__ uint32_t cluster_map(uint32_t addr, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
   return r;
 }
-// Loads from another block's shared memory; ordered after its writes by a
-// cluster_sync() in between (which is also the compiler barrier).
-__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr));
-  return v;
-}
-__device__ __forceinline__ float4 ld_cluster_v4(uint32_t addr) {
-  float4 v;
-  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(addr));
-  return v;
-}
 
 // Arrive on a local mbarrier and announce `bytes` of asynchronous copies
 // that will complete on it.
@@ -374,9 +360,6 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
-__device__ __forceinline__ void tmem_ld_wait() {
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
 __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
@@ -514,10 +497,10 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   return r;
 }
 
-// The three parts of a row, separately (the decode writes them in three
-// passes): latent elements 8l..8l+7, latent 256+8l..256+8l+7, and rope
-// 4(l-8)..4(l-8)+3.  Each latent part shuffles its scale word from the
-// lane that holds it, so every lane of the warp must call them.
+// One latent word (8 E2M1 codes) of a row times its block's scale, as four
+// f16x2; the scale word is shuffled from lane src_lane and byte_sel picks
+// the block's byte in it, so every lane of the warp must call this.  The
+// decode writes a row in three passes (two latent word groups, then rope).
 __device__ __forceinline__ uint4 dequant_latent_part(uint32_t w, uint32_t w_ex, int src_lane,
                                                      uint32_t byte_sel) {
   const uint32_t sw = __shfl_sync(0xFFFFFFFFu, w_ex, src_lane);
@@ -533,12 +516,6 @@ __device__ __forceinline__ uint4 dequant_latent_part(uint32_t w, uint32_t w_ex, 
 // (w/2)%4 of scale word w/8.
 __device__ __forceinline__ uint4 dequant_latent_word(uint32_t w, uint32_t w_ex, int word) {
   return dequant_latent_part(w, w_ex, word >> 3, (word >> 1) & 3);
-}
-__device__ __forceinline__ uint4 dequant_latent_lo(uint32_t w_lo, uint32_t w_ex, int lane) {
-  return dequant_latent_part(w_lo, w_ex, lane >> 3, (lane >> 1) & 3);
-}
-__device__ __forceinline__ uint4 dequant_latent_hi(uint32_t w_hi, uint32_t w_ex, int lane) {
-  return dequant_latent_part(w_hi, w_ex, 4 + (lane >> 3), (lane >> 1) & 3);
 }
 __device__ __forceinline__ uint2 dequant_rope(uint32_t w_ex) {
   return make_uint2(e4m3x2_to_f16x2(w_ex & 0xFFFFu), e4m3x2_to_f16x2(w_ex >> 16));

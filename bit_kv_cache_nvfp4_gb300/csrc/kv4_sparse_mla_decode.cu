@@ -8,17 +8,22 @@
 // Work unit: one thread block per (request b, draft token s, head group g,
 // split).  A head group holds HG = min(H, 64) query heads, which all share
 // every gathered row.  The block (8 compute warps and one MMA-issue
-// warpgroup) walks its share of the top-k list in tiles of 128 keys:
+// warpgroup) first stages Q with one bulk copy and resolves the slots of its
+// first two tiles, then walks its share of the top-k list in tiles of 128
+// keys:
 //   a2     slots are resolved two tiles ahead (top-k -> page table -> slot),
-//          each dependent load spread over a tile's work
+//          each dependent load spread over a tile's work; as soon as a
+//          tile's slots are known its rows are prefetched into L2
 //   a3     each warp gathers 16 rows of the next tile into registers (three
-//          coalesced 4-byte loads per lane and row) while QK runs
+//          coalesced 4-byte loads per lane and row, without L1 allocation)
+//          while QK runs
 //   a4     and dequantizes them straight into the 128-byte-swizzled f16
 //          operand tile in shared memory (576 columns per key; E2M1 x E4M3
 //          and E4M3 values are exact in f16) in three passes -- latent
-//          0..255, latent 256..511, rope -- each into the slabs that the
-//          previous tile's PV has already released; q is converted to f16
-//          with a per-head power-of-two scale folded into the score scale
+//          slabs {0,1,4,5}, latent slabs {2,3,6,7}, rope -- each into the
+//          slabs that the previous tile's PV has already released; q is
+//          converted to f16 with a per-head power-of-two scale folded into
+//          the score scale
 //   a5     as each pass lands, lane 0 of warps 8..11 issue its share of
 //          S^T[128 x HG] = K_tile . Q^T on tcgen05 (M = 128 keys, N = HG,
 //          K = 576) into four fp32 TMEM accumulators
@@ -34,10 +39,11 @@
 //          of the latent columns; V^T is the same shared-memory tile read as
 //          an MN-major operand) and signal each 128-column slab's release
 //   a8     epilogue: O / sum(p) -> bf16 out, lse = ln 2 * (m + log2 sum(p));
-//          with several splits the normalized partial (o, lse) goes to the
-//          workspace and
+//          two splits of a unit merge inside their 2-block cluster, more
+//          write the normalized partial (o, lse) to the workspace and
 //   a9     merge_kernel combines the partials by log-sum-exp.
-// Every mbarrier wait is bounded (KV4_DEV_TIMEOUT on expiry).
+// Mbarrier waits suspend the thread (try_wait with a time hint) and are
+// bounded (KV4_DEV_TIMEOUT on expiry).
 #include "kv4_device.cuh"
 #include "kv4_launch.h"
 
