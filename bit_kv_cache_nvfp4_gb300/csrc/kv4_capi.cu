@@ -151,13 +151,13 @@ kv4_status plan_impl(int B, int Sq, int H, int K, int force_splits, int* splits,
   return KV4_OK;
 }
 
-kv4_status decode_impl(const void* q_dev, const uint8_t* pool_dev, int64_t num_slots,
-                       const int32_t* page_table_dev, int64_t pt_stride, int page_size,
-                       const int32_t* topk_idx_dev, int K, const int32_t* seq_lens_dev, int B,
-                       int Sq, int H, float sm_scale, void* out_dev, float* lse_dev,
-                       void* workspace_dev, size_t workspace_bytes, int force_splits,
-                       int32_t* dev_err, kv4_stream_t stream, int fmt, bool out_f32 = false,
-                       bool early_inputs = false, bool launch = true) {
+// The decode's host-side argument checks (shape, page size, pointers,
+// ranges, alignment), shared by every decode entry point and run before any
+// device call.  KV4_OK with B == 0 means there is nothing to launch.
+kv4_status check_decode_args(const void* q_dev, const uint8_t* pool_dev, int64_t num_slots,
+                             const int32_t* page_table_dev, int64_t pt_stride, int page_size,
+                             const int32_t* topk_idx_dev, int K, const int32_t* seq_lens_dev,
+                             int B, int Sq, int H, const void* out_dev, const float* lse_dev) {
   const kv4_status shape = check_decode_shape(B, Sq, H, K);
   if (shape != KV4_OK) return shape;
   if (page_size != KV4_PAGE) return KV4_ERR_UNSUPPORTED;
@@ -173,6 +173,20 @@ kv4_status decode_impl(const void* q_dev, const uint8_t* pool_dev, int64_t num_s
       (reinterpret_cast<uintptr_t>(topk_idx_dev) & 3u) != 0 ||
       (reinterpret_cast<uintptr_t>(seq_lens_dev) & 3u) != 0)
     return KV4_ERR_INVALID_ARG;
+  return KV4_OK;
+}
+
+kv4_status decode_impl(const void* q_dev, const uint8_t* pool_dev, int64_t num_slots,
+                       const int32_t* page_table_dev, int64_t pt_stride, int page_size,
+                       const int32_t* topk_idx_dev, int K, const int32_t* seq_lens_dev, int B,
+                       int Sq, int H, float sm_scale, void* out_dev, float* lse_dev,
+                       void* workspace_dev, size_t workspace_bytes, int force_splits,
+                       int32_t* dev_err, kv4_stream_t stream, int fmt, bool out_f32 = false,
+                       bool early_inputs = false, bool launch = true) {
+  const kv4_status args = check_decode_args(q_dev, pool_dev, num_slots, page_table_dev, pt_stride,
+                                            page_size, topk_idx_dev, K, seq_lens_dev, B, Sq, H,
+                                            out_dev, lse_dev);
+  if (args != KV4_OK || B == 0) return args;
   int sms = 0;
   const kv4_status st = device_info(&sms);
   if (st != KV4_OK) return st;
@@ -484,21 +498,16 @@ namespace {
 constexpr size_t kStaticScratchBytes = size_t(24) << 20;   // 24 MiB
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
 
-std::atomic<void*> g_static_scratch_ptr[kMaxDevices];      // per device, set up once
-
 // Device address of g_static_scratch on the current device.  In host code
-// the symbol's name is only a host-side stand-in, so its address comes from
-// cudaGetSymbolAddress, asked once per device with that device current.
+// the symbol's name is only a host-side stand-in, so the address comes from
+// cudaGetSymbolAddress with that device current.  It is looked up on every
+// call (a host-side query that allocates nothing), so a context that was
+// torn down and recreated -- and the array with it -- is always addressed
+// correctly.
 kv4_status static_scratch(void** ptr) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || p == nullptr)
     return KV4_ERR_LAUNCH;
-  void* p = g_static_scratch_ptr[dev].load();
-  if (p == nullptr) {
-    if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || p == nullptr)
-      return KV4_ERR_LAUNCH;
-    g_static_scratch_ptr[dev].store(p);
-  }
   *ptr = p;
   return KV4_OK;
 }
@@ -513,10 +522,12 @@ kv4_status kv4_sparse_mla_decode_noalloc(const void* q_dev, const uint8_t* pool_
                                          float sm_scale, void* out_dev, float* lse_dev,
                                          int force_splits, int32_t* dev_err,
                                          kv4_stream_t stream) {
-  const kv4_status shape = check_decode_shape(B, Sq, H, K);
-  if (shape != KV4_OK) return shape;
-  if (page_size != KV4_PAGE) return KV4_ERR_UNSUPPORTED;
-  if (B == 0) return KV4_OK;
+  // every argument is checked first, so that a bad pointer is reported as
+  // such and not as a shape beyond the scratch array
+  const kv4_status args = check_decode_args(q_dev, pool_dev, num_slots, page_table_dev, pt_stride,
+                                            page_size, topk_idx_dev, K, seq_lens_dev, B, Sq, H,
+                                            out_dev, lse_dev);
+  if (args != KV4_OK || B == 0) return args;
   int sms = 0;
   kv4_status st = device_info(&sms);
   if (st != KV4_OK) return st;

@@ -289,12 +289,16 @@ kv4_status kv4_merge_partials(const float* o_parts_dev, const float* lse_parts_d
  *   - The split-K partials go to a file-scope device array inside the library
  *     of kv4_noalloc_scratch_bytes() bytes (24 MiB).  Every device that loads
  *     the library holds it until the process exits.
- *   - A shape whose planned partials need more than that returns
- *     KV4_ERR_SCRATCH_LIMIT and launches nothing (force fewer splits, or use
- *     kv4_sparse_mla_decode with a workspace).
- *   - The first call on each device looks up the array's device address
- *     (cudaGetSymbolAddress, with that device current); make that first call
- *     before any stream capture.
+ *   - Arguments are checked first, as in kv4_sparse_mla_decode (null or
+ *     misaligned pointers: KV4_ERR_INVALID_ARG; shapes and page sizes:
+ *     KV4_ERR_UNSUPPORTED).  Then a shape whose planned partials need more
+ *     than the array returns KV4_ERR_SCRATCH_LIMIT and launches nothing
+ *     (force fewer splits, or use kv4_sparse_mla_decode with a workspace).
+ *   - Every call looks up the array's device address on the current device
+ *     (cudaGetSymbolAddress: a host-side query that allocates nothing), so
+ *     the address stays right across a device reset.  The first call on a
+ *     device may also load the library's kernels there; make that first
+ *     call before any stream capture.
  *   - All calls share the one array, which keeps the last call's contents;
  *     nothing in it needs to start at zero (every partial is written before
  *     it is read).  Calls whose kernels overlap on the GPU (two streams, or

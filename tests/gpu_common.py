@@ -3,6 +3,8 @@ library, and oracle results for the same seeded inputs on the host."""
 from __future__ import annotations
 
 import functools
+import multiprocessing as mp
+import os
 
 import numpy as np
 import pytest
@@ -11,14 +13,21 @@ import torch
 import oracle
 from bit_kv_cache_nvfp4_gb300 import workloads as wl
 
-# Tolerances.  The computation must be within 2e-2 of the oracle on every
-# output element and within 1e-3 on every lse.  The output tensor is bf16,
-# and rounding an exact value to bf16 alone moves it by up to half a bf16
-# ulp -- more than 2e-2 once |out| >= 8, which the x8 outlier channels of the
-# workloads reach -- so each element is allowed 2e-2 plus half a bf16 ulp at
-# its magnitude.
+# Tolerances.  Every lse must be within 1e-3 of the oracle's, and every
+# output element within 2e-2 -- plainly, wherever the oracle's value is below
+# 8 in magnitude.  At |out| >= 8 (the x8 outlier channels of the workloads
+# reach it) half a bf16 ulp is itself more than 2e-2 (1/32 at [8, 16)): the
+# rounding of the exact value to the bf16 output alone can exceed the bound,
+# so there, and only there, each element is allowed 2e-2 for the computation
+# plus half a bf16 ulp at its magnitude for the output rounding.
 OUT_ATOL = 2e-2
 LSE_ATOL = 1e-3
+ROUNDING_ALLOWANCE_FROM = 8.0
+
+# Per-case parity records (largest errors, the oracle value at the worst
+# element, the share of the bound used), printed at the end of the session by
+# conftest.py and written as JSON where KV4_PARITY_LOG names a file.
+PARITY_RECORDS: list = []
 
 
 def bf16_half_ulp(x: np.ndarray) -> np.ndarray:
@@ -26,6 +35,13 @@ def bf16_half_ulp(x: np.ndarray) -> np.ndarray:
     a = np.abs(np.asarray(x, dtype=np.float64))
     e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
     return np.where(a > 0, np.exp2(e - 8), 0.0)
+
+
+def out_bound(out_ref: np.ndarray) -> np.ndarray:
+    """Per-element bound on |out_gpu - out_ref|: 2e-2, plus half a bf16 ulp
+    only where |out_ref| >= 8."""
+    a = np.abs(np.asarray(out_ref, dtype=np.float64))
+    return OUT_ATOL + np.where(a >= ROUNDING_ALLOWANCE_FROM, bf16_half_ulp(a), 0.0)
 
 
 def need_gpu():
@@ -91,6 +107,29 @@ def oracle_decode(w: wl.Workload, requests, splits: int = 1):
     return np.stack(outs), np.stack(lses)
 
 
+def _oracle_decode_job(args):
+    name, seed, requests = args
+    torch.set_num_threads(1)
+    return requests, oracle_decode(workload(name, seed), requests)
+
+
+_ORACLE_POOL = None
+
+
+def oracle_decode_many(w: wl.Workload, requests):
+    """oracle_decode for many requests of a named workload, one request per
+    job on a pool of single-threaded worker processes (started with spawn, so
+    they hold no CUDA state); results in the order of `requests`."""
+    global _ORACLE_POOL
+    if _ORACLE_POOL is None:
+        _ORACLE_POOL = mp.get_context("spawn").Pool(max(1, min(16, os.cpu_count() or 1)))
+    jobs = [(w.name, w.seed // 1000, [b]) for b in requests]
+    got = {}
+    for reqs, (o, l) in _ORACLE_POOL.imap_unordered(_oracle_decode_job, jobs):
+        got[reqs[0]] = (o[0], l[0])
+    return (np.stack([got[b][0] for b in requests]), np.stack([got[b][1] for b in requests]))
+
+
 def assert_close(out_gpu: torch.Tensor, lse_gpu: torch.Tensor, out_ref: np.ndarray,
                  lse_ref: np.ndarray, what: str = ""):
     o = out_gpu.float().cpu().numpy()
@@ -101,11 +140,23 @@ def assert_close(out_gpu: torch.Tensor, lse_gpu: torch.Tensor, out_ref: np.ndarr
     err_o = np.abs(o.astype(np.float64) - out_ref)
     err_l = np.where(both_inf, 0.0, np.abs(l - lse_ref))
     assert np.isfinite(o).all(), f"{what}: non-finite output"
-    bound = OUT_ATOL + bf16_half_ulp(out_ref)
+    bound = out_bound(out_ref)
     excess = err_o - bound
     i = np.unravel_index(np.argmax(excess), excess.shape)
     assert excess[i] <= 0, (f"{what}: |out err| {err_o[i]:.4g} > {bound[i]:.4g} at {i} "
                             f"(oracle {out_ref[i]:.5g}, gpu {o[i]:.5g})")
     mo, ml = float(err_o.max()), float(err_l.max())
     assert ml <= LSE_ATOL, f"{what}: max |lse err| {ml:.4g} > {LSE_ATOL}"
+    used = err_o / bound
+    j = np.unravel_index(np.argmax(used), used.shape)
+    small = np.abs(out_ref) < ROUNDING_ALLOWANCE_FROM
+    PARITY_RECORDS.append({
+        "case": what, "elements": int(o.size),
+        "max_out_err": mo,
+        "out_ref_at_max_err": float(out_ref[np.unravel_index(np.argmax(err_o), err_o.shape)]),
+        "max_out_err_below_8": float(err_o[small].max()) if small.any() else 0.0,
+        "max_out_err_at_8_and_above": float(err_o[~small].max()) if (~small).any() else 0.0,
+        "max_share_of_out_bound": float(used[j]),
+        "max_lse_err": ml, "share_of_lse_bound": ml / LSE_ATOL,
+    })
     return mo, ml

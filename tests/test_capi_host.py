@@ -111,3 +111,37 @@ def test_write_and_decode_checks_both_parts_first(lib):
     assert fn(ptr, 512, ptr, 64, ptr, 4, ptr, 64,
               ptr, ptr, 1, 64, ptr, 8, ptr, 1, 1, 16, 0.1, None, None, None, 0, 0, None,
               None) == 1
+
+
+def test_noalloc_checks_arguments_before_its_scratch_limit(lib):
+    """kv4_sparse_mla_decode_noalloc reports bad pointers and unsupported
+    shapes as such, before it looks at the size of its scratch array or at
+    the device."""
+    P, i64, i32, f = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float
+    fn = lib.kv4_sparse_mla_decode_noalloc
+    fn.argtypes = [P, P, i64, P, i64, i32, P, i32, P, i32, i32, i32, f, P, P, i32, P, P]
+    fn.restype = i32
+    buf = ctypes.create_string_buffer(1 << 12)
+    a = (ctypes.addressof(buf) + 255) & ~255          # 256-byte aligned inside buf
+    ok = ctypes.c_void_p(a)
+    odd = ctypes.c_void_p(a + 4)                        # 4-byte aligned only
+    # a large shape (16 splits of 16 x 64 heads would exceed the array) but a
+    # null q: invalid argument, not a scratch-limit refusal
+    assert fn(None, ok, 64, ok, 1, 64, ok, 2048, ok, 16, 1, 64, 0.1, ok, ok, 16, None,
+              None) == 1
+    # null out / lse
+    assert fn(ok, ok, 64, ok, 1, 64, ok, 2048, ok, 16, 1, 64, 0.1, None, ok, 16, None,
+              None) == 1
+    assert fn(ok, ok, 64, ok, 1, 64, ok, 2048, ok, 16, 1, 64, 0.1, ok, None, 16, None,
+              None) == 1
+    # misaligned output
+    assert fn(ok, ok, 64, ok, 1, 64, ok, 2048, ok, 16, 1, 64, 0.1, odd, ok, 16, None,
+              None) == 1
+    # unsupported page size and head count
+    assert fn(ok, ok, 64, ok, 1, 32, ok, 2048, ok, 16, 1, 64, 0.1, ok, ok, 16, None,
+              None) == 2
+    assert fn(ok, ok, 64, ok, 1, 64, ok, 2048, ok, 16, 1, 48, 0.1, ok, ok, 16, None,
+              None) == 2
+    # an empty batch is a no-op
+    assert fn(None, None, 64, None, 1, 64, None, 8, None, 0, 1, 16, 0.1, None, None, 0, None,
+              None) == 0

@@ -20,7 +20,7 @@ import torch
 import oracle
 from bit_kv_cache_nvfp4_gb300 import workloads as wl
 from gpu_common import (assert_close, bits, device_inputs, gpu_pool, need_gpu, oracle_decode,
-                        workload)
+                        oracle_decode_many, workload)
 
 pytestmark = pytest.mark.gpu
 
@@ -36,8 +36,8 @@ def kv():
 CASES = {
     "tiny": None,          # all requests
     "decode": None,
-    "long": [0, 17, 40, 63],
-    "specverify": [0, 9, 31],
+    "long": [0, 3, 7, 12, 17, 21, 26, 30, 33, 38, 40, 45, 50, 54, 59, 63],
+    "specverify": [0, 2, 4, 6, 9, 11, 13, 15, 17, 19, 21, 23, 25, 27, 29, 31],
     "splitk": None,
 }
 
@@ -53,7 +53,7 @@ def test_decode_matches_oracle(name):
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     req = CASES[name] or list(range(w.B))
-    out_ref, lse_ref = oracle_decode(w, req)
+    out_ref, lse_ref = oracle_decode_many(w, req)
     mo, ml = assert_close(out[req], lse[req], out_ref, lse_ref, name)
     print(f"{name}: max|out err| {mo:.3g}  max|lse err| {ml:.3g}")
     # properties that hold for every request at full size

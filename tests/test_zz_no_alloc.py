@@ -4,13 +4,19 @@ It exists for callers that cannot allocate device memory when they run the
 decode -- e.g. a plugin whose host engine gives it only its inputs and
 outputs and owns all device memory -- and keeps its split-K partials in a
 static device array inside the library.  This test calls it through the
-C ABI twice in a row (the second call reuses the array with the first call's
-contents still in it) on a shape forced to 16 splits -- more than one thread
-block cluster merges, so the partials do go to the array -- checks both
-results against the regular entry point within the parity tolerance, and checks that a shape needing more partial storage than
-the array holds is refused with KV4_ERR_SCRATCH_LIMIT.  It sits in a file of
-its own that pytest collects last, and builds everything it needs itself, so
-it passes both alone in a fresh process and after the other tests.
+C ABI on a shape forced to 16 splits -- more than one thread block cluster
+merges, so the partials do go to the array:
+
+- first with other queries (negated), which fills the array with partials
+  unlike the ones the next call must produce;
+- then twice in a row with the real queries, each result checked against the
+  regular entry point and against the CPU oracle, within the parity bound.
+
+A call that read a stale partial instead of writing its own would fail the
+first of those checks.  It also checks that a shape needing more partial
+storage than the array holds is refused with KV4_ERR_SCRATCH_LIMIT.  The file
+is collected last and builds everything it needs itself, so it passes both
+alone in a fresh process and after the other tests.
 """
 import ctypes
 
@@ -19,7 +25,7 @@ import pytest
 import torch
 
 from bit_kv_cache_nvfp4_gb300 import workloads as wl
-from gpu_common import LSE_ATOL, OUT_ATOL, bf16_half_ulp, need_gpu
+from gpu_common import LSE_ATOL, need_gpu, oracle_decode, out_bound
 
 pytestmark = pytest.mark.gpu
 
@@ -64,6 +70,15 @@ def test_noalloc_decode_matches_regular_entry_point():
     torch.cuda.synchronize()
     ref_o = ref_out.float().cpu().numpy()
     ref_l = ref_lse.cpu().numpy()
+    ora_o, ora_l = oracle_decode(w, list(range(w.B)))
+
+    # other queries first: the array then holds partials unlike the next call's
+    other_out, other_lse = torch.empty_like(ref_out), torch.empty_like(ref_lse)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    assert _call(f, q.neg(), pool, pt, topk, lens, w, other_out, other_lse, err,
+                 force_splits=16) == 0
+    torch.cuda.synchronize()
+    assert not torch.equal(other_lse, ref_lse)
 
     for call in range(2):
         out = torch.full_like(ref_out, float("nan"))
@@ -75,8 +90,9 @@ def test_noalloc_decode_matches_regular_entry_point():
         o = out.float().cpu().numpy()
         l = lse.cpu().numpy()
         assert np.isfinite(o).all() and np.isfinite(l).all(), f"call {call}"
-        assert np.all(np.abs(o - ref_o) <= OUT_ATOL + bf16_half_ulp(ref_o)), f"call {call}"
-        assert np.all(np.abs(l - ref_l) <= LSE_ATOL), f"call {call}"
+        for what, ro, rl in (("regular entry point", ref_o, ref_l), ("oracle", ora_o, ora_l)):
+            assert np.all(np.abs(o - ro) <= out_bound(ro)), f"call {call} vs {what}"
+            assert np.all(np.abs(l - rl) <= LSE_ATOL), f"call {call} vs {what}"
 
 
 def test_noalloc_refuses_shapes_beyond_its_scratch():
