@@ -408,6 +408,9 @@ def run_gpu(args):
     # end to end through the public API, host buffers in and out
     e2e = run_e2e(kv, w, dev, pool, pt, lens, flush, args)
     cache_write = run_cache_write(kv, dev, flush, args)
+    per_config = None
+    if rank == 0 and not args.skip_per_config:
+        per_config = run_per_config(kv, dev, flush, args, long_inputs=(w, pool))
     latent = fp8 = None
     if not args.skip_variants:
         scratch = run_scratch_path(kv, w, dev, pool, q, pt, topk, lens, flush, args)
@@ -477,6 +480,7 @@ def run_gpu(args):
             "latent_rows_288B": latent,
             "fp8_comparison": fp8,
             "cache_write_1M_tokens": cache_write,
+            "per_config": per_config,
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clocks.summary(),
             "wall_s_timed_loop": wall,
@@ -501,6 +505,106 @@ def _time_loop(fn, flush, stream, steps, warmup):
         e1[i].record(stream)
     torch.cuda.synchronize()
     return sum(a.elapsed_time(b) for a, b in zip(e0, e1)) / steps
+
+
+def graph_time_us(fn, flush, trials: int = 7, replays: int = 200):
+    """Device time of one fn() call, in the timing form of the pages'
+    graph-timed microbenchmarks: fn is captured in a CUDA graph and replayed
+    `replays` times back to back between two events; the median over
+    `trials` of the mean per replay.  Returns (cold, hot) microseconds: hot
+    replays fn alone (its inputs stay in L2 from one replay to the next);
+    cold replays [256 MiB L2 flush, fn] and subtracts the flush alone."""
+    stream = torch.cuda.current_stream()
+
+    def capture(body):
+        for _ in range(2):                       # warm-up outside the capture
+            body()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            body()
+        return g
+
+    def timed(g):
+        meds = []
+        for _ in range(trials):
+            g.replay()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(replays):
+                g.replay()
+            b.record(stream)
+            b.synchronize()
+            meds.append(a.elapsed_time(b) * 1e3 / replays)
+        return statistics.median(meds)
+
+    def flushed():
+        flush.zero_()
+        fn()
+
+    hot = timed(capture(fn))
+    cold = timed(capture(flushed)) - timed(capture(flush.zero_))
+    return cold, hot
+
+
+PER_CONFIG_BOUND = {"tiny": "latency", "decode": "hbm ~ tensor", "long": "hbm ~ tensor (ridge)",
+                    "specverify": "tensor", "splitk": "latency and SM fill"}
+
+
+def run_per_config(kv, dev, flush, args, long_inputs=None):
+    """Every configuration of the pages' workloads, each as one decode step
+    (the cache write of the step's new tokens, then the decode), timed with
+    CUDA-graph replays (cold and hot L2; graph_time_us), with the decode
+    kernel alone, gathered-KV GB/s, both roofline fractions, and the oracle
+    on one core on a bounded sample of the same workload."""
+    peak_gbs, peak_tflops, _ = measured_peaks()
+    res = {}
+    for name in wl.CONFIG_NAMES:
+        if name == "long" and long_inputs is not None:
+            w, pool = long_inputs
+        else:
+            w = wl.make_workload(name, seed=0)
+            pool = build_pool(w, dev)
+        q = wl.queries(w, dev)
+        pt, topk, lens = w.page_table.to(dev), w.topk.to(dev), w.seq_lens.to(dev)
+        nl, nr, ns = wl.newest_tokens(w, dev)
+        splits, ws_bytes = kv.decode_plan(w.B, w.Sq, w.H, w.K)
+        out = torch.empty((w.B, w.Sq, w.H, 512), dtype=torch.bfloat16, device=dev)
+        lse = torch.empty((w.B, w.Sq, w.H), dtype=torch.float32, device=dev)
+        ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+
+        def step():
+            kv.quantize_write_and_decode(nl, nr, ns, pool, q, pt, topk, lens, w.sm_scale,
+                                         out=out, lse=lse, workspace=ws)
+
+        def decode():
+            kv.sparse_mla_decode(q, pool, pt, topk, lens, w.sm_scale, out=out, lse=lse,
+                                 workspace=ws)
+
+        step_cold, step_hot = graph_time_us(step, flush)
+        dec_cold, dec_hot = graph_time_us(decode, flush)
+        valid = valid_key_count(w)
+        alg = algorithmic_bytes(w, valid)
+        flops = 2.0 * w.H * valid * (576 + 512)
+        t_hbm, t_tensor = alg / (peak_gbs * 1e3), flops / (peak_tflops * 1e6)   # us
+        reqs = [0]
+        runs = [oracle_sample(w, reqs)[0] for _ in range(3 if w.H * w.Sq <= 64 else 1)]
+        o_s = statistics.median(runs)
+        res[name] = {
+            "B": w.B, "Sq": w.Sq, "H": w.H, "K": w.K, "splits": splits,
+            "step_us_cold": step_cold, "step_us_hot": step_hot,
+            "decode_us_cold": dec_cold, "decode_us_hot": dec_hot,
+            "kv_gbs_cold": valid * 352 / (step_cold * 1e-6) / 1e9,
+            "algorithmic_bytes": alg, "flops": flops,
+            "bound_per_pages_table": PER_CONFIG_BOUND[name],
+            "ideal_us": {"hbm": t_hbm, "tensor": t_tensor},
+            "decode_hbm_frac": t_hbm / dec_cold, "decode_tensor_frac": t_tensor / dec_cold,
+            "oracle_1core_ms_per_request": o_s * 1e3,
+            "oracle_1core_ms_per_step_est": o_s * 1e3 * w.B,
+        }
+        del pool, q, pt, topk, lens, out, lse, ws
+        torch.cuda.empty_cache()
+    return res
 
 
 def run_scratch_path(kv, w, dev, pool, q, pt, topk, lens, flush, args):
@@ -632,50 +736,91 @@ def run_latent_rows(kv, w, dev, q, pt, topk, lens, flush, err, args, valid):
             "note": "QK over the 512 latent columns, PV over the same 512; same workload"}
 
 
-def run_e2e(kv, w, dev, pool, pt, lens, flush, args):
-    """Same step through the public API with pinned host inputs and outputs."""
+def run_e2e(kv, w, dev, pool, pt, lens, flush, args, variants: int = 4):
+    """The same step through the public API with pinned host inputs and
+    outputs, as a serving loop runs it: every step copies its inputs (q, the
+    top-k list, the new tokens and their slots) from pinned host memory and
+    reads its result (out, lse) back into pinned host memory, and the copies
+    of step i+1's inputs and of step i-1's result run on two copy streams
+    while step i computes (double-buffered device inputs and outputs).  The
+    timed region spans all K steps, copies included.  L2 stays cold without a
+    flush: consecutive steps rotate over `variants` top-k sets (the same
+    positions shifted, so the same counts and structure) whose rows together
+    exceed L2."""
+    K = args.steps
+    L = lens.to(torch.int64).cpu().view(-1, 1, 1)
     q_h = wl.queries(w).pin_memory()
-    topk_h = w.topk.pin_memory()
+    topk_h = [((w.topk.to(torch.int64) + 7919 * 64 * v) % L).to(torch.int32).pin_memory()
+              for v in range(variants)]
     nl, nr, ns = wl.newest_tokens(w)
     nl_h, nr_h, ns_h = nl.pin_memory(), nr.pin_memory(), ns.pin_memory()
-    out_h = torch.empty((w.B, w.Sq, w.H, 512), dtype=torch.bfloat16).pin_memory()
-    lse_h = torch.empty((w.B, w.Sq, w.H), dtype=torch.float32).pin_memory()
-    q_d = torch.empty_like(q_h, device=dev)
-    topk_d = torch.empty_like(topk_h, device=dev)
-    nl_d, nr_d, ns_d = (torch.empty_like(nl_h, device=dev), torch.empty_like(nr_h, device=dev),
-                        torch.empty_like(ns_h, device=dev))
-    stream = torch.cuda.current_stream(dev)
-    h2d = sum(t.numel() * t.element_size() for t in (q_h, topk_h, nl_h, nr_h, ns_h))
-    d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
+    out_h = [torch.empty((w.B, w.Sq, w.H, 512), dtype=torch.bfloat16).pin_memory()
+             for _ in range(2)]
+    lse_h = [torch.empty((w.B, w.Sq, w.H), dtype=torch.float32).pin_memory() for _ in range(2)]
+    bufs = [dict(q=torch.empty_like(q_h, device=dev), topk=torch.empty_like(topk_h[0], device=dev),
+                 nl=torch.empty_like(nl_h, device=dev), nr=torch.empty_like(nr_h, device=dev),
+                 ns=torch.empty_like(ns_h, device=dev),
+                 out=torch.empty(out_h[0].shape, dtype=torch.bfloat16, device=dev),
+                 lse=torch.empty(lse_h[0].shape, dtype=torch.float32, device=dev))
+            for _ in range(2)]
+    splits, ws_bytes = kv.decode_plan(w.B, w.Sq, w.H, w.K)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    compute = torch.cuda.current_stream(dev)
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    h2d = sum(t.numel() * t.element_size() for t in (q_h, topk_h[0], nl_h, nr_h, ns_h))
+    d2h = out_h[0].numel() * out_h[0].element_size() + lse_h[0].numel() * lse_h[0].element_size()
 
-    def step():
-        q_d.copy_(q_h, non_blocking=True)
-        topk_d.copy_(topk_h, non_blocking=True)
-        nl_d.copy_(nl_h, non_blocking=True)
-        nr_d.copy_(nr_h, non_blocking=True)
-        ns_d.copy_(ns_h, non_blocking=True)
-        out, lse = kv.quantize_write_and_decode(nl_d, nr_d, ns_d, pool, q_d, pt, topk_d, lens,
-                                                w.sm_scale)
-        out_h.copy_(out, non_blocking=True)
-        lse_h.copy_(lse, non_blocking=True)
+    def run(n):
+        ev_in = [torch.cuda.Event() for _ in range(n)]
+        ev_dec = [torch.cuda.Event() for _ in range(n)]
+        ev_out = [torch.cuda.Event() for _ in range(n)]
 
-    for _ in range(max(3, args.warmup)):
-        step()
+        def load(i):                       # inputs of step i into buffer i % 2
+            b = bufs[i % 2]
+            with torch.cuda.stream(s_in):
+                if i >= 2:
+                    s_in.wait_event(ev_dec[i - 2])        # buffer free again
+                b["q"].copy_(q_h, non_blocking=True)
+                b["topk"].copy_(topk_h[i % variants], non_blocking=True)
+                b["nl"].copy_(nl_h, non_blocking=True)
+                b["nr"].copy_(nr_h, non_blocking=True)
+                b["ns"].copy_(ns_h, non_blocking=True)
+                ev_in[i].record(s_in)
+
+        load(0)
+        for i in range(n):
+            if i + 1 < n:
+                load(i + 1)
+            b = bufs[i % 2]
+            compute.wait_event(ev_in[i])
+            if i >= 2:
+                compute.wait_event(ev_out[i - 2])         # result buffer read back
+            kv.quantize_write_and_decode(b["nl"], b["nr"], b["ns"], pool, b["q"], pt, b["topk"],
+                                         lens, w.sm_scale, out=b["out"], lse=b["lse"],
+                                         workspace=ws)
+            ev_dec[i].record(compute)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_dec[i])
+                out_h[i % 2].copy_(b["out"], non_blocking=True)
+                lse_h[i % 2].copy_(b["lse"], non_blocking=True)
+                ev_out[i].record(s_out)
+        compute.wait_event(ev_out[n - 1])
+
+    run(max(3, args.warmup))
     torch.cuda.synchronize(dev)
-    times = []
-    for _ in range(args.steps):
-        flush.zero_()
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        step()
-        b.record(stream)
-        b.synchronize()
-        times.append(a.elapsed_time(b))
-    t = sum(times) / len(times)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s_in.wait_stream(compute)
+    a.record(compute)
+    s_in.wait_event(a)
+    run(K)
+    b.record(compute)
+    b.synchronize()
+    t = a.elapsed_time(b) / K
     valid = valid_key_count(w)
     return {"value": valid * 352 / (t * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": t,
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "form": (f"pipelined over {K} steps (inputs of step i+1 and result of step i-1 "
+                     f"copied while step i computes); L2 cold by rotating {variants} top-k sets")}
 
 
 def main(argv=None):
@@ -690,6 +835,8 @@ def main(argv=None):
                    help="sessions of the long-context workload per rank (smaller: profiling)")
     p.add_argument("--skip-variants", action="store_true",
                    help="skip the 288-byte row and FP8 comparison measurements")
+    p.add_argument("--skip-per-config", action="store_true",
+                   help="skip the graph-timed measurement of every workload configuration")
     p.add_argument("--splits", type=int, default=0,
                    help="force the split-K count (0: the library's plan)")
     args = p.parse_args(argv)

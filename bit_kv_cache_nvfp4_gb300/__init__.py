@@ -26,7 +26,8 @@ __all__ = [
     "quantize_write_mse", "quantize_write_fp8", "decode_plan_fp8", "sparse_mla_decode_fp8",
     "fp8_scratch", "scratch_index", "ROW_BYTES_FP8", "quantize_write_and_decode", "quantize_write_latent", "decode_plan_latent", "sparse_mla_decode_latent",
     "debug_gather_dequant_latent", "sparse_mla_decode_partial", "dcp_mask_topk",
-    "merge_partials", "gather_partials", "dcp_sparse_mla_decode", "ROW_BYTES", "ROW_BYTES_LATENT", "LATENT", "ROPE", "QK_DIM", "PAGE", "DEV_BAD_SLOT", "DEV_BAD_PAGE",
+    "merge_partials", "gather_partials", "dcp_sparse_mla_decode", "dcp_local_page_table",
+    "dcp_local_slots", "dcp_local_pages", "ROW_BYTES", "ROW_BYTES_LATENT", "LATENT", "ROPE", "QK_DIM", "PAGE", "DEV_BAD_SLOT", "DEV_BAD_PAGE",
     "DEV_TIMEOUT",
 ]
 
@@ -91,6 +92,12 @@ def load_library():
         lib.kv4_sparse_mla_decode_partial.restype = i32
         lib.kv4_dcp_mask_topk.argtypes = [P, P, i64, P, i32, i32, i32, i32, i32, P, P]
         lib.kv4_dcp_mask_topk.restype = i32
+        lib.kv4_dcp_local_page_table.argtypes = [P, i64, i32, i32, i32, P, P]
+        lib.kv4_dcp_local_page_table.restype = i32
+        lib.kv4_dcp_local_slots.argtypes = [P, i64, i32, i32, P, P]
+        lib.kv4_dcp_local_slots.restype = i32
+        lib.kv4_fp8_scratch_index.argtypes = [P, i32, P, i32, i32, P, P, P, P]
+        lib.kv4_fp8_scratch_index.restype = i32
         lib.kv4_merge_partials.argtypes = [P, P, i32, i64, P, P, P]
         lib.kv4_merge_partials.restype = i32
         lib.kv4_quantize_write_latent.argtypes = [P, i64, P, i64, P, i64, P, P]
@@ -291,22 +298,22 @@ def scratch_index(topk_idx: torch.Tensor, seq_lens: torch.Tensor):
     """Indexing that makes a scratch copy (row (b*Sq + s)*K + k for key k of
     token s of request b) look like a paged pool: (page_table, topk, seq_lens)
     for a decode of B*Sq one-token requests whose K positions are 0..K-1,
-    masked where the original key is masked.  K must be a multiple of 64."""
+    masked where the original key is masked (kv4_fp8_scratch_index).  K must
+    be a multiple of 64."""
+    lib = load_library()
     B, Sq, K = topk_idx.shape
     if K % PAGE:
         raise ValueError("the scratch path needs K to be a multiple of 64")
     dev = topk_idx.device
     n = B * Sq
-    pages = K // PAGE
-    page_table = (torch.arange(n, device=dev, dtype=torch.int32)[:, None] * pages +
-                  torch.arange(pages, device=dev, dtype=torch.int32)[None, :])
-    pos = torch.arange(K, device=dev, dtype=torch.int32)
-    s_idx = torch.arange(Sq, device=dev)
-    l_eff = seq_lens.to(torch.int64)[:, None] - (Sq - 1 - s_idx)[None, :]          # [B, Sq]
-    valid = (topk_idx >= 0) & (topk_idx.to(torch.int64) < l_eff[..., None])
-    topk = torch.where(valid, pos, torch.full_like(pos, -1)).reshape(n, 1, K).contiguous()
-    lens = torch.full((n,), K, dtype=torch.int32, device=dev)
-    return page_table.contiguous(), topk, lens
+    page_table = torch.empty((n, max(1, K // PAGE)), dtype=torch.int32, device=dev)
+    topk = torch.empty((n, 1, K), dtype=torch.int32, device=dev)
+    lens = torch.empty((n,), dtype=torch.int32, device=dev)
+    _check("kv4_fp8_scratch_index", lib.kv4_fp8_scratch_index(
+        _dev(topk_idx, "topk_idx", torch.int32), K, _dev(seq_lens, "seq_lens", torch.int32), B,
+        Sq, _dev(page_table, "pt_out", torch.int32), _dev(topk, "topk_out", torch.int32),
+        _dev(lens, "lens_out", torch.int32), _stream(dev)))
+    return page_table, topk, lens
 
 
 def sparse_mla_decode_partial(q: torch.Tensor, pool: torch.Tensor, page_table: torch.Tensor,
@@ -335,6 +342,35 @@ def dcp_mask_topk(topk_idx: torch.Tensor, page_table: torch.Tensor, seq_lens: to
         page_table.shape[1], _dev(seq_lens, "seq_lens", torch.int32), B, Sq, K, int(world),
         int(rank), _dev(out, "topk_out", torch.int32), _stream(topk_idx.device)))
     return out
+
+
+def dcp_local_page_table(page_table: torch.Tensor, world: int, rank: int) -> torch.Tensor:
+    """Rank ``rank``'s page table over its own pool: p // world where the
+    rank owns physical page p (p % world == rank), -1 elsewhere."""
+    lib = load_library()
+    B, stride = page_table.shape
+    out = torch.empty_like(page_table)
+    _check("kv4_dcp_local_page_table", lib.kv4_dcp_local_page_table(
+        _dev(page_table, "page_table", torch.int32), stride, B, int(world), int(rank),
+        _dev(out, "pt_local", torch.int32), _stream(page_table.device)))
+    return out
+
+
+def dcp_local_slots(slot_mapping: torch.Tensor, world: int, rank: int) -> torch.Tensor:
+    """Cache-write slots in rank ``rank``'s own pool: (page // world) * 64 +
+    slot % 64 for the tokens on the rank's pages, -1 (no write) elsewhere."""
+    lib = load_library()
+    out = torch.empty_like(slot_mapping)
+    _check("kv4_dcp_local_slots", lib.kv4_dcp_local_slots(
+        _dev(slot_mapping, "slot_mapping", torch.int64), slot_mapping.numel(), int(world),
+        int(rank), _dev(out, "slots_out", torch.int64), _stream(slot_mapping.device)))
+    return out
+
+
+def dcp_local_pages(num_pages: int, world: int, rank: int) -> int:
+    """Pages of rank ``rank``'s own pool when the cache has ``num_pages``
+    physical pages: those p < num_pages with p % world == rank."""
+    return max(0, (num_pages - rank + world - 1) // world)
 
 
 def merge_partials(o_parts: torch.Tensor, lse_parts: torch.Tensor):
@@ -367,16 +403,19 @@ def gather_partials(o: torch.Tensor, lse: torch.Tensor, group=None):
     return torch.stack(o_list), torch.stack(lse_list)
 
 
-def dcp_sparse_mla_decode(q, pool, page_table, topk_idx, seq_lens, sm_scale, group=None,
+def dcp_sparse_mla_decode(q, local_pool, page_table, topk_idx, seq_lens, sm_scale, group=None,
                           dev_err=None):
     """One decode step with the context split over the ranks of ``group``:
-    each rank decodes the keys on its pages (its pool holds them), the ranks
-    all-gather their fp32 (o, lse), and every rank merges them into the full
-    result (out bf16 [B,Sq,H,512], lse fp32 [B,Sq,H])."""
+    each rank decodes the keys on its pages from its own pool (``local_pool``:
+    the rank's pages only, written through dcp_local_slots) via its local page
+    table, the ranks all-gather their fp32 (o, lse), and every rank merges
+    them into the full result (out bf16 [B,Sq,H,512], lse fp32 [B,Sq,H]).
+    ``page_table`` is the global (physical) one."""
     import torch.distributed as dist
     world, rank = dist.get_world_size(group), dist.get_rank(group)
     mine = dcp_mask_topk(topk_idx, page_table, seq_lens, world, rank)
-    o, lse = sparse_mla_decode_partial(q, pool, page_table, mine, seq_lens, sm_scale,
+    pt_local = dcp_local_page_table(page_table, world, rank)
+    o, lse = sparse_mla_decode_partial(q, local_pool, pt_local, mine, seq_lens, sm_scale,
                                        dev_err=dev_err)
     o_parts, lse_parts = gather_partials(o, lse, group)
     return merge_partials(o_parts, lse_parts)

@@ -46,7 +46,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
         return LIB_PATH
     nvcc = _nvcc()
     os.makedirs(BUILD_DIR, exist_ok=True)
-    flags = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
+    flags = ARCH + ["-O3", "-lineinfo", "-std=c++20", "-Xcompiler", "-fPIC,-O2",
                     "-I", INCLUDE, "-I", CSRC] + list(extra_flags or [])
     procs = []
     objs = []

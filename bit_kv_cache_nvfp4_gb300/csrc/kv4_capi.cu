@@ -359,6 +359,36 @@ kv4_status kv4_dcp_mask_topk(const int32_t* topk_idx_dev, const int32_t* page_ta
              : KV4_ERR_LAUNCH;
 }
 
+kv4_status kv4_dcp_local_page_table(const int32_t* page_table_dev, int64_t pt_stride, int B,
+                                   int world, int rank, int32_t* pt_local_dev,
+                                   kv4_stream_t stream) {
+  if (B < 0 || pt_stride < 1 || world < 1 || rank < 0 || rank >= world) return KV4_ERR_INVALID_ARG;
+  if (B == 0) return KV4_OK;
+  if (!page_table_dev || !pt_local_dev) return KV4_ERR_INVALID_ARG;
+  int sms = 0;
+  const kv4_status st = device_info(&sms);
+  if (st != KV4_OK) return st;
+  return kv4::launch_dcp_local_page_table(page_table_dev, static_cast<int64_t>(B) * pt_stride,
+                                          world, rank, pt_local_dev,
+                                          reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? KV4_OK
+             : KV4_ERR_LAUNCH;
+}
+
+kv4_status kv4_dcp_local_slots(const int64_t* slot_mapping_dev, int64_t n_tokens, int world,
+                               int rank, int64_t* slots_out_dev, kv4_stream_t stream) {
+  if (n_tokens < 0 || world < 1 || rank < 0 || rank >= world) return KV4_ERR_INVALID_ARG;
+  if (n_tokens == 0) return KV4_OK;
+  if (!slot_mapping_dev || !slots_out_dev) return KV4_ERR_INVALID_ARG;
+  int sms = 0;
+  const kv4_status st = device_info(&sms);
+  if (st != KV4_OK) return st;
+  return kv4::launch_dcp_local_slots(slot_mapping_dev, n_tokens, world, rank, slots_out_dev,
+                                     reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? KV4_OK
+             : KV4_ERR_LAUNCH;
+}
+
 kv4_status kv4_merge_partials(const float* o_parts_dev, const float* lse_parts_dev, int R,
                               int64_t n_rows, void* out_dev, float* lse_dev,
                               kv4_stream_t stream) {
@@ -439,6 +469,24 @@ kv4_status kv4_fp8_scratch(const uint8_t* pool_dev, int64_t num_slots,
   kv4::GatherArgs a{pool_dev, num_slots,    page_table_dev, pt_stride, topk_idx_dev, K,
                     seq_lens_dev, B,         Sq,             scratch_dev, 1,          dev_err};
   return kv4::launch_fp8_scratch(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? KV4_OK
+             : KV4_ERR_LAUNCH;
+}
+
+kv4_status kv4_fp8_scratch_index(const int32_t* topk_idx_dev, int K, const int32_t* seq_lens_dev,
+                                 int B, int Sq, int32_t* pt_out_dev, int32_t* topk_out_dev,
+                                 int32_t* lens_out_dev, kv4_stream_t stream) {
+  if (B < 0 || Sq < 1 || K < 0) return KV4_ERR_INVALID_ARG;
+  if (K % KV4_PAGE != 0) return KV4_ERR_UNSUPPORTED;
+  if (B == 0 || K == 0) return KV4_OK;
+  if (!topk_idx_dev || !seq_lens_dev || !pt_out_dev || !topk_out_dev || !lens_out_dev)
+    return KV4_ERR_INVALID_ARG;
+  int sms = 0;
+  const kv4_status st = device_info(&sms);
+  if (st != KV4_OK) return st;
+  return kv4::launch_fp8_scratch_index(topk_idx_dev, seq_lens_dev, B, Sq, K, pt_out_dev,
+                                       topk_out_dev, lens_out_dev,
+                                       reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
              ? KV4_OK
              : KV4_ERR_LAUNCH;
 }

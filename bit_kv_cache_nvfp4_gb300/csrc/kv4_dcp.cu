@@ -4,7 +4,11 @@
 // are merged).
 //
 // Ownership (this project's reading; the page names no rule): physical page p
-// of the pool lives on rank p mod world.  A rank's top-k list keeps the
+// of the pool lives on rank p mod world, as page p / world of that rank's own
+// pool, which therefore holds only about 1/world of the pages.  The rank's
+// cache writes go to its local slots (dcp_local_slots_kernel), and its decode
+// reads through a rank-local page table (dcp_local_page_table_kernel) that
+// maps each owned page to its local index.  A rank's top-k list keeps the
 // positions whose page it owns and replaces the others by -1 (masked), so
 // the ranks partition every query's keys.  A position outside [0, L_eff)
 // stays masked everywhere; a position whose page-table entry cannot be read
@@ -44,6 +48,39 @@ __global__ void __launch_bounds__(256) dcp_mask_topk_kernel(const int32_t* topk,
       else if (page % world == rank) keep = idx;
     }
     topk_out[i] = keep;
+  }
+}
+
+// Rank-local page table: entry p (a physical page) becomes p / world where
+// the rank owns it (p >= 0, p % world == rank) and -1 elsewhere -- a
+// position on another rank's page never reaches this rank's decode (its
+// top-k list masks it), and a negative entry stays unreadable, so the rank
+// whose top-k keeps that position (rank 0) reports it.
+__global__ void __launch_bounds__(256) dcp_local_page_table_kernel(const int32_t* page_table,
+                                                                   int64_t n, int world,
+                                                                   int rank, int32_t* out) {
+  grid_dependency_wait();
+  grid_launch_dependents();
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int32_t p = page_table[i];
+    out[i] = (p >= 0 && p % world == rank) ? p / world : -1;
+  }
+}
+
+// Rank-local cache-write slots: global slot s (page s / 64) becomes
+// (page / world) * 64 + s % 64 on the page's owner and -1 (no write)
+// elsewhere; a negative slot stays -1.
+__global__ void __launch_bounds__(256) dcp_local_slots_kernel(const int64_t* slots, int64_t n,
+                                                              int world, int rank,
+                                                              int64_t* out) {
+  grid_dependency_wait();
+  grid_launch_dependents();
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t s = slots[i];
+    const int64_t page = s >= 0 ? s / kPage : -1;
+    out[i] = (page >= 0 && page % world == rank) ? (page / world) * kPage + s % kPage : -1;
   }
 }
 
@@ -104,6 +141,24 @@ cudaError_t launch_dcp_mask_topk(const int32_t* topk, const int32_t* page_table,
   if (blocks > 4096) blocks = 4096;
   return launch_pdl(dcp_mask_topk_kernel, static_cast<unsigned>(blocks), 256, 0, stream, 1, topk,
                     page_table, pt_stride, seq_lens, B, Sq, K, world, rank, topk_out);
+}
+
+cudaError_t launch_dcp_local_page_table(const int32_t* page_table, int64_t n, int world,
+                                        int rank, int32_t* out, cudaStream_t stream) {
+  if (n <= 0) return cudaSuccess;
+  int64_t blocks = (n + 255) / 256;
+  if (blocks > 4096) blocks = 4096;
+  return launch_pdl(dcp_local_page_table_kernel, static_cast<unsigned>(blocks), 256, 0, stream, 1,
+                    page_table, n, world, rank, out);
+}
+
+cudaError_t launch_dcp_local_slots(const int64_t* slots, int64_t n, int world, int rank,
+                                   int64_t* out, cudaStream_t stream) {
+  if (n <= 0) return cudaSuccess;
+  int64_t blocks = (n + 255) / 256;
+  if (blocks > 4096) blocks = 4096;
+  return launch_pdl(dcp_local_slots_kernel, static_cast<unsigned>(blocks), 256, 0, stream, 1,
+                    slots, n, world, rank, out);
 }
 
 cudaError_t launch_merge_partials(const float* o_parts, const float* lse_parts, int R,

@@ -413,6 +413,22 @@ __device__ __forceinline__ void mma_f16kind(uint32_t d_tmem, uint64_t a_desc, ui
       : "memory");
 }
 
+// The same MMA with both descriptors given as a base plus a compile-time
+// offset (16-byte units), added inside the instruction sequence: the issuing
+// thread then holds only the two bases in registers however many MMAs are
+// unrolled.
+template <uint32_t A_OFF, uint32_t B_OFF>
+__device__ __forceinline__ void mma_f16kind_at(uint32_t d_tmem, uint64_t a_base, uint64_t b_base,
+                                               uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 ad, bd;\n\t"
+      "add.s64 ad, %1, %5;\n\tadd.s64 bd, %2, %6;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_base), "l"(b_base), "r"(idesc), "r"(accumulate), "n"(A_OFF), "n"(B_OFF)
+      : "memory");
+}
+
 // Arrive on an mbarrier once every MMA issued so far by this thread is done.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile(

@@ -110,6 +110,10 @@ cudaError_t launch_dcp_mask_topk(const int32_t* topk, const int32_t* page_table,
                                  int64_t pt_stride, const int32_t* seq_lens, int B, int Sq,
                                  int K, int world, int rank, int32_t* topk_out,
                                  cudaStream_t stream);
+cudaError_t launch_dcp_local_page_table(const int32_t* page_table, int64_t n, int world,
+                                        int rank, int32_t* out, cudaStream_t stream);
+cudaError_t launch_dcp_local_slots(const int64_t* slots, int64_t n, int world, int rank,
+                                   int64_t* out, cudaStream_t stream);
 cudaError_t launch_merge_partials(const float* o_parts, const float* lse_parts, int R,
                                   int64_t n_rows, void* out_bf16, float* lse,
                                   cudaStream_t stream);
@@ -118,6 +122,9 @@ cudaError_t launch_debug_gather(const GatherArgs& a, cudaStream_t stream);
 // The FP8 scratch copy of the rows the keys select: a.rows is uint8
 // [B*Sq*K, 576] (E4M3 of the dequantized NVFP4 values; masked keys 0).
 cudaError_t launch_fp8_scratch(const GatherArgs& a, cudaStream_t stream);
+cudaError_t launch_fp8_scratch_index(const int32_t* topk, const int32_t* seq_lens, int B, int Sq,
+                                     int K, int32_t* pt_out, int32_t* topk_out,
+                                     int32_t* lens_out, cudaStream_t stream);
 size_t decode_smem_bytes(int HG, int fmt);
 // How many clusters of `splits` blocks of the HG variant can be resident at
 // once on this device (0: such clusters cannot run).  A unit split in two

@@ -20,7 +20,7 @@
 //   a4     and dequantizes them straight into the 128-byte-swizzled f16
 //          operand tile in shared memory (576 columns per key; E2M1 x E4M3
 //          and E4M3 values are exact in f16) in three passes -- latent
-//          slabs {0,1,4,5}, latent slabs {2,3,6,7}, rope -- each into the
+//          slabs 0-3, latent slabs 4-7, rope -- each into the
 //          slabs that the previous tile's PV has already released; q is
 //          converted to f16 with a per-head power-of-two scale folded into
 //          the score scale
@@ -50,6 +50,7 @@
 #include <math.h>
 
 #include <type_traits>
+#include <utility>
 
 namespace kv4 {
 namespace {
@@ -72,6 +73,13 @@ static_assert(2 * kComputeRegs + kIssueRegs <= 3 * kLaunchRegs, "register split 
 #endif
 constexpr int kPvIssuers = KV4_PV_ISSUERS;    // 2: slabs 0,2 are released half way through PV
 static_assert(kPvIssuers == 2 || kPvIssuers == 4, "PV issuers");
+// QK issuers, each accumulating its share of the 36 k-steps into its own
+// partial S^T sum (which the softmax adds up: fewer sums, fewer TMEM reads)
+#ifndef KV4_QK_ISSUERS
+#define KV4_QK_ISSUERS 4
+#endif
+constexpr int kQkIssuers = KV4_QK_ISSUERS;
+static_assert(kQkIssuers == 1 || kQkIssuers == 2 || kQkIssuers == 4, "QK issuers");
 constexpr int kBarCompute = 3;            // named barrier of the 256 compute threads (1, 2: softmax groups)
 constexpr float kRaiseThreshold = 8.0f;   // log2 units: p <= 256 between raises
 
@@ -208,12 +216,27 @@ __device__ __forceinline__ void tmem_load_cols(uint32_t taddr, float (&x)[N]) {
   }
 }
 
-// Scores: the sum of the four partial S^T accumulators (columns c + i gap),
-// added as (S0 + S1) + (S2 + S3).
+// Scores: the sum of the kQkIssuers partial S^T accumulators (columns
+// c + i gap), added as (S0 + S1) + (S2 + S3).
 template <int N>
 __device__ __forceinline__ void load_scores(uint32_t taddr, uint32_t gap, float (&x)[N]) {
   __syncwarp();
-  if constexpr (N == 32) {
+  if constexpr (kQkIssuers == 1) {
+    tmem_load_cols<N>(taddr, x);
+  } else if constexpr (kQkIssuers == 2) {
+    if constexpr (N == 32) {
+      uint32_t va[32], vb[32];
+      tmem_ld32x2_sync(taddr, taddr + gap, va, vb);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(va[j]) + __uint_as_float(vb[j]);
+    } else {
+      float y[N];
+      tmem_load_cols<N>(taddr, x);
+      tmem_load_cols<N>(taddr + gap, y);
+#pragma unroll
+      for (int j = 0; j < N; ++j) x[j] += y[j];
+    }
+  } else if constexpr (N == 32) {
     uint32_t va[32], vb[32];
     tmem_ld32x2_sync(taddr, taddr + gap, va, vb);
 #pragma unroll
@@ -337,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
   constexpr int kQThread = 32 * (kComputeWarps + 1);   // inits the barriers, copies Q
   if (warp == kComputeWarps) tmem_alloc(smem_addr(tmem_slot), L::tmem_cols);
   if (tid == kQThread) {
-    mbar_init(bar_qk, 4);
+    mbar_init(bar_qk, kQkIssuers);
     for (int p = 0; p < 4; ++p) mbar_init(bar_pv0 + 8 * p, 1);
     for (int p = 0; p < 3; ++p) mbar_init(bar_part0 + 8 * p, kComputeWarps);
     mbar_init(bar_p, 1);
@@ -454,8 +477,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
     // ==== MMA issue warpgroup: lane 0 of each of its warps is an issuer ====
     // A thread's MMAs run one after another, each fetching fresh operands,
     // so QK is spread over four issuers (four partial sums of S^T) and PV
-    // over two (issuer 0: O slabs 0 then 1, issuer 1: slabs 2 then 3, so
-    // that slabs 0 and 2 are released half way through).
+    // over two (issuer 0: O slabs 0 then 2, issuer 1: slabs 1 then 3, so
+    // that slabs 0 and 1 -- latent columns 0-255 -- are released half way
+    // through).
     setmaxnreg_dec<kIssueRegs>();
     if (lane == 0) {
       const int qi = warp - kComputeWarps;         // issuer 0..3
@@ -466,38 +490,55 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
       const uint64_t desc_v = smem_desc(kv_addr, kChunkBytes, 1024, kSwizzle128);    // MN-major A
       const uint64_t desc_p = smem_desc(kv_addr + 8 * kChunkBytes, 8192, L::p_atom_bytes,
                                         L::p_swizzle_mode);                         // MN-major B
-      // QK k-steps [k0, k0 + n) (16 columns each; chunk = k-step / 4) into
-      // this issuer's partial sum; 'first' starts the sum.
-      auto issue_qk = [&](const int k0, const int n, const bool first) {
-        constexpr uint32_t idesc = idesc_f16(128, HG, false, false);
-#pragma unroll 1
-        for (int j = 0; j < n; ++j) {
-          const uint32_t kk = k0 + j;
-          const uint32_t c = kk >> 2, sub = kk & 3;
-          mma_f16kind(tmem + L::col_s + qi * HG, desc_k + ((c * kChunkBytes + sub * 32) >> 4),
-                      desc_q + ((c * (HG * 128) + sub * 32) >> 4), idesc,
-                      (first && j == 0) ? 0u : 1u);
-        }
-      };
-      // latent chunk of each pass for this issuer: pass a writes chunks
-      // 0, 1, 4, 5 and pass b chunks 2, 3, 6, 7
-      const int chunk_a = (qi & 1) + 4 * (qi >> 1);
-      const int chunk_b = chunk_a + 2;
-      for (int it = 0; it < my_tiles; ++it) {
-        const uint32_t par = it & 1;
-        // a5: each part of S^T = K_tile . Q^T as soon as the compute warps wrote it
+      // a5 for issuer QI: its share of S^T = K_tile . Q^T, each part as soon as
+      // the compute warps wrote it.  Pass a writes latent chunks (64 columns =
+      // 4 k-steps of 16) 0-3 and pass b chunks 4-7; issuer QI
+      // takes kCpi of each pass's four, and kRpi of the four rope k-steps
+      // (chunk 8).  Every operand offset is a compile-time constant.
+      constexpr uint32_t idesc_qk = idesc_f16(128, HG, false, false);
+      constexpr int kCpi = 4 / kQkIssuers;
+      constexpr int kRpi = 4 / kQkIssuers;
+      const uint32_t d_s = tmem + L::col_s + qi * HG;
+      auto issue_qk = [&](auto qi_const, const uint32_t par) {
+        constexpr int QI = decltype(qi_const)::value;
+        auto chunk = [&](auto c_const, const bool first) {
+          constexpr int c = decltype(c_const)::value;
+          [&]<int... SUB>(std::integer_sequence<int, SUB...>) {
+            ((mma_f16kind_at<((c * kChunkBytes + SUB * 32) >> 4), ((c * (HG * 128) + SUB * 32) >> 4)>(
+                 d_s, desc_k, desc_q, idesc_qk, (first && SUB == 0) ? 0u : 1u)), ...);
+          }(std::make_integer_sequence<int, 4>{});
+        };
         wait(bar_part0, par);
         tc_fence_after_sync();
-        issue_qk(4 * chunk_a, 4, true);
+        [&]<int... I>(std::integer_sequence<int, I...>) {
+          (chunk(std::integral_constant<int, QI * kCpi + I>{}, I == 0), ...);
+        }(std::make_integer_sequence<int, kCpi>{});
         wait(bar_part0 + 8, par);
         tc_fence_after_sync();
-        issue_qk(4 * chunk_b, 4, false);
+        [&]<int... I>(std::integer_sequence<int, I...>) {
+          (chunk(std::integral_constant<int, 4 + QI * kCpi + I>{}, false), ...);
+        }(std::make_integer_sequence<int, kCpi>{});
         if constexpr (ROPE) {
           wait(bar_part0 + 16, par);
           tc_fence_after_sync();
-          issue_qk(32 + qi, 1, false);               // rope: one 16-column step each
+          [&]<int... J>(std::integer_sequence<int, J...>) {
+            ((mma_f16kind_at<((8 * kChunkBytes + (QI * kRpi + J) * 32) >> 4),
+                             ((8 * (HG * 128) + (QI * kRpi + J) * 32) >> 4)>(
+                 d_s, desc_k, desc_q, idesc_qk, 1u)), ...);
+          }(std::make_integer_sequence<int, kRpi>{});
         }
         mma_commit(bar_qk);
+      };
+      for (int it = 0; it < my_tiles; ++it) {
+        const uint32_t par = it & 1;
+        if (qi == 0) issue_qk(std::integral_constant<int, 0>{}, par);
+        if constexpr (kQkIssuers >= 2) {
+          if (qi == 1) issue_qk(std::integral_constant<int, 1>{}, par);
+        }
+        if constexpr (kQkIssuers == 4) {
+          if (qi == 2) issue_qk(std::integral_constant<int, 2>{}, par);
+          if (qi == 3) issue_qk(std::integral_constant<int, 3>{}, par);
+        }
         if (qi >= kPvIssuers) continue;
         // a7: O^T += V^T . P^T, 4 / kPvIssuers O slabs (128 columns each) per
         // issuer, each committed on its own so that the next tile's
@@ -508,7 +549,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
         constexpr int kSlabsPerIssuer = 4 / kPvIssuers;
 #pragma unroll 1
         for (int j = 0; j < kSlabsPerIssuer; ++j) {
-          const int mb = kSlabsPerIssuer * qi + j;
+          const int mb = qi + kPvIssuers * j;
 #pragma unroll 1
           for (int ks = 0; ks < 8; ++ks)
             mma_f16kind(tmem + L::col_o + mb * HG,
@@ -545,9 +586,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
     // Rows of the next tile travel in registers: warp w holds rows 16w..16w+15
     // as three 32-bit words per lane -- latent word wa(l), latent word wb(l),
     // and word 64 + l (lanes 0..7: scales, 8..23: rope, which only 352-byte
-    // rows have) -- where pass A
-    // covers slabs {0,1,4,5} and pass B slabs {2,3,6,7}:
-    //   wa(l) = l < 16 ? l : l + 16,   wb(l) = wa(l) + 16.
+    // rows have) -- where pass A covers slabs 0-3 and pass B slabs 4-7, each
+    // as one contiguous 128-byte run of the row:
+    //   wa(l) = l,   wb(l) = 32 + l.
     // Each group is reloaded for the next tile right after the pass that
     // consumed it, so the gather is spread over the whole tile.
     // An NVFP4 row's latent word w (8 codes) and an FP8 row's 8-byte latent
@@ -557,8 +598,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
     using LatWord = std::conditional_t<FP8, uint2, uint32_t>;
     constexpr int kExtraWord0 = FP8 ? 120 : 64;
     const bool extra_lane = FP8 ? (lane >= 8 && lane < 24) : (lane < (ROPE ? 24 : 8));
-    const int word_a = lane < 16 ? lane : lane + 16;
-    const int word_b = word_a + 16;
+    const int word_a = lane;
+    const int word_b = lane + 32;
     LatWord wa[16], wb[16];
     uint32_t wex[16];
     // one word of each of this warp's 16 rows of the tile whose slots are
@@ -652,10 +693,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
 
       // ---- a3/a4 in three passes, each into slabs that the previous tile's
       // PV has released; QK starts on each part as soon as all warps wrote it.
-      // pass A: slabs 0,1 and 4,5 (PV slabs 0 and 2, which are issued first)
+      // pass A: slabs 0-3 (O slabs 0 and 1, which PV runs first)
       if (it > 0) {
         wait(bar_pv0, par ^ 1);
-        wait(bar_pv0 + 16, par ^ 1);
+        wait(bar_pv0 + 8, par ^ 1);
         __syncwarp();
         tc_fence_after_sync();
       }
@@ -667,9 +708,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_part0);
       if (it + 1 < my_tiles) load_latent(wa, next_slots, word_a);        // next tile
-      // pass B: slabs 2,3 and 6,7 (PV slabs 1 and 3; PV is then complete)
+      // pass B: slabs 4-7 (O slabs 2 and 3; PV is then complete)
       if (it > 0) {
-        wait(bar_pv0 + 8, par ^ 1);
+        wait(bar_pv0 + 16, par ^ 1);
         wait(bar_pv0 + 24, par ^ 1);
         __syncwarp();
         tc_fence_after_sync();
@@ -1125,6 +1166,33 @@ __global__ void __launch_bounds__(256) fp8_scratch_kernel(GatherArgs a) {
   if (lane >= 8 && lane < 24) *reinterpret_cast<uint32_t*>(out + 512 + 4 * (lane - 8)) = rope;
 }
 
+// The scratch path's indexing: for n = b*Sq + s, page-table row n holds the
+// pages n*(K/64) .. n*(K/64) + K/64 - 1 of the scratch buffer, and the top-k
+// list of one-token request n keeps position k where key k of the original
+// query is valid (0 <= topk[b,s,k] < L_eff) and -1 where it is masked; every
+// such request has length K.  One thread per top-k entry.
+__global__ void __launch_bounds__(256) fp8_scratch_index_kernel(const int32_t* topk,
+                                                                const int32_t* seq_lens, int B,
+                                                                int Sq, int K, int32_t* pt_out,
+                                                                int32_t* topk_out,
+                                                                int32_t* lens_out) {
+  grid_dependency_wait();
+  grid_launch_dependents();
+  const int64_t n_keys = static_cast<int64_t>(B) * Sq * K;
+  const int pages = K / kPage;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n_keys;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t n = i / K;
+    const int k = static_cast<int>(i % K);
+    const int b = static_cast<int>(n / Sq), s = static_cast<int>(n % Sq);
+    const int64_t l_eff = static_cast<int64_t>(seq_lens[b]) - (Sq - 1 - s);
+    const int32_t idx = topk[i];
+    topk_out[i] = (idx >= 0 && idx < l_eff) ? k : -1;
+    if (k < pages) pt_out[n * pages + k] = static_cast<int32_t>(n * pages + k);
+    if (k == 0) lens_out[n] = K;
+  }
+}
+
 template <int HG, int FMT>
 cudaError_t configure_decode() {
   static cudaError_t state = cudaErrorNotReady;   // per process; attributes are per kernel
@@ -1253,6 +1321,17 @@ cudaError_t launch_fp8_scratch(const GatherArgs& a, cudaStream_t stream) {
   if (rows <= 0) return cudaSuccess;
   return launch_pdl(fp8_scratch_kernel, static_cast<unsigned>((rows + 7) / 8), 256, 0, stream, 1,
                     a);
+}
+
+cudaError_t launch_fp8_scratch_index(const int32_t* topk, const int32_t* seq_lens, int B, int Sq,
+                                     int K, int32_t* pt_out, int32_t* topk_out,
+                                     int32_t* lens_out, cudaStream_t stream) {
+  const int64_t n = static_cast<int64_t>(B) * Sq * K;
+  if (n <= 0) return cudaSuccess;
+  int64_t blocks = (n + 255) / 256;
+  if (blocks > 4096) blocks = 4096;
+  return launch_pdl(fp8_scratch_index_kernel, static_cast<unsigned>(blocks), 256, 0, stream, 1,
+                    topk, seq_lens, B, Sq, K, pt_out, topk_out, lens_out);
 }
 
 cudaError_t launch_debug_gather(const GatherArgs& a, cudaStream_t stream) {

@@ -238,17 +238,79 @@ kv4_status kv4_debug_gather_dequant_latent(const uint8_t* pool_dev, int64_t num_
                                            kv4_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * FP8 comparison paths.
+ * Source: README "4-bit KV cache", kv4mla bullet (the NVFP4 decode against
+ * the 576-byte FP8 row it replaces, and against an "FP8 scratch" path that
+ * first copies the selected rows, dequantized to FP8, into HBM).
+ *   kv4_quantize_write_fp8     the FP8 row: 576 E4M3 bytes, latent [0,512)
+ *                              then rope [512,576), each x rounded to
+ *                              nearest even and saturated at 448, no scale;
+ *                              pool uint8 [num_slots, 576]; otherwise as
+ *                              kv4_quantize_write
+ *   kv4_decode_plan_fp8 /
+ *   kv4_sparse_mla_decode_fp8  the decode over a pool of 576-byte FP8 rows:
+ *                              arguments, layouts, workspace and errors as
+ *                              kv4_sparse_mla_decode
+ *   kv4_fp8_scratch            for every (b, s, k) the NVFP4 row key k
+ *                              selects, dequantized as the decode does and
+ *                              cast to E4M3, into row (b*Sq + s)*K + k of
+ *                              scratch_dev uint8 [B*Sq*K, 576] (16-byte
+ *                              aligned); masked keys give zero rows; index
+ *                              errors as in the decode
+ *   kv4_fp8_scratch_index      the indexing that makes that scratch buffer
+ *                              look like a paged pool, for a decode of
+ *                              B*Sq one-token requests: pt_out int32
+ *                              [B*Sq, K/64] (entry (n, p) = n*(K/64) + p),
+ *                              topk_out int32 [B*Sq, 1, K] (k where key k
+ *                              of the original query is valid, -1 where it
+ *                              is masked), lens_out int32 [B*Sq] (= K).  K
+ *                              must be a multiple of 64 (else
+ *                              KV4_ERR_UNSUPPORTED).
+ * ------------------------------------------------------------------------- */
+kv4_status kv4_quantize_write_fp8(const void* latent_dev, int64_t latent_row_stride,
+                                  const void* rope_dev, int64_t rope_row_stride,
+                                  const int64_t* slot_mapping_dev, int64_t n_tokens,
+                                  uint8_t* pool_dev, int64_t num_slots, int32_t* dev_err,
+                                  kv4_stream_t stream);
+kv4_status kv4_decode_plan_fp8(int B, int Sq, int H, int K, int force_splits, int* splits,
+                               size_t* workspace_bytes);
+kv4_status kv4_sparse_mla_decode_fp8(const void* q_dev, const uint8_t* pool_dev,
+                                     int64_t num_slots, const int32_t* page_table_dev,
+                                     int64_t pt_stride, int page_size,
+                                     const int32_t* topk_idx_dev, int K,
+                                     const int32_t* seq_lens_dev, int B, int Sq, int H,
+                                     float sm_scale, void* out_dev, float* lse_dev,
+                                     void* workspace_dev, size_t workspace_bytes,
+                                     int force_splits, int32_t* dev_err, kv4_stream_t stream);
+kv4_status kv4_fp8_scratch(const uint8_t* pool_dev, int64_t num_slots,
+                           const int32_t* page_table_dev, int64_t pt_stride, int page_size,
+                           const int32_t* topk_idx_dev, int K, const int32_t* seq_lens_dev,
+                           int B, int Sq, uint8_t* scratch_dev, int32_t* dev_err,
+                           kv4_stream_t stream);
+kv4_status kv4_fp8_scratch_index(const int32_t* topk_idx_dev, int K, const int32_t* seq_lens_dev,
+                                 int B, int Sq, int32_t* pt_out_dev, int32_t* topk_out_dev,
+                                 int32_t* lens_out_dev, kv4_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * Decode-context parallelism (DCP).
  * Source: README "Parallelism and disaggregation" (ranks attend over their
  * part of the context and merge (o, lse)).  Ownership rule (this project's
- * reading): physical page p lives on rank p mod world.  One decode step on
- * `world` ranks is:
+ * reading): physical page p lives on rank p mod world, as page p / world of
+ * that rank's own pool -- a rank holds only its pages, about 1/world of the
+ * cache.  The cache write of a token goes to its owner's pool at the local
+ * slot kv4_dcp_local_slots gives (slot_out = (page / world) * 64 + slot % 64
+ * on the owner, -1 -- no write -- elsewhere; int64 [N] in and out).  The
+ * decode reads through the rank-local page table of kv4_dcp_local_page_table
+ * (pt_local [B, pt_stride] int32: p / world where the rank owns page p,
+ * -1 elsewhere and for negative entries).  One decode step on `world` ranks
+ * is:
  *   1. kv4_dcp_mask_topk on every rank: topk_out [B,Sq,K] int32 keeps the
  *      positions whose page the rank owns and is -1 elsewhere.  Positions
  *      outside [0, L_eff) are -1 on every rank; a position whose page entry
  *      cannot be read (page index >= pt_stride or a negative entry) is kept
  *      on rank 0 only, whose decode then reports KV4_DEV_BAD_PAGE.
- *   2. kv4_sparse_mla_decode_partial on every rank with its topk_out: the
+ *   2. kv4_sparse_mla_decode_partial on every rank with its own pool, its
+ *      pt_local and its topk_out: the
  *      same decode as kv4_sparse_mla_decode (same arguments, workspace and
  *      errors), except that o_dev is fp32 [B,Sq,H,512] -- the normalized
  *      weighted sum over the rank's keys, not rounded to bf16 -- and lse_dev
@@ -265,6 +327,11 @@ kv4_status kv4_dcp_mask_topk(const int32_t* topk_idx_dev, const int32_t* page_ta
                              int64_t pt_stride, const int32_t* seq_lens_dev, int B, int Sq,
                              int K, int world, int rank, int32_t* topk_out_dev,
                              kv4_stream_t stream);
+kv4_status kv4_dcp_local_page_table(const int32_t* page_table_dev, int64_t pt_stride, int B,
+                                   int world, int rank, int32_t* pt_local_dev,
+                                   kv4_stream_t stream);
+kv4_status kv4_dcp_local_slots(const int64_t* slot_mapping_dev, int64_t n_tokens, int world,
+                               int rank, int64_t* slots_out_dev, kv4_stream_t stream);
 kv4_status kv4_sparse_mla_decode_partial(const void* q_dev, const uint8_t* pool_dev,
                                          int64_t num_slots, const int32_t* page_table_dev,
                                          int64_t pt_stride, int page_size,

@@ -29,6 +29,21 @@ def test_exports_every_declared_symbol(lib):
     assert not missing, missing
 
 
+def test_header_declares_every_exported_symbol(lib):
+    """Every kv4_* function the library exports is declared in the header."""
+    import shutil
+    import subprocess
+    nm = shutil.which("nm")
+    if nm is None:
+        pytest.skip("nm not available")
+    from bit_kv_cache_nvfp4_gb300 import build
+    out = subprocess.run([nm, "-D", "--defined-only", build.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout.split()
+    exported = sorted({w for w in out if re.fullmatch(r"kv4_[a-z0-9_]+", w)})
+    names = set(declared(os.path.join(ROOT, "include", "kv4mla.h")))
+    assert exported and not [n for n in exported if n not in names]
+
+
 def test_oracle_exports_every_declared_symbol():
     import oracle
     olib = ctypes.CDLL(oracle.build())

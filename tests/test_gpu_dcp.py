@@ -1,17 +1,22 @@
 """Decode-context parallelism kernels on one GPU, against the CPU oracle.
 
 The ranks are emulated one after another on the same GPU (nothing waits on
-another rank): for R ranks, kv4_dcp_mask_topk gives every rank its keys,
+another rank).  For R ranks, every rank holds only its own pages: its pool
+has the pages p with p % R == rank, as page p // R, written through
+kv4_dcp_local_slots; kv4_dcp_mask_topk gives it its keys,
+kv4_dcp_local_page_table its page table over that pool,
 kv4_sparse_mla_decode_partial its fp32 (o, lse), and kv4_merge_partials
 combines the stacked partials -- which must agree with the oracle's decode
-over all keys within the decode tolerances.  The mask is checked bit for bit
-against the ownership rule written out in numpy."""
+over all keys within the decode tolerances.  The mask, the local page table
+and the local slots are checked bit for bit against the rules written out in
+numpy."""
 import numpy as np
 import pytest
 import torch
 
-from gpu_common import assert_close, device_inputs, gpu_pool, need_gpu, oracle_decode, workload
-from test_dcp_cpu import owned_topk
+from gpu_common import assert_close, device_inputs, need_gpu, oracle_decode, workload
+from bit_kv_cache_nvfp4_gb300 import workloads as wl
+from test_dcp_cpu import local_page_table, local_slots, owned_topk
 
 pytestmark = pytest.mark.gpu
 
@@ -40,21 +45,61 @@ def test_mask_matches_ownership_rule(world):
     assert np.array_equal(seen, valid.astype(np.int64))    # a partition of the valid keys
 
 
+@pytest.mark.parametrize("world", [2, 3, 8])
+def test_local_addressing_matches_rule(world):
+    need_gpu()
+    w = workload("decode")
+    pt = w.page_table.clone()
+    pt[0, 1] = -3                                        # a negative entry stays unreadable
+    slots = torch.cat([wl.token_slots(w, b, torch.arange(0, int(w.seq_lens[b]), 997))
+                       for b in range(w.B)])
+    slots[::11] = -1                                     # skipped tokens stay skipped
+    for r in range(world):
+        got_pt = kv().dcp_local_page_table(pt.cuda(), world, r).cpu().numpy()
+        assert np.array_equal(got_pt, local_page_table(pt.numpy(), world, r)), r
+        got_sl = kv().dcp_local_slots(slots.cuda(), world, r).cpu().numpy()
+        assert np.array_equal(got_sl, local_slots(slots.numpy(), world, r)), r
+
+
+def local_pool(w, world, rank, dev):
+    """Rank `rank`'s own pool: the pages it owns, written at local slots."""
+    m = kv()
+    n_pages = m.dcp_local_pages(w.num_slots // 64, world, rank)
+    pool = torch.zeros((n_pages * 64, 352), dtype=torch.uint8, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    for lat, rope, slots in wl.iter_pool_chunks(w, chunk=1 << 18, device=dev):
+        m.quantize_write(lat, rope, m.dcp_local_slots(slots, world, rank), pool, err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    return pool
+
+
 @pytest.mark.parametrize("name,world", [("decode", 1), ("decode", 2), ("decode", 4),
                                         ("decode", 8), ("long", 8)])
 def test_emulated_ranks_match_oracle(name, world):
     need_gpu()
     w = workload(name)
-    pool = gpu_pool(w)
     q, pt, topk, lens = device_inputs(w)
     m = kv()
     parts_o, parts_l = [], []
+    pages = []
     for r in range(world):
+        pool = local_pool(w, world, r, q.device)          # this rank's pages only
+        pages.append(pool.shape[0] // 64)
         mine = m.dcp_mask_topk(topk, pt, lens, world, r)
-        o, l = m.sparse_mla_decode_partial(q, pool, pt, mine, lens, w.sm_scale)
+        pt_local = m.dcp_local_page_table(pt, world, r)
+        err = torch.zeros(1, dtype=torch.int32, device=q.device)
+        o, l = m.sparse_mla_decode_partial(q, pool, pt_local, mine, lens, w.sm_scale,
+                                           dev_err=err)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
         assert o.dtype == torch.float32
         parts_o.append(o)
         parts_l.append(l)
+        del pool
+    # the ranks' pools partition the cache's pages, about 1/world each
+    assert sum(pages) == w.num_slots // 64
+    assert max(pages) == -(-(w.num_slots // 64) // world)
     out, lse = m.merge_partials(torch.stack(parts_o), torch.stack(parts_l))
     torch.cuda.synchronize()
     req = [0, 7, 15] if name == "decode" else [0, 41]
