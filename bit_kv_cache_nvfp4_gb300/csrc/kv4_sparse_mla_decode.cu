@@ -529,6 +529,27 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
         }
         mma_commit(bar_qk);
       };
+      // a7 for issuer QI: O slabs QI, QI + kPvIssuers, ... (128 latent
+      // columns each, M = 128) += V^T . P^T over the tile's 128 keys (8
+      // k-steps of 16 keys), every operand offset a compile-time constant;
+      // each slab is committed on its own barrier.
+      constexpr uint32_t idesc_pv = idesc_f16(128, HG, true, true);
+      constexpr int kSlabsPerIssuer = 4 / kPvIssuers;
+      auto issue_pv = [&](auto qi_const, const bool acc_prev) {
+        constexpr int QI = decltype(qi_const)::value;
+        [&]<int... J>(std::integer_sequence<int, J...>) {
+          ([&] {
+            constexpr int mb = QI + kPvIssuers * J;
+            [&]<int... KS>(std::integer_sequence<int, KS...>) {
+              ((mma_f16kind_at<(((2 * mb) * kChunkBytes + (2 * KS) * 1024) >> 4),
+                               (((2 * KS) * L::p_atom_bytes) >> 4)>(
+                   tmem + L::col_o + mb * HG, desc_v, desc_p, idesc_pv,
+                   (acc_prev || KS > 0) ? 1u : 0u)), ...);
+            }(std::make_integer_sequence<int, 8>{});
+            mma_commit(bar_pv0 + 8 * mb);
+          }(), ...);
+        }(std::make_integer_sequence<int, kSlabsPerIssuer>{});
+      };
       for (int it = 0; it < my_tiles; ++it) {
         const uint32_t par = it & 1;
         if (qi == 0) issue_qk(std::integral_constant<int, 0>{}, par);
@@ -545,18 +566,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
         // dequantization can reuse its shared memory as early as possible
         wait(bar_p, par);
         tc_fence_after_sync();
-        constexpr uint32_t idesc = idesc_f16(128, HG, true, true);
-        constexpr int kSlabsPerIssuer = 4 / kPvIssuers;
-#pragma unroll 1
-        for (int j = 0; j < kSlabsPerIssuer; ++j) {
-          const int mb = qi + kPvIssuers * j;
-#pragma unroll 1
-          for (int ks = 0; ks < 8; ++ks)
-            mma_f16kind(tmem + L::col_o + mb * HG,
-                        desc_v + (((2 * mb) * kChunkBytes + (2 * ks) * 1024) >> 4),
-                        desc_p + (((2 * ks) * L::p_atom_bytes) >> 4), idesc,
-                        (it > 0 || ks > 0) ? 1u : 0u);
-          mma_commit(bar_pv0 + 8 * mb);
+        if (qi == 0) issue_pv(std::integral_constant<int, 0>{}, it > 0);
+        if (qi == 1) issue_pv(std::integral_constant<int, 1>{}, it > 0);
+        if constexpr (kPvIssuers == 4) {
+          if (qi == 2) issue_pv(std::integral_constant<int, 2>{}, it > 0);
+          if (qi == 3) issue_pv(std::integral_constant<int, 3>{}, it > 0);
         }
       }
     }
@@ -589,8 +603,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
     // rows have) -- where pass A covers slabs 0-3 and pass B slabs 4-7, each
     // as one contiguous 128-byte run of the row:
     //   wa(l) = l,   wb(l) = 32 + l.
-    // Each group is reloaded for the next tile right after the pass that
-    // consumed it, so the gather is spread over the whole tile.
+    // All three groups are reloaded for the next tile after the last pass,
+    // while QK finishes.
     // An NVFP4 row's latent word w (8 codes) and an FP8 row's 8-byte latent
     // unit w (8 E4M3 values) both become the f16 unit of columns 8w..8w+7.
     // The extra word of lane l is word 64 + l of an NVFP4 row (scales, rope)
@@ -707,7 +721,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
       fence_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_part0);
-      if (it + 1 < my_tiles) load_latent(wa, next_slots, word_a);        // next tile
       // pass B: slabs 4-7 (O slabs 2 and 3; PV is then complete)
       if (it > 0) {
         wait(bar_pv0 + 16, par ^ 1);
@@ -722,7 +735,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
       fence_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_part0 + 8);
-      if (it + 1 < my_tiles) load_latent(wb, next_slots, word_b);
       if constexpr (ROPE) {
         // pass C: rope -> slab 8 (the previous tile's P lived there; PV is done)
         if (lane >= 8 && lane < 24) {
@@ -734,7 +746,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_part0 + 16);
       }
-      if (it + 1 < my_tiles) load_extra(wex, next_slots);
+      // the next tile's rows, gathered while QK finishes (the passes above
+      // run back to back, so that QK receives its parts as early as possible)
+      if (it + 1 < my_tiles) {
+        load_latent(wa, next_slots, word_a);
+        load_latent(wb, next_slots, word_b);
+        load_extra(wex, next_slots);
+      }
 
       // ---- a2, second step: page-table entry of the key two tiles ahead
       if (resolve_ahead) {
