@@ -195,6 +195,13 @@ __device__ __forceinline__ uint32_t cluster_map(uint32_t addr, uint32_t rank) {
   return r;
 }
 
+// Arrive (release, cluster scope) on an mbarrier of another block of the
+// cluster; `bar_cluster` is its shared::cluster address (cluster_map).
+__device__ __forceinline__ void mbar_remote_arrive(uint32_t bar_cluster) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster)
+               : "memory");
+}
+
 // Arrive on a local mbarrier and announce `bytes` of asynchronous copies
 // that will complete on it.
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {

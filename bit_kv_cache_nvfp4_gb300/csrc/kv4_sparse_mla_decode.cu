@@ -61,6 +61,12 @@ namespace {
 // Registers are moved from the issue warpgroup to the compute warpgroups
 // with setmaxnreg; per SM sub-partition (one warp of each warpgroup) that is
 // 2 x 232 + 40 = 504 of the 3 x 168 the block is launched with.
+#ifndef KV4_PRO_PREFETCH
+#define KV4_PRO_PREFETCH 1
+#endif
+#ifndef KV4_TILE_PREFETCH
+#define KV4_TILE_PREFETCH 1
+#endif
 constexpr int kComputeWarps = 8;
 constexpr int kComputeThreads = 32 * kComputeWarps;
 constexpr int kThreads = kComputeThreads + 128;
@@ -100,6 +106,7 @@ struct Layout {
   // control block
   static constexpr uint32_t bar_off = ctl_off;                        // uint64 x 12
   static constexpr uint32_t tmem_off = ctl_off + 96;                  // uint32
+  static constexpr uint32_t done_off = ctl_off + 104;                 // uint64: merge barrier
   static constexpr uint32_t slot_off = ctl_off + 112;                 // int32 [3][128]
   static constexpr uint32_t mref_off = slot_off + 3 * 128 * 4;        // float [HG]
   static constexpr uint32_t alpha_off = mref_off + HG * 4;            // float [HG]
@@ -117,9 +124,8 @@ struct Layout {
   // (free after the last QK): half of HG x 512 fp32 fits in Q's 8 or 9 slabs
   // of HG x 128 B.
   static_assert(HG * kLatent * 4 / 2 <= q_bytes, "peer slice must fit in the Q region");
-  // the merge stages the outgoing half (fp32) and then its own merged half
-  // (bf16 or fp32) in the K/V region
-  static_assert(HG * kLatent * 4 / 2 * 2 <= kv_bytes, "merge staging fits the K/V region");
+  // the merge stages the outgoing half (fp32) in the K/V region
+  static_assert(HG * kLatent * 4 / 2 <= kv_bytes, "merge staging fits the K/V region");
   static_assert(xlse_off % 16 == 0 && xlse_in_off % 16 == 0, "bulk-copy operands are 16-byte aligned");
   static constexpr uint32_t smem_bytes = end + 1024;                  // + alignment slack
   // tensor memory: O^T slabs at columns [0, 4HG); S^T as four partial sums
@@ -343,6 +349,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
   const uint32_t bar_fault = bars + 72;
   const uint32_t bar_merge = bars + 80;           // cluster merge: the peer's data arrived
   const uint32_t bar_q = bars + 88;               // Q copied into the K/V region
+  // cluster merge: the peer has received this block's outgoing half (so the
+  // bulk copies that read it from this block's shared memory are done)
+  const uint32_t bar_done = smem_addr(smem + L::done_off);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::tmem_off);
   int32_t* slot_s = reinterpret_cast<int32_t*>(smem + L::slot_off);
   float* m_ref = reinterpret_cast<float*>(smem + L::mref_off);
@@ -367,6 +376,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
     mbar_init(bar_fault, 1);
     mbar_init(bar_merge, 1);
     mbar_init(bar_q, 1);
+    mbar_init(bar_done, 1);
     fence_mbar_init();
   }
   // Everything above touches no global memory and may overlap the end of
@@ -408,7 +418,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
       const int32_t pi = slot_page_index(idx, l_eff, a.pt_stride, a.dev_err);
       const int32_t sl = pi >= 0 ? slot_from_page(__ldg(pt_row + pi), idx, a.num_slots, a.dev_err) : -1;
       slot_s[pro_t * 128 + pro_r] = sl;
-      if (sl >= 0) {
+      if (KV4_PRO_PREFETCH && sl >= 0) {
         const uint8_t* row = a.pool + static_cast<int64_t>(sl) * L::row_bytes;
         prefetch_l2_line(row);
         prefetch_l2_line(row + 128);
@@ -575,10 +585,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
       }
     }
     __syncwarp();
-    if (a.cluster_merge) {                     // the compute warps' merge barriers
-      cluster_sync();
-      cluster_sync();
-    }
+    if (a.cluster_merge) cluster_sync();       // the compute warps' merge barrier
   } else {
     // ==== compute warpgroups (warps 0..7) ====
     setmaxnreg_inc<kComputeRegs>();
@@ -838,7 +845,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
         if (resolve_ahead)
           slot_s[((it + 2) % 3) * 128 + warp * 16 + lane] =
               pi_ahead >= 0 ? slot_from_page(page_ahead, idx_ahead, a.num_slots, a.dev_err) : -1;
-        if (it + 2 < my_tiles) prefetch_rows(slot_s + ((it + 2) % 3) * 128);
+        if (KV4_TILE_PREFETCH && it + 2 < my_tiles) prefetch_rows(slot_s + ((it + 2) % 3) * 128);
         fence_async_smem();
         tc_fence_before_sync();
       }
@@ -927,12 +934,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
     //      QK is done; each block arrived on it before waiting for its last
     //      PV), one bulk copy moves the staged half and this block's lse into
     //      the peer; meanwhile the threads read their own half from TMEM;
-    //   3. once the peer's half has arrived, the merged values go through a
-    //      second staging area (head-major rows) so that the output leaves in
-    //      16-byte stores;
-    //   4. a last cluster barrier keeps the staged half alive until the
-    //      peer's copy of it has landed.
-    // (The issue warpgroup meets the same two cluster barriers.)
+    //   3. once the peer's half has arrived, each block tells the peer so
+    //      (a remote mbarrier arrive: the peer's outgoing half has been read)
+    //      and stores its merged columns straight to out (for each head a
+    //      warp writes 32 consecutive columns);
+    //   4. before exiting, each block waits for the peer's word that this
+    //      block's outgoing half has arrived there.
+    // (The issue warpgroup meets the same cluster barrier.)
     if (cmerge) {
       constexpr int U = HG / 4;                              // 16-byte units of a row
       constexpr uint32_t kHalfBytes = HG * kLatent * 4 / 2;
@@ -942,7 +950,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
       float* xw = reinterpret_cast<float*>(smem + L::xw_off);
       float* xinv = reinterpret_cast<float*>(smem + L::xinv_off);
       uint8_t* stage_out = kv_s;                             // outgoing half, fp32
-      uint8_t* stage_res = kv_s + kHalfBytes;                // this block's merged rows
       auto row_unit = [&](int s2, int u) -> uint32_t {       // byte offset of a staged unit
         return static_cast<uint32_t>(((s2 * 128 + r_key) * U + (u ^ (r_key % U))) * 16);
       };
@@ -992,6 +999,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
         for (int j = 0; j < HPT; ++j) mine[s2][j] *= inv[j];
       }
       wait(bar_merge, 0);                      // the peer's half and lse are here
+      // the peer's copies into this block are complete, so its outgoing half
+      // has been read: let it finish (and exit) whenever it is done
+      if (tid == 0) mbar_remote_arrive(cluster_map(bar_done, peer));
       if (tid < HG) {
         const float l0 = rank == 0 ? xlse[tid] : xlse_in[tid];
         const float l1 = rank == 0 ? xlse_in[tid] : xlse[tid];
@@ -1005,18 +1015,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
         if (rank == 0) a.lse[out_head0 + tid] = wsum > 0.0f ? m + logf(wsum) : -INFINITY;
       }
       named_sync(kBarCompute, kComputeThreads);
-      // merged rows -> stage_res (head-major, 256 columns; lanes store
-      // consecutive columns of one head: no bank conflicts), then 16-byte
-      // units to out[head, 256 rank + ...]
-      auto merge_and_store = [&](auto* res) {
-        using T = std::remove_pointer_t<decltype(res)>;
+      // merged values straight to out[head, 256 rank + column]: for each head
+      // a warp's lanes store 32 consecutive columns (64 or 128 contiguous bytes)
+      {
         float w0[HPT], w1[HPT], xi[HPT];
         lds_vec<HPT>(xw + h0, w0);
         lds_vec<HPT>(xw + HG + h0, w1);
         lds_vec<HPT>(xinv + h0, xi);
 #pragma unroll
         for (int s2 = 0; s2 < 2; ++s2) {
-          const int c = s2 * 128 + r_key;                  // column within this block's half
+          const int64_t col = 256 * static_cast<int64_t>(rank) + s2 * 128 + r_key;
 #pragma unroll
           for (int k = 0; k < HPT / 4; ++k) {
             const float4 t = *reinterpret_cast<const float4*>(q_s + row_unit(s2, h0 / 4 + k));
@@ -1028,23 +1036,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
               const float v0 = rank == 0 ? mine[s2][j] : theirs[i];
               const float v1 = rank == 0 ? theirs[i] : mine[s2][j];
               const float v = (w0[j] * v0 + w1[j] * v1) * xi[j];
-              if constexpr (std::is_same_v<T, float>) res[(h0 + j) * 256 + c] = v;
-              else res[(h0 + j) * 256 + c] = __float2bfloat16_rn(v);
+              const int64_t o = (out_head0 + h0 + j) * kLatent + col;
+              if (a.out_f32) static_cast<float*>(a.out)[o] = v;
+              else static_cast<__nv_bfloat16*>(a.out)[o] = __float2bfloat16_rn(v);
             }
           }
         }
-        named_sync(kBarCompute, kComputeThreads);
-        constexpr int kUnitsPerRow = 256 * static_cast<int>(sizeof(T)) / 16;
-        const uint4* src = reinterpret_cast<const uint4*>(res);
-        for (int i = tid; i < HG * kUnitsPerRow; i += kComputeThreads) {
-          const int h = i / kUnitsPerRow, u = i % kUnitsPerRow;
-          T* dst = static_cast<T*>(a.out) + (out_head0 + h) * kLatent + 256 * static_cast<int64_t>(rank);
-          reinterpret_cast<uint4*>(dst)[u] = src[i];
-        }
-      };
-      if (a.out_f32) merge_and_store(reinterpret_cast<float*>(stage_res));
-      else merge_and_store(reinterpret_cast<__nv_bfloat16*>(stage_res));
-      cluster_sync();                          // the peer's copy of the staged half has landed
+      }
+      // before exiting: the peer has received this block's outgoing half
+      if (tid == 0) wait(bar_done, 0);
     }
   }  // compute warpgroups
   if (timed_out) flag_error(a.dev_err, kDevTimeout);
