@@ -367,6 +367,13 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+// log2(x) (MUFU, about 2 ulp for x in [1, 2]).
+__device__ __forceinline__ float fast_log2(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }

@@ -61,12 +61,6 @@ namespace {
 // Registers are moved from the issue warpgroup to the compute warpgroups
 // with setmaxnreg; per SM sub-partition (one warp of each warpgroup) that is
 // 2 x 232 + 40 = 504 of the 3 x 168 the block is launched with.
-#ifndef KV4_PRO_PREFETCH
-#define KV4_PRO_PREFETCH 1
-#endif
-#ifndef KV4_TILE_PREFETCH
-#define KV4_TILE_PREFETCH 1
-#endif
 constexpr int kComputeWarps = 8;
 constexpr int kComputeThreads = 32 * kComputeWarps;
 constexpr int kThreads = kComputeThreads + 128;
@@ -418,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
       const int32_t pi = slot_page_index(idx, l_eff, a.pt_stride, a.dev_err);
       const int32_t sl = pi >= 0 ? slot_from_page(__ldg(pt_row + pi), idx, a.num_slots, a.dev_err) : -1;
       slot_s[pro_t * 128 + pro_r] = sl;
-      if (KV4_PRO_PREFETCH && sl >= 0) {
+      if (sl >= 0) {
         const uint8_t* row = a.pool + static_cast<int64_t>(sl) * L::row_bytes;
         prefetch_l2_line(row);
         prefetch_l2_line(row + 128);
@@ -427,6 +421,67 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
       }
     }
   }
+  // (Compute warps.)  Rows of the next tile travel in registers: warp w
+  // holds rows 16w..16w+15 as three 32-bit words per lane -- latent word
+  // wa(l), latent word wb(l),
+  // and word 64 + l (lanes 0..7: scales, 8..23: rope, which only 352-byte
+  // rows have) -- where pass A covers slabs 0-3 and pass B slabs 4-7, each
+  // as one contiguous 128-byte run of the row:
+  //   wa(l) = l,   wb(l) = 32 + l.
+  // All three groups are reloaded for the next tile after the last pass,
+  // while QK finishes.
+  // An NVFP4 row's latent word w (8 codes) and an FP8 row's 8-byte latent
+  // unit w (8 E4M3 values) both become the f16 unit of columns 8w..8w+7.
+  // The extra word of lane l is word 64 + l of an NVFP4 row (scales, rope)
+  // and word 120 + l of an FP8 row (rope only, lanes 8..23).
+  using LatWord = std::conditional_t<FP8, uint2, uint32_t>;
+  constexpr int kExtraWord0 = FP8 ? 120 : 64;
+  const bool extra_lane = FP8 ? (lane >= 8 && lane < 24) : (lane < (ROPE ? 24 : 8));
+  const int word_a = lane;
+  const int word_b = lane + 32;
+  LatWord wa[16], wb[16];
+  uint32_t wex[16];
+  // the slots of this warp's 16 rows of the tile whose slots are at `slots`
+  // (re-read from shared memory for every tile, so that they hold no
+  // registers across it)
+  auto read_slots = [&](const int32_t* slots, int32_t (&sv)[16]) {
+#pragma unroll
+    for (int i = 0; i < 16; i += 4) {
+      const int4 t = *reinterpret_cast<const int4*>(slots + warp * 16 + i);
+      sv[i] = t.x; sv[i + 1] = t.y; sv[i + 2] = t.z; sv[i + 3] = t.w;
+    }
+  };
+  // The three words of each of this warp's 16 rows of the tile whose slots
+  // are at `slots` (read once), grouped by word -- every row's first word,
+  // then every row's second, then the extra words; a masked key gives a
+  // zero row.  (Issuing each row's three words back to back measured
+  // slower.)
+  auto load_rows = [&](const int32_t* slots) {
+    int32_t sv[16];
+    read_slots(slots, sv);
+    auto word_ptr = [&](int i) {
+      return reinterpret_cast<const uint32_t*>(a.pool + static_cast<int64_t>(sv[i]) * L::row_bytes);
+    };
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      if constexpr (FP8)
+        wa[i] = sv[i] >= 0 ? ldg_stream_u64(reinterpret_cast<const uint2*>(word_ptr(i)) + word_a)
+                           : make_uint2(0, 0);
+      else
+        wa[i] = sv[i] >= 0 ? ldg_stream_u32(word_ptr(i) + word_a) : 0u;
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      if constexpr (FP8)
+        wb[i] = sv[i] >= 0 ? ldg_stream_u64(reinterpret_cast<const uint2*>(word_ptr(i)) + word_b)
+                           : make_uint2(0, 0);
+      else
+        wb[i] = sv[i] >= 0 ? ldg_stream_u32(word_ptr(i) + word_b) : 0u;
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      wex[i] = (sv[i] >= 0 && extra_lane) ? ldg_stream_u32(word_ptr(i) + kExtraWord0 + lane) : 0u;
+  };
   // Q -> f16, 128-byte-swizzled K-major operand.  Each head is scaled by
   // 2^-e_h (exact) so that its largest magnitude lies in [2^14, 2^15): every
   // bf16 element then converts to f16 without loss (apart from elements
@@ -442,29 +497,36 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
     const int h = tid / TPH, part = tid % TPH;
     const bool active = h < HG;                    // HG = 16 uses 128 threads
     const uint4* qst = reinterpret_cast<const uint4*>(kv_s);
-    uint4 qv[UPT];
     uint32_t m = 0;
     if (active) wait(bar_q, 0);
+    // two passes over the staged rows (maximum, then conversion), so that no
+    // thread holds its whole share of Q in registers
 #pragma unroll
     for (int j = 0; j < UPT; ++j) {
       const int gu = part + ((j + h) % UPT) * TPH;   // 16-byte unit of head h
-      qv[j] = active ? qst[h * UNITS + gu] : make_uint4(0, 0, 0, 0);
-      const uint32_t w[4] = {qv[j].x, qv[j].y, qv[j].z, qv[j].w};
+      const uint4 qv = active ? qst[h * UNITS + gu] : make_uint4(0, 0, 0, 0);
+      const uint32_t w[4] = {qv.x, qv.y, qv.z, qv.w};
 #pragma unroll
       for (int k = 0; k < 4; ++k)
         m = max(m, max((w[k] << 16) & 0x7FFFFFFFu, w[k] & 0x7FFF0000u));   // |bf16| as fp32 bits
     }
 #pragma unroll
     for (int off = 1; off < TPH; off <<= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
-    const float amax = __uint_as_float(m);
-    const int e = amax > 0.0f ? ilogbf(amax) + 1 - 15 : 0;
-    const float f = exp2f(static_cast<float>(-e));
-    if (active && part == 0) qscale[h] = a.sm_scale * 1.4426950408889634f * exp2f(static_cast<float>(e));
+    // e = floor(log2 amax) + 1 - 15 from the bits of amax (|bf16| widened to
+    // fp32: normal, subnormal or zero), kept in [-126, 126] so that 2^-e and
+    // 2^e are normal floats built from their exponent fields
+    const int lg = m >= 0x00800000u ? static_cast<int>(m >> 23) - 127
+                                    : (m != 0u ? (31 - __clz(static_cast<int>(m))) - 149 : 14);
+    const int e = min(126, max(-126, lg - 14));
+    const float f = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+    if (active && part == 0)
+      qscale[h] = a.sm_scale * 1.4426950408889634f * __uint_as_float(static_cast<uint32_t>(127 + e) << 23);
     if (active) {
 #pragma unroll
       for (int j = 0; j < UPT; ++j) {
         const int gu = part + ((j + h) % UPT) * TPH;
-        const uint32_t w[4] = {qv[j].x, qv[j].y, qv[j].z, qv[j].w};
+        const uint4 qv = qst[h * UNITS + gu];
+        const uint32_t w[4] = {qv.x, qv.y, qv.z, qv.w};
         uint32_t o[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
@@ -604,62 +666,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
     float l_sum[HPT];
 #pragma unroll
     for (int h = 0; h < HPT; ++h) l_sum[h] = 0.0f;
-    // Rows of the next tile travel in registers: warp w holds rows 16w..16w+15
-    // as three 32-bit words per lane -- latent word wa(l), latent word wb(l),
-    // and word 64 + l (lanes 0..7: scales, 8..23: rope, which only 352-byte
-    // rows have) -- where pass A covers slabs 0-3 and pass B slabs 4-7, each
-    // as one contiguous 128-byte run of the row:
-    //   wa(l) = l,   wb(l) = 32 + l.
-    // All three groups are reloaded for the next tile after the last pass,
-    // while QK finishes.
-    // An NVFP4 row's latent word w (8 codes) and an FP8 row's 8-byte latent
-    // unit w (8 E4M3 values) both become the f16 unit of columns 8w..8w+7.
-    // The extra word of lane l is word 64 + l of an NVFP4 row (scales, rope)
-    // and word 120 + l of an FP8 row (rope only, lanes 8..23).
-    using LatWord = std::conditional_t<FP8, uint2, uint32_t>;
-    constexpr int kExtraWord0 = FP8 ? 120 : 64;
-    const bool extra_lane = FP8 ? (lane >= 8 && lane < 24) : (lane < (ROPE ? 24 : 8));
-    const int word_a = lane;
-    const int word_b = lane + 32;
-    LatWord wa[16], wb[16];
-    uint32_t wex[16];
-    // one word of each of this warp's 16 rows of the tile whose slots are
-    // at `slots` (the slots are re-read from shared memory for every group,
-    // so that they hold no registers across the tile)
-    auto read_slots = [&](const int32_t* slots, int32_t (&sv)[16]) {
-#pragma unroll
-      for (int i = 0; i < 16; i += 4) {
-        const int4 t = *reinterpret_cast<const int4*>(slots + warp * 16 + i);
-        sv[i] = t.x; sv[i + 1] = t.y; sv[i + 2] = t.z; sv[i + 3] = t.w;
-      }
-    };
-    auto load_latent = [&](LatWord (&w)[16], const int32_t* slots, int word) {
-      int32_t sv[16];
-      read_slots(slots, sv);
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const uint8_t* row = a.pool + static_cast<int64_t>(sv[i]) * L::row_bytes;
-        if constexpr (FP8)
-          w[i] = sv[i] >= 0 ? ldg_stream_u64(reinterpret_cast<const uint2*>(row) + word)
-                            : make_uint2(0, 0);
-        else
-          w[i] = sv[i] >= 0 ? ldg_stream_u32(reinterpret_cast<const uint32_t*>(row) + word) : 0u;
-      }                                                    // masked key: zero row
-    };
-    auto load_extra = [&](uint32_t (&w)[16], const int32_t* slots) {
-      int32_t sv[16];
-      read_slots(slots, sv);
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const uint32_t* row =
-            reinterpret_cast<const uint32_t*>(a.pool + static_cast<int64_t>(sv[i]) * L::row_bytes);
-        w[i] = (sv[i] >= 0 && extra_lane) ? ldg_stream_u32(row + kExtraWord0 + lane) : 0u;
-      }
-    };
-    // Start this warp's 16 rows of a tile (slots at `slots`, just written by
-    // its lanes 0..15) on their way into L2, so that the register gather one
-    // tile later finds them there: lane l asks for line (l & 3) of rows l/4
-    // and 8 + l/4 (a row's bytes span at most four 128-byte lines).
+    // Start this warp's 16 rows of a tile (slots at `slots`, written by its
+    // lanes 0..15 a tile earlier) on their way into L2, so that the register
+    // gather at the end of the current tile finds them there: lane l asks for
+    // line (l & 3) of rows l/4 and 8 + l/4 (a row's bytes span at most four
+    // 128-byte lines).
     auto prefetch_rows = [&](const int32_t* slots) {
       __syncwarp();
 #pragma unroll
@@ -678,11 +689,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
       }
     };
     if (a.early_inputs) grid_dependency_wait();   // the pool rows are written
-    if (my_tiles > 0) {
-      load_latent(wa, slot_s, word_a);
-      load_latent(wb, slot_s, word_b);
-      load_extra(wex, slot_s);
-    }
+    if (my_tiles > 0) load_rows(slot_s);
 
     // dequant store addresses (shared-window): latent word w of row r goes to
     // slab w/8, unit (w%8) ^ (r%8) of the row's 128-byte line; rows of this
@@ -714,6 +721,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
 
       // ---- a3/a4 in three passes, each into slabs that the previous tile's
       // PV has released; QK starts on each part as soon as all warps wrote it.
+      // the next tile's rows on their way into L2 while the previous PV runs
+      // (tile 1's were started in the prologue; the gather follows the last
+      // pass below)
+      if (it > 0 && it + 1 < my_tiles) prefetch_rows(next_slots);
       // pass A: slabs 0-3 (O slabs 0 and 1, which PV runs first)
       if (it > 0) {
         wait(bar_pv0, par ^ 1);
@@ -755,11 +766,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
       }
       // the next tile's rows, gathered while QK finishes (the passes above
       // run back to back, so that QK receives its parts as early as possible)
-      if (it + 1 < my_tiles) {
-        load_latent(wa, next_slots, word_a);
-        load_latent(wb, next_slots, word_b);
-        load_extra(wex, next_slots);
-      }
+      if (it + 1 < my_tiles) load_rows(next_slots);
 
       // ---- a2, second step: page-table entry of the key two tiles ahead
       if (resolve_ahead) {
@@ -845,7 +852,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
         if (resolve_ahead)
           slot_s[((it + 2) % 3) * 128 + warp * 16 + lane] =
               pi_ahead >= 0 ? slot_from_page(page_ahead, idx_ahead, a.num_slots, a.dev_err) : -1;
-        if (KV4_TILE_PREFETCH && it + 2 < my_tiles) prefetch_rows(slot_s + ((it + 2) % 3) * 128);
         fence_async_smem();
         tc_fence_before_sync();
       }
@@ -1006,17 +1012,21 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
         const float l0 = rank == 0 ? xlse[tid] : xlse_in[tid];
         const float l1 = rank == 0 ? xlse_in[tid] : xlse[tid];
         const float m = fmaxf(l0, l1);
-        const float w0 = l0 != -INFINITY ? expf(l0 - m) : 0.0f;
-        const float w1 = l1 != -INFINITY ? expf(l1 - m) : 0.0f;
+        // base-2 hardware exponent and logarithm (wsum lies in [1, 2])
+        const float w0 = l0 != -INFINITY ? fast_exp2((l0 - m) * 1.4426950408889634f) : 0.0f;
+        const float w1 = l1 != -INFINITY ? fast_exp2((l1 - m) * 1.4426950408889634f) : 0.0f;
         const float wsum = w0 + w1;
         xw[tid] = w0;
         xw[HG + tid] = w1;
-        xinv[tid] = wsum > 0.0f ? 1.0f / wsum : 0.0f;
-        if (rank == 0) a.lse[out_head0 + tid] = wsum > 0.0f ? m + logf(wsum) : -INFINITY;
+        xinv[tid] = wsum > 0.0f ? __frcp_rn(wsum) : 0.0f;
+        if (rank == 0)
+          a.lse[out_head0 + tid] =
+              wsum > 0.0f ? m + fast_log2(wsum) * 0.69314718055994531f : -INFINITY;
       }
       named_sync(kBarCompute, kComputeThreads);
       // merged values straight to out[head, 256 rank + column]: for each head
-      // a warp's lanes store 32 consecutive columns (64 or 128 contiguous bytes)
+      // a warp's lanes store 32 consecutive columns (storing bf16 pairs after
+      // a lane-pair exchange measured no faster)
       {
         float w0[HPT], w1[HPT], xi[HPT];
         lds_vec<HPT>(xw + h0, w0);
@@ -1361,3 +1371,4 @@ cudaError_t launch_debug_gather(const GatherArgs& a, cudaStream_t stream) {
 }
 
 }  // namespace kv4
+
