@@ -58,10 +58,12 @@ struct Plan {
 
 // Split-K planner: pick the number of partitions S of each query's tiles
 // that minimizes (waves of thread blocks) x (fixed cost of a block + tiles
-// per partition), plus a half-tile charge for the merge when S > 1; ties go
-// to the smaller S.  One block runs per SM.  The fixed cost (prologue: Q
-// load and conversion, first dependent loads; epilogue: output or partial
-// writes) is about two tiles of work.
+// per partition), plus a charge for the merge when S > 1 -- half a tile,
+// and 0.06 tile more for every partial beyond two (the merge kernel reads
+// them one row per warp) -- ties going to the smaller S.  One block runs per
+// SM.  The fixed cost (prologue: Q load and conversion, first dependent
+// loads; epilogue: output or partial writes) is about two tiles of work.
+// (Fitted to graph-timed sweeps of forced S on the five workloads.)
 Plan make_plan(int B, int Sq, int H, int K, int force_splits, int sms, int fmt) {
   Plan p{};
   p.HG = heads_per_block(H);
@@ -77,7 +79,7 @@ Plan make_plan(int B, int Sq, int H, int K, int force_splits, int sms, int fmt) 
         const long long waves = (static_cast<long long>(p.units) * c + sms - 1) / sms;
         const int per = (p.tiles + c - 1) / c;
         const double cost = static_cast<double>(waves) * (kBlockFixedTiles + per) +
-                            (c > 1 ? 0.5 : 0.0);
+                            (c > 1 ? 0.5 + 0.06 * (c > 2 ? c - 2 : 0) : 0.0);
         if (cost < best - 1e-9) { best = cost; S = c; }
       }
     }

@@ -1080,6 +1080,9 @@ __global__ void __launch_bounds__(256) merge_kernel(DecodeArgs a, int n_units) {
   const int NG = a.H / HG;
   const int g = unit % NG, bs = unit / NG;
   const float* lse_p = a.ws_lse + static_cast<int64_t>(unit) * a.splits * HG + h;
+  const float4* o_p = reinterpret_cast<const float4*>(
+      a.ws_o + (static_cast<int64_t>(unit) * a.splits * HG + h) * kLatent);
+  const int64_t o_stride = static_cast<int64_t>(HG) * kLatent / 4;   // float4 per split
   float m = -INFINITY;
   for (int i = 0; i < a.splits; ++i) m = fmaxf(m, lse_p[i * HG]);
   float4 acc[4];
@@ -1087,13 +1090,14 @@ __global__ void __launch_bounds__(256) merge_kernel(DecodeArgs a, int n_units) {
   for (int j = 0; j < 4; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
   float wsum = 0.0f;
   if (m != -INFINITY) {
+    // in split order, without branches, eight partials' loads in flight at a
+    // time (a split with no key has lse = -inf and weight 0; its o is 0)
+#pragma unroll 8
     for (int i = 0; i < a.splits; ++i) {
       const float li = lse_p[i * HG];
-      if (li == -INFINITY) continue;
-      const float w = expf(li - m);
+      const float w = li != -INFINITY ? fast_exp2((li - m) * 1.4426950408889634f) : 0.0f;
       wsum += w;
-      const float4* o = reinterpret_cast<const float4*>(
-          a.ws_o + ((static_cast<int64_t>(unit) * a.splits + i) * HG + h) * kLatent);
+      const float4* o = o_p + i * o_stride;
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const float4 v = o[j * 32 + lane];
@@ -1102,13 +1106,14 @@ __global__ void __launch_bounds__(256) merge_kernel(DecodeArgs a, int n_units) {
     }
   }
   const int64_t row = static_cast<int64_t>(bs) * a.H + g * HG + h;
-  const float inv = wsum > 0.0f ? 1.0f / wsum : 0.0f;
+  const float inv = wsum > 0.0f ? __frcp_rn(wsum) : 0.0f;
 #pragma unroll
   for (int j = 0; j < 4; ++j)
     store_out4(a.out, row * kLatent + j * 128 + lane * 4,
                make_float4(acc[j].x * inv, acc[j].y * inv, acc[j].z * inv, acc[j].w * inv),
                a.out_f32 != 0);
-  if (lane == 0) a.lse[row] = (wsum > 0.0f) ? m + logf(wsum) : -INFINITY;
+  if (lane == 0)
+    a.lse[row] = (wsum > 0.0f) ? m + fast_log2(wsum) * 0.69314718055994531f : -INFINITY;
 }
 
 // Debug: the decode's index resolution and dequantization (the f16 operand
