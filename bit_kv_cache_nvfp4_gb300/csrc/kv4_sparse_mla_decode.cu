@@ -376,6 +376,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
     mbar_init(bar_done, 1);
     fence_mbar_init();
   }
+  // every barrier is initialised and the TMEM address is in place before any
+  // thread waits on the one or reads the other
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
   // Everything above touches no global memory and may overlap the end of
   // the previous kernel of the stream, which may have produced any input.
   // When that kernel is known to be this call's own cache write (which
@@ -384,46 +390,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
   // waits just before its first read of pool rows.
   if (!a.early_inputs) grid_dependency_wait();
   grid_launch_dependents();
-  // The HG x QK bf16 rows of Q (contiguous) into the K/V region, which holds
-  // no tile yet, by one bulk copy; they are converted below.
+  // The HG x QK bf16 rows of Q (contiguous) go into the K/V region, which
+  // holds no tile yet, by one bulk copy; the compute warps convert them.
   constexpr uint32_t kQBytes = HG * L::QK * 2;
   static_assert(kQBytes <= L::kv_bytes, "Q staging fits the K/V region");
-  if (tid == kQThread) {
-    mbar_arrive_expect_tx(bar_q, kQBytes);
-    bulk_copy_g2s(kv_addr,
-                  static_cast<const __nv_bfloat16*>(a.q) + (static_cast<int64_t>(bs) * a.H + g * HG) * L::QK,
-                  kQBytes, bar_q);
-  }
-  // The request's page-table row into L2 (up to 32 KB, one 128-byte line
-  // per thread), so that the slot lookups below and two tiles ahead find
-  // their second dependent load there.
-  {
-    const int64_t pt_lines = (a.pt_stride * 4 + 127) / 128;
-    if (tid < pt_lines) prefetch_l2_line(reinterpret_cast<const uint8_t*>(pt_row) + tid * 128);
-  }
-  const int64_t l_eff = static_cast<int64_t>(__ldg(a.seq_lens + b)) - (a.Sq - 1 - s);
-  if (tid < HG) m_ref[tid] = -INFINITY;
-  // Slots of the first two tiles (a ring of three tiles, filled two ahead):
-  // top-k entry, page-table entry, slot -- one row per thread -- and each
-  // row is started on its way into L2 (its bytes span at most four 128-byte
-  // lines) while Q arrives and is converted.
-  {
-    const int pro_t = tid >> 7, pro_r = tid & 127;
-    const int pro_k = (tile_begin + pro_t) * kTileKeys + pro_r;
-    if (tid < kComputeThreads && pro_t < my_tiles) {
-      const int32_t idx = pro_k < a.K ? __ldg(topk_row + pro_k) : -1;
-      const int32_t pi = slot_page_index(idx, l_eff, a.pt_stride, a.dev_err);
-      const int32_t sl = pi >= 0 ? slot_from_page(__ldg(pt_row + pi), idx, a.num_slots, a.dev_err) : -1;
-      slot_s[pro_t * 128 + pro_r] = sl;
-      if (sl >= 0) {
-        const uint8_t* row = a.pool + static_cast<int64_t>(sl) * L::row_bytes;
-        prefetch_l2_line(row);
-        prefetch_l2_line(row + 128);
-        prefetch_l2_line(row + 256);
-        prefetch_l2_line(row + L::row_bytes - 1);
-      }
-    }
-  }
   // (Compute warps.)  Rows of the next tile travel in registers: warp w
   // holds rows 16w..16w+15 as three 32-bit words per lane -- latent word
   // wa(l), latent word wb(l),
@@ -485,29 +455,30 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
     for (int i = 0; i < 16; ++i)
       wex[i] = (sv[i] >= 0 && extra_lane) ? ldg_stream_u32(word_ptr(i) + kExtraWord0 + lane) : 0u;
   };
-  // Q -> f16, 128-byte-swizzled K-major operand.  Each head is scaled by
+  // Q -> f16, 128-byte-swizzled K-major operand, by the compute threads
+  // while their first slot lookups are in flight.  Each head is scaled by
   // 2^-e_h (exact) so that its largest magnitude lies in [2^14, 2^15): every
   // bf16 element then converts to f16 without loss (apart from elements
   // below 2^-24 of the head's maximum); 2^e_h is folded into the head's
   // score scale.  TPH threads own a head (its QK/8 16-byte units interleaved
   // among them, the order rotated by head so that a warp's reads of the
   // staged rows spread over all banks) and reduce its maximum with shuffles.
-  {
+  auto convert_q = [&] {
     constexpr int UNITS = L::QK / 8;               // 16-byte units of a head
     constexpr int TPH = HG == 64 ? 4 : 8;          // threads per head
     constexpr int UPT = UNITS / TPH;               // 16-byte units per thread
     static_assert(UNITS % TPH == 0, "units per thread");
     const int h = tid / TPH, part = tid % TPH;
-    const bool active = h < HG;                    // HG = 16 uses 128 threads
+    if (h >= HG) return;                           // HG = 16 uses 128 threads
     const uint4* qst = reinterpret_cast<const uint4*>(kv_s);
     uint32_t m = 0;
-    if (active) wait(bar_q, 0);
+    wait(bar_q, 0);
     // two passes over the staged rows (maximum, then conversion), so that no
     // thread holds its whole share of Q in registers
 #pragma unroll
     for (int j = 0; j < UPT; ++j) {
       const int gu = part + ((j + h) % UPT) * TPH;   // 16-byte unit of head h
-      const uint4 qv = active ? qst[h * UNITS + gu] : make_uint4(0, 0, 0, 0);
+      const uint4 qv = qst[h * UNITS + gu];
       const uint32_t w[4] = {qv.x, qv.y, qv.z, qv.w};
 #pragma unroll
       for (int k = 0; k < 4; ++k)
@@ -522,33 +493,34 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
                                     : (m != 0u ? (31 - __clz(static_cast<int>(m))) - 149 : 14);
     const int e = min(126, max(-126, lg - 14));
     const float f = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
-    if (active && part == 0)
+    if (part == 0)
       qscale[h] = a.sm_scale * 1.4426950408889634f * __uint_as_float(static_cast<uint32_t>(127 + e) << 23);
-    if (active) {
 #pragma unroll
-      for (int j = 0; j < UPT; ++j) {
-        const int gu = part + ((j + h) % UPT) * TPH;
-        const uint4 qv = qst[h * UNITS + gu];
-        const uint32_t w[4] = {qv.x, qv.y, qv.z, qv.w};
-        uint32_t o[4];
+    for (int j = 0; j < UPT; ++j) {
+      const int gu = part + ((j + h) % UPT) * TPH;
+      const uint4 qv = qst[h * UNITS + gu];
+      const uint32_t w[4] = {qv.x, qv.y, qv.z, qv.w};
+      uint32_t o[4];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const __half2 hv = __floats2half2_rn(__uint_as_float(w[k] << 16) * f,
-                                               __uint_as_float(w[k] & 0xFFFF0000u) * f);
-          o[k] = *reinterpret_cast<const uint32_t*>(&hv);
-        }
-        const uint32_t off = (gu >> 3) * (HG * 128) + (h >> 3) * 1024 + (h & 7) * 128 + (gu & 7) * 16;
-        *reinterpret_cast<uint4*>(q_s + swizzle<3>(off)) = make_uint4(o[0], o[1], o[2], o[3]);
+      for (int k = 0; k < 4; ++k) {
+        const __half2 hv = __floats2half2_rn(__uint_as_float(w[k] << 16) * f,
+                                             __uint_as_float(w[k] & 0xFFFF0000u) * f);
+        o[k] = *reinterpret_cast<const uint32_t*>(&hv);
       }
+      const uint32_t off = (gu >> 3) * (HG * 128) + (h >> 3) * 1024 + (h & 7) * 128 + (gu & 7) * 16;
+      *reinterpret_cast<uint4*>(q_s + swizzle<3>(off)) = make_uint4(o[0], o[1], o[2], o[3]);
     }
-  }
-  fence_async_smem();
-  tc_fence_before_sync();
-  __syncthreads();
-  tc_fence_after_sync();
-  const uint32_t tmem = *tmem_slot;
-
+  };
+  // The roles split here and never meet again before the epilogue; each
+  // takes its register share first, while it has no load in flight (the
+  // reallocation waits for the thread's outstanding loads).
   if (warp >= kComputeWarps) {
+    if (tid == kQThread) {
+      mbar_arrive_expect_tx(bar_q, kQBytes);
+      bulk_copy_g2s(kv_addr,
+                    static_cast<const __nv_bfloat16*>(a.q) + (static_cast<int64_t>(bs) * a.H + g * HG) * L::QK,
+                    kQBytes, bar_q);
+    }
     // ==== MMA issue warpgroup: lane 0 of each of its warps is an issuer ====
     // QK comes from kQkIssuers issuers (one partial sum of S^T each) and PV
     // from two (issuer 0: O slabs 0 then 2, issuer 1: slabs 1 then 3, so
@@ -653,6 +625,39 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
   } else {
     // ==== compute warpgroups (warps 0..7) ====
     setmaxnreg_inc<kComputeRegs>();
+    // The request's page-table row into L2 (up to 32 KB, one 128-byte line
+    // per thread), so that the slot lookups two tiles ahead find their
+    // second dependent load there.
+    {
+      const int64_t pt_lines = (a.pt_stride * 4 + 127) / 128;
+      if (tid < pt_lines) prefetch_l2_line(reinterpret_cast<const uint8_t*>(pt_row) + tid * 128);
+    }
+    const int64_t l_eff = static_cast<int64_t>(__ldg(a.seq_lens + b)) - (a.Sq - 1 - s);
+    if (tid < HG) m_ref[tid] = -INFINITY;
+    // Slots of the first two tiles (a ring of three tiles, filled two
+    // ahead): lane l of warp w resolves row 16w + (l mod 16) of tile l/16 --
+    // the rows the warp gathers itself -- by its top-k entry, page-table
+    // entry and slot.  The two dependent loads are in flight during the Q
+    // conversion.
+    {
+      const int t0 = lane >> 4, r0 = warp * 16 + (lane & 15);
+      const bool on = t0 < my_tiles;
+      int32_t idx = -1, pi = -1, page = -1;
+      if (on) {
+        const int k0 = (tile_begin + t0) * kTileKeys + r0;
+        idx = k0 < a.K ? __ldg(topk_row + k0) : -1;
+        pi = slot_page_index(idx, l_eff, a.pt_stride, a.dev_err);
+        if (pi >= 0) page = __ldg(pt_row + pi);
+      }
+      convert_q();
+      fence_async_smem();                            // Q is read by the tensor core
+      if (on)
+        slot_s[t0 * 128 + r0] = pi >= 0 ? slot_from_page(page, idx, a.num_slots, a.dev_err) : -1;
+    }
+    // Q, its scales, the reference maxima and the first slots are in place
+    named_sync(kBarCompute, kComputeThreads);
+    if (a.early_inputs) grid_dependency_wait();      // the pool rows are written
+    if (my_tiles > 0) load_rows(slot_s);
 
     // softmax roles: group G owns heads [G*HPT, G*HPT + HPT); thread (quarter,
     // lane) owns key row r = quarter*32 + lane of each tile = TMEM lane r.
@@ -690,8 +695,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
         return dequant_latent_word(w, w_ex, word);
       }
     };
-    if (a.early_inputs) grid_dependency_wait();   // the pool rows are written
-    if (my_tiles > 0) load_rows(slot_s);
 
     // dequant store addresses (shared-window): latent word w of row r goes to
     // slab w/8, unit (w%8) ^ (r%8) of the row's 128-byte line; rows of this
@@ -724,9 +727,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
       // ---- a3/a4 in three passes, each into slabs that the previous tile's
       // PV has released; QK starts on each part as soon as all warps wrote it.
       // the next tile's rows on their way into L2 while the previous PV runs
-      // (tile 1's were started in the prologue; the gather follows the last
-      // pass below)
-      if (it > 0 && it + 1 < my_tiles) prefetch_rows(next_slots);
+      // (the gather follows the last pass below)
+      if (it + 1 < my_tiles) prefetch_rows(next_slots);
       // pass A: slabs 0-3 (O slabs 0 and 1, which PV runs first)
       if (it > 0) {
         wait(bar_pv0, par ^ 1);
@@ -1028,7 +1030,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
       named_sync(kBarCompute, kComputeThreads);
       // merged values straight to out[head, 256 rank + column]: for each head
       // a warp's lanes store 32 consecutive columns (storing bf16 pairs after
-      // a lane-pair exchange measured no faster)
+      // a lane-pair exchange, or staging the rows for bulk copies, measured
+      // no faster)
       {
         float w0[HPT], w1[HPT], xi[HPT];
         lds_vec<HPT>(xw + h0, w0);
