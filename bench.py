@@ -14,8 +14,9 @@ events); barrier + synchronize around the timed loop; max over ranks.
 value = gathered-KV bytes of all ranks / max step time (GB/s).  The decode
 kernel alone (the roofline's kernel) is timed in a second loop, with an
 event the library records right after the decode kernel.  e2e repeats the
-step through the public API from pinned host buffers (inputs in, out/lse
-back) inside the timed region.
+step through the library's host-buffer C-ABI entry point (kv4_host_pipe_step)
+from pinned host buffers (inputs in, out/lse back, copies inside the timed
+region).
 
 --impl reference times the CPU oracle (single-threaded C++, the method's
 plain definition) on a bounded sample of the same workload.
@@ -406,7 +407,7 @@ def run_gpu(args):
     value = tot_bytes / (max_ms * 1e-3) / 1e9
 
     # end to end through the public API, host buffers in and out
-    e2e = run_e2e(kv, w, dev, pool, pt, lens, flush, args)
+    e2e = run_e2e(kv, w, dev, pool, pt, flush, args)
     cache_write = run_cache_write(kv, dev, flush, args)
     per_config = None
     if rank == 0 and not args.skip_per_config:
@@ -736,91 +737,54 @@ def run_latent_rows(kv, w, dev, q, pt, topk, lens, flush, err, args, valid):
             "note": "QK over the 512 latent columns, PV over the same 512; same workload"}
 
 
-def run_e2e(kv, w, dev, pool, pt, lens, flush, args, variants: int = 4):
-    """The same step through the public API with pinned host inputs and
-    outputs, as a serving loop runs it: every step copies its inputs (q, the
-    top-k list, the new tokens and their slots) from pinned host memory and
-    reads its result (out, lse) back into pinned host memory, and the copies
-    of step i+1's inputs and of step i-1's result run on two copy streams
-    while step i computes (double-buffered device inputs and outputs).  The
-    timed region spans all K steps, copies included.  L2 stays cold without a
-    flush: consecutive steps rotate over `variants` top-k sets (the same
-    positions shifted, so the same counts and structure) whose rows together
-    exceed L2."""
+def run_e2e(kv, w, dev, pool, pt, flush, args, variants: int = 4):
+    """The same step through the library's host-buffer C-ABI entry point
+    (kv4_host_pipe_step, via HostPipe), as a serving loop runs it: every step
+    copies its inputs (q, the top-k list, seq_lens, the new tokens and their
+    slots) from pinned host memory into device staging and its result (out,
+    lse) back into pinned host memory; the library keeps two steps in flight
+    (inputs of step i+1 and the result of step i-1 move on two copy streams
+    while step i computes).  The timed region spans all K steps, copies
+    included.  L2 stays cold without a flush: consecutive steps rotate over
+    `variants` top-k sets (the same positions shifted, so the same counts and
+    structure) whose rows together exceed L2."""
     K = args.steps
-    L = lens.to(torch.int64).cpu().view(-1, 1, 1)
+    L = w.seq_lens.to(torch.int64).view(-1, 1, 1)
     q_h = wl.queries(w).pin_memory()
     topk_h = [((w.topk.to(torch.int64) + 7919 * 64 * v) % L).to(torch.int32).pin_memory()
               for v in range(variants)]
+    lens_h = w.seq_lens.clone().pin_memory()
     nl, nr, ns = wl.newest_tokens(w)
     nl_h, nr_h, ns_h = nl.pin_memory(), nr.pin_memory(), ns.pin_memory()
     out_h = [torch.empty((w.B, w.Sq, w.H, 512), dtype=torch.bfloat16).pin_memory()
              for _ in range(2)]
     lse_h = [torch.empty((w.B, w.Sq, w.H), dtype=torch.float32).pin_memory() for _ in range(2)]
-    bufs = [dict(q=torch.empty_like(q_h, device=dev), topk=torch.empty_like(topk_h[0], device=dev),
-                 nl=torch.empty_like(nl_h, device=dev), nr=torch.empty_like(nr_h, device=dev),
-                 ns=torch.empty_like(ns_h, device=dev),
-                 out=torch.empty(out_h[0].shape, dtype=torch.bfloat16, device=dev),
-                 lse=torch.empty(lse_h[0].shape, dtype=torch.float32, device=dev))
-            for _ in range(2)]
-    splits, ws_bytes = kv.decode_plan(w.B, w.Sq, w.H, w.K)
-    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
-    compute = torch.cuda.current_stream(dev)
-    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    h2d = sum(t.numel() * t.element_size() for t in (q_h, topk_h[0], nl_h, nr_h, ns_h))
+    h2d = sum(t.numel() * t.element_size() for t in (q_h, topk_h[0], lens_h, nl_h, nr_h, ns_h))
     d2h = out_h[0].numel() * out_h[0].element_size() + lse_h[0].numel() * lse_h[0].element_size()
+    pipe = kv.HostPipe(w.B, w.Sq, w.H, w.K, ns_h.shape[0], dev)
 
     def run(n):
-        ev_in = [torch.cuda.Event() for _ in range(n)]
-        ev_dec = [torch.cuda.Event() for _ in range(n)]
-        ev_out = [torch.cuda.Event() for _ in range(n)]
-
-        def load(i):                       # inputs of step i into buffer i % 2
-            b = bufs[i % 2]
-            with torch.cuda.stream(s_in):
-                if i >= 2:
-                    s_in.wait_event(ev_dec[i - 2])        # buffer free again
-                b["q"].copy_(q_h, non_blocking=True)
-                b["topk"].copy_(topk_h[i % variants], non_blocking=True)
-                b["nl"].copy_(nl_h, non_blocking=True)
-                b["nr"].copy_(nr_h, non_blocking=True)
-                b["ns"].copy_(ns_h, non_blocking=True)
-                ev_in[i].record(s_in)
-
-        load(0)
         for i in range(n):
-            if i + 1 < n:
-                load(i + 1)
-            b = bufs[i % 2]
-            compute.wait_event(ev_in[i])
-            if i >= 2:
-                compute.wait_event(ev_out[i - 2])         # result buffer read back
-            kv.quantize_write_and_decode(b["nl"], b["nr"], b["ns"], pool, b["q"], pt, b["topk"],
-                                         lens, w.sm_scale, out=b["out"], lse=b["lse"],
-                                         workspace=ws)
-            ev_dec[i].record(compute)
-            with torch.cuda.stream(s_out):
-                s_out.wait_event(ev_dec[i])
-                out_h[i % 2].copy_(b["out"], non_blocking=True)
-                lse_h[i % 2].copy_(b["lse"], non_blocking=True)
-                ev_out[i].record(s_out)
-        compute.wait_event(ev_out[n - 1])
+            pipe.step(nl_h, nr_h, ns_h, pool, q_h, pt, topk_h[i % variants], lens_h, w.sm_scale,
+                      out_h[i % 2], lse_h[i % 2])
 
     run(max(3, args.warmup))
-    torch.cuda.synchronize(dev)
+    pipe.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    s_in.wait_stream(compute)
-    a.record(compute)
-    s_in.wait_event(a)
+    a.record(pipe.compute)
+    pipe.copy_in.wait_event(a)             # the first input copy starts after `a`
     run(K)
-    b.record(compute)
+    pipe.compute.wait_stream(pipe.copy_out)  # ... and the last result copy ends before `b`
+    b.record(pipe.compute)
     b.synchronize()
+    pipe.close()
     t = a.elapsed_time(b) / K
     valid = valid_key_count(w)
     return {"value": valid * 352 / (t * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": t,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "form": (f"pipelined over {K} steps (inputs of step i+1 and result of step i-1 "
-                     f"copied while step i computes); L2 cold by rotating {variants} top-k sets")}
+            "form": (f"kv4_host_pipe_step from pinned host buffers, {K} steps, two in flight "
+                     f"(inputs of step i+1 and result of step i-1 copied while step i "
+                     f"computes); L2 cold by rotating {variants} top-k sets")}
 
 
 def main(argv=None):

@@ -28,7 +28,7 @@ __all__ = [
     "debug_gather_dequant_latent", "sparse_mla_decode_partial", "dcp_mask_topk",
     "merge_partials", "gather_partials", "dcp_sparse_mla_decode", "dcp_local_page_table",
     "dcp_local_slots", "dcp_local_pages", "ROW_BYTES", "ROW_BYTES_LATENT", "LATENT", "ROPE", "QK_DIM", "PAGE", "DEV_BAD_SLOT", "DEV_BAD_PAGE",
-    "DEV_TIMEOUT",
+    "DEV_TIMEOUT", "HostPipe",
 ]
 
 ROW_BYTES, LATENT, ROPE, QK_DIM, PAGE, TILE_KEYS = 352, 512, 64, 576, 64, 128
@@ -112,6 +112,16 @@ def load_library():
                                                       lib.kv4_sparse_mla_decode.argtypes[:1] +
                                                       lib.kv4_sparse_mla_decode.argtypes[3:])
         lib.kv4_quantize_write_and_decode.restype = i32
+        lib.kv4_host_pipe_bytes.argtypes = [i32, i32, i32, i32, i64, i32, ctypes.POINTER(sz)]
+        lib.kv4_host_pipe_bytes.restype = i32
+        lib.kv4_host_pipe_create.argtypes = [i32, i32, i32, i32, i64, i32, P, sz, P, P, P,
+                                             ctypes.POINTER(P)]
+        lib.kv4_host_pipe_create.restype = i32
+        lib.kv4_host_pipe_step.argtypes = [P, P, P, P, i64, P, i64, P, i64, i32, P, P, P, f32, P,
+                                           P, P]
+        lib.kv4_host_pipe_step.restype = i32
+        lib.kv4_host_pipe_destroy.argtypes = [P]
+        lib.kv4_host_pipe_destroy.restype = i32
         lib.kv4_set_wait_limit.argtypes = [i64, i32]
         lib.kv4_set_wait_limit.restype = i32
         lib.kv4_set_timing_event.argtypes = [P]
@@ -508,6 +518,99 @@ def quantize_write_and_decode(latent: torch.Tensor, rope: torch.Tensor,
         _dev(lse, "lse", torch.float32), ws_ptr, ws_len, force_splits, _err_ptr(dev_err),
         _stream(dev)))
     return out, lse
+
+
+def _host(t: torch.Tensor, name: str, dtype: torch.dtype):
+    if not isinstance(t, torch.Tensor) or t.is_cuda:
+        raise TypeError(f"{name} must be a host (CPU) tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+class HostPipe:
+    """Decode steps fed from host memory (kv4_host_pipe_*): each step copies
+    its inputs from host tensors into device staging on a copy-in stream, runs
+    the write and the decode on the current stream, and copies out and lse
+    back into host tensors on a copy-out stream; two steps are in flight.
+
+    The staging memory (two areas and the split-K workspace) is allocated here
+    with PyTorch on `device`.  Host tensors should be pinned.  A step's host
+    inputs must stay unchanged, and its host outputs unread, until
+    ``synchronize()`` (or a later ``synchronize`` of the copy-out stream)."""
+
+    def __init__(self, B: int, Sq: int, H: int, K: int, max_new: int, device=None,
+                 force_splits: int = 0):
+        lib = load_library()
+        self._lib = lib
+        self.device = torch.device("cuda") if device is None else torch.device(device)
+        self.shape = (B, Sq, H, K)
+        self.max_new = max_new
+        nbytes = ctypes.c_size_t(0)
+        _check("kv4_host_pipe_bytes", lib.kv4_host_pipe_bytes(B, Sq, H, K, max_new, force_splits,
+                                                              ctypes.byref(nbytes)))
+        self._staging = torch.empty(max(nbytes.value, 256), dtype=torch.uint8, device=self.device)
+        self.copy_in = torch.cuda.Stream(self.device)
+        self.copy_out = torch.cuda.Stream(self.device)
+        self.compute = torch.cuda.current_stream(self.device)
+        handle = ctypes.c_void_p(None)
+        _check("kv4_host_pipe_create", lib.kv4_host_pipe_create(
+            B, Sq, H, K, max_new, force_splits, ctypes.c_void_p(self._staging.data_ptr()),
+            self._staging.numel(), ctypes.c_void_p(self.copy_in.cuda_stream),
+            ctypes.c_void_p(self.compute.cuda_stream),
+            ctypes.c_void_p(self.copy_out.cuda_stream), ctypes.byref(handle)))
+        self._handle = handle
+
+    def step(self, latent: torch.Tensor, rope: torch.Tensor, slot_mapping: torch.Tensor,
+             pool: torch.Tensor, q: torch.Tensor, page_table: torch.Tensor,
+             topk_idx: torch.Tensor, seq_lens: torch.Tensor, sm_scale: float,
+             out: torch.Tensor, lse: torch.Tensor, dev_err: torch.Tensor | None = None) -> None:
+        """Enqueue one step.  Host tensors: latent bf16 [N, 512], rope bf16
+        [N, 64], slot_mapping int64 [N], q bf16 [B, Sq, H, 576], topk_idx int32
+        [B, Sq, K], seq_lens int32 [B], out bf16 [B, Sq, H, 512], lse fp32
+        [B, Sq, H].  Device tensors: pool, page_table (and dev_err)."""
+        if self._handle is None:
+            raise RuntimeError("HostPipe is closed")
+        B, Sq, H, K = self.shape
+        n = slot_mapping.shape[0]
+        if (tuple(q.shape) != (B, Sq, H, QK_DIM) or tuple(topk_idx.shape) != (B, Sq, K) or
+                tuple(seq_lens.shape) != (B,) or tuple(out.shape) != (B, Sq, H, LATENT) or
+                tuple(lse.shape) != (B, Sq, H) or tuple(latent.shape) != (n, LATENT) or
+                tuple(rope.shape) != (n, ROPE)):
+            raise ValueError("host tensors must match the pipe's shape")
+        if pool.dim() != 2 or pool.shape[1] != ROW_BYTES or page_table.shape[0] != B:
+            raise ValueError(f"pool must be [num_slots, {ROW_BYTES}] and page_table [B, *]")
+        _check("kv4_host_pipe_step", self._lib.kv4_host_pipe_step(
+            self._handle, _host(latent, "latent", torch.bfloat16),
+            _host(rope, "rope", torch.bfloat16), _host(slot_mapping, "slot_mapping", torch.int64),
+            n, _dev(pool, "pool", torch.uint8), pool.shape[0],
+            _dev(page_table, "page_table", torch.int32), page_table.shape[1], PAGE,
+            _host(q, "q", torch.bfloat16), _host(topk_idx, "topk_idx", torch.int32),
+            _host(seq_lens, "seq_lens", torch.int32), float(sm_scale),
+            _host(out, "out", torch.bfloat16), _host(lse, "lse", torch.float32),
+            _err_ptr(dev_err)))
+
+    def synchronize(self) -> None:
+        """Wait until every enqueued step's results are in host memory."""
+        self.copy_out.synchronize()
+        self.compute.synchronize()
+
+    def close(self) -> None:
+        """Wait for the enqueued steps, then release the pipe (its staging
+        memory returns to PyTorch only after that)."""
+        if self._handle is not None:
+            self.synchronize()
+            self.copy_in.synchronize()
+            _check("kv4_host_pipe_destroy", self._lib.kv4_host_pipe_destroy(self._handle))
+            self._handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def debug_gather_dequant(pool: torch.Tensor, page_table: torch.Tensor, topk_idx: torch.Tensor,

@@ -8,6 +8,7 @@
 #include <atomic>
 #include <cstdint>
 #include <cstdlib>
+#include <new>
 
 namespace {
 
@@ -306,6 +307,231 @@ kv4_status kv4_quantize_write_and_decode(
                      topk_idx_dev, K, seq_lens_dev, B, Sq, H, sm_scale, out_dev, lse_dev,
                      workspace_dev, workspace_bytes, force_splits, dev_err, stream,
                      kv4::kFmtNvfp4, false, n_tokens > 0);
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Host-buffer pipe: the write-and-decode step fed from host memory, two steps
+// in flight over two device staging areas.
+// ---------------------------------------------------------------------------
+struct kv4_host_pipe {
+  struct Area {
+    void* q;
+    int32_t* topk;
+    int32_t* lens;
+    void* latent;
+    void* rope;
+    int64_t* slots;
+    void* out;
+    float* lse;
+  };
+  int B, Sq, H, K, force_splits;
+  int64_t max_new;
+  size_t q_bytes, topk_bytes, lens_bytes, out_bytes, lse_bytes;
+  Area area[2];
+  void* ws;
+  size_t ws_bytes;
+  cudaStream_t s_in, s_comp, s_out;
+  cudaEvent_t in_ready[2], comp_done[2], out_done[2];
+  bool used[2];
+  uint64_t steps;
+};
+
+namespace {
+
+size_t round256(size_t n) { return (n + 255) & ~static_cast<size_t>(255); }
+
+// Byte sizes of one staging area's buffers and of the whole staging memory.
+struct PipeSizes {
+  size_t q, topk, lens, latent, rope, slots, out, lse, area, ws, total;
+};
+
+kv4_status pipe_sizes(int B, int Sq, int H, int K, int64_t max_new, int force_splits,
+                      PipeSizes* z) {
+  const kv4_status shape = check_decode_shape(B, Sq, H, K);
+  if (shape != KV4_OK) return shape;
+  if (B < 1 || max_new < 0 || max_new > INT32_MAX || force_splits < 0)
+    return KV4_ERR_INVALID_ARG;
+  int splits = 0;
+  size_t ws = 0;
+  const kv4_status st = plan_impl(B, Sq, H, K, force_splits, &splits, &ws, kv4::kFmtNvfp4);
+  if (st != KV4_OK) return st;
+  const size_t rows = static_cast<size_t>(B) * Sq * H;
+  z->q = rows * KV4_QK_DIM * 2;
+  z->topk = static_cast<size_t>(B) * Sq * K * 4;
+  z->lens = static_cast<size_t>(B) * 4;
+  z->latent = static_cast<size_t>(max_new) * KV4_LATENT * 2;
+  z->rope = static_cast<size_t>(max_new) * KV4_ROPE * 2;
+  z->slots = static_cast<size_t>(max_new) * 8;
+  z->out = rows * KV4_LATENT * 2;
+  z->lse = rows * 4;
+  z->area = round256(z->q) + round256(z->topk) + round256(z->lens) + round256(z->latent) +
+            round256(z->rope) + round256(z->slots) + round256(z->out) + round256(z->lse);
+  z->ws = round256(ws);
+  z->total = 2 * z->area + z->ws;
+  return KV4_OK;
+}
+
+void destroy_events(kv4_host_pipe* p) {
+  for (int i = 0; i < 2; ++i) {
+    if (p->in_ready[i]) cudaEventDestroy(p->in_ready[i]);
+    if (p->comp_done[i]) cudaEventDestroy(p->comp_done[i]);
+    if (p->out_done[i]) cudaEventDestroy(p->out_done[i]);
+  }
+}
+
+}  // namespace
+
+extern "C" {
+
+kv4_status kv4_host_pipe_bytes(int B, int Sq, int H, int K, int64_t max_new, int force_splits,
+                               size_t* staging_bytes) {
+  if (!staging_bytes) return KV4_ERR_INVALID_ARG;
+  PipeSizes z{};
+  const kv4_status st = pipe_sizes(B, Sq, H, K, max_new, force_splits, &z);
+  if (st != KV4_OK) return st;
+  *staging_bytes = z.total;
+  return KV4_OK;
+}
+
+kv4_status kv4_host_pipe_create(int B, int Sq, int H, int K, int64_t max_new, int force_splits,
+                                void* staging_dev, size_t staging_bytes, kv4_stream_t copy_in,
+                                kv4_stream_t compute, kv4_stream_t copy_out,
+                                kv4_host_pipe** pipe) {
+  if (!pipe) return KV4_ERR_INVALID_ARG;
+  *pipe = nullptr;
+  PipeSizes z{};
+  const kv4_status st = pipe_sizes(B, Sq, H, K, max_new, force_splits, &z);
+  if (st != KV4_OK) return st;
+  if (!staging_dev || (reinterpret_cast<uintptr_t>(staging_dev) & 255u) != 0 ||
+      staging_bytes < z.total)
+    return KV4_ERR_INVALID_ARG;
+  kv4_host_pipe* p = new (std::nothrow) kv4_host_pipe{};
+  if (!p) return KV4_ERR_LAUNCH;
+  p->B = B;
+  p->Sq = Sq;
+  p->H = H;
+  p->K = K;
+  p->force_splits = force_splits;
+  p->max_new = max_new;
+  p->q_bytes = z.q;
+  p->topk_bytes = z.topk;
+  p->lens_bytes = z.lens;
+  p->out_bytes = z.out;
+  p->lse_bytes = z.lse;
+  uint8_t* cur = static_cast<uint8_t*>(staging_dev);
+  auto take = [&](size_t n) {
+    uint8_t* r = cur;
+    cur += round256(n);
+    return r;
+  };
+  for (int i = 0; i < 2; ++i) {
+    kv4_host_pipe::Area& a = p->area[i];
+    a.q = take(z.q);
+    a.topk = reinterpret_cast<int32_t*>(take(z.topk));
+    a.lens = reinterpret_cast<int32_t*>(take(z.lens));
+    a.latent = take(z.latent);
+    a.rope = take(z.rope);
+    a.slots = reinterpret_cast<int64_t*>(take(z.slots));
+    a.out = take(z.out);
+    a.lse = reinterpret_cast<float*>(take(z.lse));
+  }
+  p->ws = z.ws > 0 ? take(z.ws) : nullptr;
+  p->ws_bytes = z.ws;
+  p->s_in = reinterpret_cast<cudaStream_t>(copy_in);
+  p->s_comp = reinterpret_cast<cudaStream_t>(compute);
+  p->s_out = reinterpret_cast<cudaStream_t>(copy_out);
+  for (int i = 0; i < 2; ++i) {
+    if (cudaEventCreateWithFlags(&p->in_ready[i], cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&p->comp_done[i], cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&p->out_done[i], cudaEventDisableTiming) != cudaSuccess) {
+      destroy_events(p);
+      delete p;
+      return KV4_ERR_LAUNCH;
+    }
+  }
+  *pipe = p;
+  return KV4_OK;
+}
+
+kv4_status kv4_host_pipe_step(kv4_host_pipe* p, const void* latent_host, const void* rope_host,
+                              const int64_t* slots_host, int64_t n_new, uint8_t* pool_dev,
+                              int64_t num_slots, const int32_t* page_table_dev, int64_t pt_stride,
+                              int page_size, const void* q_host, const int32_t* topk_host,
+                              const int32_t* seq_lens_host, float sm_scale, void* out_host,
+                              float* lse_host, int32_t* dev_err) {
+  if (!p) return KV4_ERR_INVALID_ARG;
+  if (n_new < 0 || n_new > p->max_new) return KV4_ERR_INVALID_ARG;
+  if (!q_host || (p->K > 0 && !topk_host) || !seq_lens_host || !out_host || !lse_host ||
+      (n_new > 0 && (!latent_host || !rope_host || !slots_host)))
+    return KV4_ERR_INVALID_ARG;
+  const int s = static_cast<int>(p->steps & 1);
+  const kv4_host_pipe::Area& a = p->area[s];
+  // every device-side argument is checked before anything is enqueued
+  const kv4_status d = decode_impl(a.q, pool_dev, num_slots, page_table_dev, pt_stride, page_size,
+                                   a.topk, p->K, a.lens, p->B, p->Sq, p->H, sm_scale, a.out,
+                                   a.lse, p->ws, p->ws_bytes, p->force_splits, dev_err, p->s_comp,
+                                   kv4::kFmtNvfp4, false, false, false);
+  if (d != KV4_OK) return d;
+  if (n_new > 0 && (!pool_dev || num_slots < 0 || num_slots > INT64_MAX / KV4_ROW_BYTES))
+    return KV4_ERR_INVALID_ARG;
+
+  const size_t latent_bytes = static_cast<size_t>(n_new) * KV4_LATENT * 2;
+  const size_t rope_bytes = static_cast<size_t>(n_new) * KV4_ROPE * 2;
+  const size_t slot_bytes = static_cast<size_t>(n_new) * 8;
+  bool ok = true;
+  auto h2d = [&](void* dst, const void* src, size_t n) {
+    if (ok && n > 0)
+      ok = cudaMemcpyAsync(dst, src, n, cudaMemcpyHostToDevice, p->s_in) == cudaSuccess;
+  };
+  auto d2h = [&](void* dst, const void* src, size_t n) {
+    if (ok && n > 0)
+      ok = cudaMemcpyAsync(dst, src, n, cudaMemcpyDeviceToHost, p->s_out) == cudaSuccess;
+  };
+  auto wait_on = [&](cudaStream_t stream, cudaEvent_t ev) {
+    if (ok) ok = cudaStreamWaitEvent(stream, ev, 0) == cudaSuccess;
+  };
+  auto record = [&](cudaEvent_t ev, cudaStream_t stream) {
+    if (ok) ok = cudaEventRecord(ev, stream) == cudaSuccess;
+  };
+  // inputs into area s once the step two before has finished computing from it
+  if (p->used[s]) wait_on(p->s_in, p->comp_done[s]);
+  h2d(a.q, q_host, p->q_bytes);
+  h2d(a.topk, topk_host, p->topk_bytes);
+  h2d(a.lens, seq_lens_host, p->lens_bytes);
+  h2d(a.latent, latent_host, latent_bytes);
+  h2d(a.rope, rope_host, rope_bytes);
+  h2d(a.slots, slots_host, slot_bytes);
+  record(p->in_ready[s], p->s_in);
+  // the step, once its inputs are in and the step two before has read its
+  // results out of area s
+  wait_on(p->s_comp, p->in_ready[s]);
+  if (p->used[s]) wait_on(p->s_comp, p->out_done[s]);
+  if (!ok) return KV4_ERR_LAUNCH;
+  const kv4_status r = kv4_quantize_write_and_decode(
+      a.latent, KV4_LATENT, a.rope, KV4_ROPE, a.slots, n_new, pool_dev, num_slots, a.q,
+      page_table_dev, pt_stride, page_size, a.topk, p->K, a.lens, p->B, p->Sq, p->H, sm_scale,
+      a.out, a.lse, p->ws, p->ws_bytes, p->force_splits, dev_err,
+      reinterpret_cast<kv4_stream_t>(p->s_comp));
+  if (r != KV4_OK) return r;
+  record(p->comp_done[s], p->s_comp);
+  // results back to the host
+  wait_on(p->s_out, p->comp_done[s]);
+  d2h(out_host, a.out, p->out_bytes);
+  d2h(lse_host, a.lse, p->lse_bytes);
+  record(p->out_done[s], p->s_out);
+  if (!ok) return KV4_ERR_LAUNCH;
+  p->used[s] = true;
+  ++p->steps;
+  return KV4_OK;
+}
+
+kv4_status kv4_host_pipe_destroy(kv4_host_pipe* p) {
+  if (!p) return KV4_ERR_INVALID_ARG;
+  destroy_events(p);
+  delete p;
+  return KV4_OK;
 }
 
 kv4_status kv4_debug_gather_dequant(const uint8_t* pool_dev, int64_t num_slots,

@@ -22,8 +22,10 @@
  * Conventions for every entry point:
  *  - Pointers named *_dev are DEVICE pointers of the current CUDA device;
  *    the caller allocates and owns every buffer (including the workspace).
- *    The library keeps no pointer after a call returns, never allocates
- *    device memory and never synchronizes.
+ *    The library keeps no pointer after a call returns (apart from a host
+ *    pipe, which keeps its staging memory and streams until destroyed),
+ *    never allocates device memory and never synchronizes.  Pointers named
+ *    *_host are host pointers.
  *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
  *    stream) and runs asynchronously; outputs are valid once the stream has
  *    reached that point.
@@ -184,6 +186,75 @@ kv4_status kv4_quantize_write_and_decode(
     const int32_t* seq_lens_dev, int B, int Sq, int H, float sm_scale, void* out_dev,
     float* lse_dev, void* workspace_dev, size_t workspace_bytes, int force_splits,
     int32_t* dev_err, kv4_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Host-buffer steps (kv4_host_pipe_*) -- the step of
+ * kv4_quantize_write_and_decode fed from HOST memory, as a serving loop runs
+ * it: each step's inputs (the new tokens and their slots, q, the top-k list,
+ * seq_lens) are copied from host buffers into device staging, the write and
+ * the decode run, and out / lse are copied back into host buffers.  The
+ * pages have no counterpart: it is the same hot path (README "4-bit KV
+ * cache", kv4mla bullet: the write, then the decode it feeds) with its
+ * host<->device copies.
+ *
+ * A pipe keeps two steps in flight.  Step i's inputs are copied on copy_in
+ * while step i-1 computes on `compute`, and step i-1's results are copied
+ * back on copy_out while step i computes.  Steps alternate between two
+ * staging areas; CUDA events order the three streams (a step's copies into
+ * an area wait until the step two before it has finished computing from it,
+ * and its compute waits until that step's results have left it).
+ *
+ *   kv4_host_pipe_bytes(B, Sq, H, K, max_new, force_splits, &bytes)
+ *       device staging bytes of a pipe of this shape: two areas (q, top-k,
+ *       seq_lens, new tokens and slots, out, lse) and the split-K workspace.
+ *   kv4_host_pipe_create(B, Sq, H, K, max_new, force_splits, staging_dev,
+ *                        staging_bytes, copy_in, compute, copy_out, &pipe)
+ *       B, Sq, H, K: the decode shape of every step (as in
+ *       kv4_sparse_mla_decode); max_new: the most new tokens one step
+ *       writes; force_splits: as in kv4_decode_plan; staging_dev:
+ *       caller-owned device memory of at least kv4_host_pipe_bytes bytes,
+ *       256-byte aligned, which nothing else uses while the pipe lives;
+ *       copy_in, compute, copy_out: the caller's streams (one stream for all
+ *       three serializes the steps).  Creates six CUDA events and a small
+ *       host object; allocates no device memory.
+ *   kv4_host_pipe_step(pipe, latent_host, rope_host, slots_host, n_new,
+ *                      pool_dev, num_slots, page_table_dev, pt_stride,
+ *                      page_size, q_host, topk_host, seq_lens_host, sm_scale,
+ *                      out_host, lse_host, dev_err)
+ *       enqueues one step and returns.  Host buffers (contiguous):
+ *       latent_host bf16 [n_new, 512], rope_host bf16 [n_new, 64],
+ *       slots_host int64 [n_new] (0 <= n_new <= max_new), q_host bf16
+ *       [B, Sq, H, 576], topk_host int32 [B, Sq, K], seq_lens_host int32 [B],
+ *       out_host bf16 [B, Sq, H, 512], lse_host fp32 [B, Sq, H].  pool_dev
+ *       and page_table_dev are device buffers, as in the device calls, and
+ *       dev_err is a device word (or NULL).  Results equal those of
+ *       kv4_quantize_write_and_decode on the same values bit for bit.
+ *       Host buffers should be page-locked (cudaHostAlloc /
+ *       cudaHostRegister): with pageable memory the copies still happen but
+ *       block the calling thread.  A step's host inputs must stay unchanged,
+ *       and its host outputs unread, until copy_out has passed the step
+ *       (synchronize copy_out, or wait on an event recorded on it after the
+ *       call).  Argument errors return nonzero before anything is enqueued;
+ *       KV4_ERR_LAUNCH (a failed copy or launch) leaves the pipe unusable:
+ *       destroy it.
+ *   kv4_host_pipe_destroy(pipe)
+ *       releases the events and the host object; work already enqueued
+ *       completes normally.  The staging memory stays the caller's.
+ * ------------------------------------------------------------------------- */
+typedef struct kv4_host_pipe kv4_host_pipe;
+kv4_status kv4_host_pipe_bytes(int B, int Sq, int H, int K, int64_t max_new, int force_splits,
+                               size_t* staging_bytes);
+kv4_status kv4_host_pipe_create(int B, int Sq, int H, int K, int64_t max_new, int force_splits,
+                                void* staging_dev, size_t staging_bytes, kv4_stream_t copy_in,
+                                kv4_stream_t compute, kv4_stream_t copy_out,
+                                kv4_host_pipe** pipe);
+kv4_status kv4_host_pipe_step(kv4_host_pipe* pipe, const void* latent_host, const void* rope_host,
+                              const int64_t* slots_host, int64_t n_new, uint8_t* pool_dev,
+                              int64_t num_slots, const int32_t* page_table_dev, int64_t pt_stride,
+                              int page_size, const void* q_host, const int32_t* topk_host,
+                              const int32_t* seq_lens_host, float sm_scale, void* out_host,
+                              float* lse_host, int32_t* dev_err);
+kv4_status kv4_host_pipe_destroy(kv4_host_pipe* pipe);
 
 /* ---------------------------------------------------------------------------
  * kv4_debug_gather_dequant -- the decode's own index resolution and

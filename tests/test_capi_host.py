@@ -160,3 +160,25 @@ def test_noalloc_checks_arguments_before_its_scratch_limit(lib):
     # an empty batch is a no-op
     assert fn(None, None, 64, None, 1, 64, None, 8, None, 0, 1, 16, 0.1, None, None, 0, None,
               None) == 0
+
+
+def test_host_pipe_checks_arguments_without_a_device(lib):
+    """The host-buffer pipe entry points refuse null handles and outputs and
+    unsupported shapes before any device call."""
+    P, i64, i32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+    lib.kv4_host_pipe_bytes.argtypes = [i32, i32, i32, i32, i64, i32, ctypes.POINTER(sz)]
+    lib.kv4_host_pipe_create.argtypes = [i32, i32, i32, i32, i64, i32, P, sz, P, P, P,
+                                         ctypes.POINTER(P)]
+    lib.kv4_host_pipe_step.argtypes = [P, P, P, P, i64, P, i64, P, i64, i32, P, P, P,
+                                       ctypes.c_float, P, P, P]
+    lib.kv4_host_pipe_destroy.argtypes = [P]
+    n = sz()
+    assert lib.kv4_host_pipe_bytes(1, 1, 64, 2048, 1, 0, None) == 1
+    assert lib.kv4_host_pipe_bytes(1, 1, 48, 2048, 1, 0, ctypes.byref(n)) == 2
+    assert lib.kv4_host_pipe_bytes(1, 0, 64, 2048, 1, 0, ctypes.byref(n)) == 1
+    assert lib.kv4_host_pipe_bytes(0, 1, 64, 2048, 1, 0, ctypes.byref(n)) == 1
+    assert lib.kv4_host_pipe_bytes(1, 1, 64, 2048, -1, 0, ctypes.byref(n)) == 1
+    assert lib.kv4_host_pipe_create(1, 1, 64, 2048, 1, 0, None, 0, None, None, None, None) == 1
+    assert lib.kv4_host_pipe_step(None, None, None, None, 0, None, 0, None, 1, 64, None, None,
+                                  None, 0.1, None, None, None) == 1
+    assert lib.kv4_host_pipe_destroy(None) == 1
