@@ -637,27 +637,36 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
     // Slots of the first two tiles (a ring of three tiles, filled two
     // ahead): lane l of warp w resolves row 16w + (l mod 16) of tile l/16 --
     // the rows the warp gathers itself -- by its top-k entry, page-table
-    // entry and slot.  The two dependent loads are in flight during the Q
-    // conversion.
+    // entry and slot, while Q is on its way; tile 0's rows are then started
+    // into L2 (a row's bytes span at most four 128-byte lines), so that the
+    // gather after the Q conversion finds them there.
     {
       const int t0 = lane >> 4, r0 = warp * 16 + (lane & 15);
-      const bool on = t0 < my_tiles;
-      int32_t idx = -1, pi = -1, page = -1;
-      if (on) {
+      if (t0 < my_tiles) {
         const int k0 = (tile_begin + t0) * kTileKeys + r0;
-        idx = k0 < a.K ? __ldg(topk_row + k0) : -1;
-        pi = slot_page_index(idx, l_eff, a.pt_stride, a.dev_err);
-        if (pi >= 0) page = __ldg(pt_row + pi);
+        const int32_t idx = k0 < a.K ? __ldg(topk_row + k0) : -1;
+        const int32_t pi = slot_page_index(idx, l_eff, a.pt_stride, a.dev_err);
+        const int32_t sl =
+            pi >= 0 ? slot_from_page(__ldg(pt_row + pi), idx, a.num_slots, a.dev_err) : -1;
+        slot_s[t0 * 128 + r0] = sl;
+        if (t0 == 0 && sl >= 0) {
+          const uint8_t* row = a.pool + static_cast<int64_t>(sl) * L::row_bytes;
+          prefetch_l2_line(row);
+          prefetch_l2_line(row + 128);
+          prefetch_l2_line(row + 256);
+          prefetch_l2_line(row + L::row_bytes - 1);
+        }
       }
-      convert_q();
-      fence_async_smem();                            // Q is read by the tensor core
-      if (on)
-        slot_s[t0 * 128 + r0] = pi >= 0 ? slot_from_page(page, idx, a.num_slots, a.dev_err) : -1;
     }
-    // Q, its scales, the reference maxima and the first slots are in place
-    named_sync(kBarCompute, kComputeThreads);
+    convert_q();
+    fence_async_smem();                              // Q is read by the tensor core
+    __syncwarp();                                    // this warp's slots are written
     if (a.early_inputs) grid_dependency_wait();      // the pool rows are written
     if (my_tiles > 0) load_rows(slot_s);
+    // Q's scales, the reference maxima and the slots are in place for every
+    // compute warp (the barrier also waits for this thread's gathers, which
+    // the first pass needs anyway)
+    named_sync(kBarCompute, kComputeThreads);
 
     // softmax roles: group G owns heads [G*HPT, G*HPT + HPT); thread (quarter,
     // lane) owns key row r = quarter*32 + lane of each tile = TMEM lane r.
