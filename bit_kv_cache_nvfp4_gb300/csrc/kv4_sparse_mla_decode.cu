@@ -8,9 +8,10 @@
 // Work unit: one thread block per (request b, draft token s, head group g,
 // split).  A head group holds HG = min(H, 64) query heads, which all share
 // every gathered row.  The block (8 compute warps and one MMA-issue
-// warpgroup) first stages Q with one bulk copy and resolves the slots of its
-// first two tiles, then walks its share of the top-k list in tiles of 128
-// keys:
+// warpgroup) splits into its two roles at once; the issuer stages Q with one
+// bulk copy while the compute warps resolve the slots of the first two tiles,
+// convert Q and gather tile 0, then the block walks its share of the top-k
+// list in tiles of 128 keys:
 //   a2     slots are resolved two tiles ahead (top-k -> page table -> slot),
 //          each dependent load spread over a tile's work; as soon as a
 //          tile's slots are known its rows are prefetched into L2
@@ -35,9 +36,10 @@
 //          cross-thread reduction and no rescale), p is rounded to f16 and
 //          written as the PV operand over the tile's rope columns, which
 //          QK^T no longer needs
-//   a7     two issuers run O^T[512 x HG] += V^T . P^T (slabs 0-1 and 2-3
-//          of the latent columns; V^T is the same shared-memory tile read as
-//          an MN-major operand) and signal each 128-column slab's release
+//   a7     two issuers run O^T[512 x HG] += V^T . P^T (issuer 0 the
+//          128-column slabs 0 then 2 of the latent columns, issuer 1 slabs 1
+//          then 3; V^T is the same shared-memory tile read as an MN-major
+//          operand) and signal each slab's release
 //   a8     epilogue: O / sum(p) -> bf16 out, lse = ln 2 * (m + log2 sum(p));
 //          two splits of a unit merge inside their 2-block cluster, more
 //          write the normalized partial (o, lse) to the workspace and
