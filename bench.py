@@ -85,12 +85,23 @@ DECODE_SOURCES = ("bit_kv_cache_nvfp4_gb300/csrc/kv4_sparse_mla_decode.cu",
                   "bit_kv_cache_nvfp4_gb300/csrc/kv4_device.cuh")
 
 
+def _code_only(text: str) -> str:
+    """C++ source without comments and blank lines, each line stripped: a
+    change to comments alone leaves the compiled kernel as it was."""
+    import re
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(line.strip() for line in text.splitlines() if line.strip())
+
+
 def decode_source_hash() -> str:
+    """Hash of the decode kernel's code (comments excluded), which the
+    committed DRAM-traffic capture records."""
     import hashlib
     h = hashlib.sha256()
     for rel in DECODE_SOURCES:
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 
