@@ -1083,52 +1083,65 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
   }
 }
 
-// a9: out = sum_i exp(lse_i - lse) o_i, lse = log sum_i exp(lse_i).
-// One warp per (unit, head); lane l covers columns 4l..4l+3 of each 128.
-__global__ void __launch_bounds__(256) merge_kernel(DecodeArgs a, int n_units) {
+// a9 for more than two splits: out = sum_i w_i o_i / sum_i w_i with
+// w_i = exp(lse_i - max lse), lse = max lse + log(sum_i w_i), o_i the
+// normalized partials.  A group of `group` warps (one block) takes one
+// (unit, head, 128-column quarter of the latent) row: warp k accumulates the
+// partials k, k + group, ... (at most eight per warp, so each lane has all
+// its loads in flight at once), lane l the columns 4l..4l+3 of the quarter;
+// the warps' sums then meet in shared memory and warp 0 adds them in warp
+// order.  Every warp first takes the maximum lse over all splits itself.
+constexpr int kMergeMaxWarps = 8;
+__global__ void __launch_bounds__(32 * kMergeMaxWarps) merge_kernel(DecodeArgs a, int n_units,
+                                                                     int group) {
   grid_dependency_wait();                      // the decode's partials
   grid_launch_dependents();
-  const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
+  __shared__ float4 part_acc[kMergeMaxWarps][32];
+  __shared__ float part_w[kMergeMaxWarps];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int HG = a.HG;
-  if (gw >= n_units * HG) return;
-  const int unit = gw / HG, h = gw % HG;
+  const int quarter = blockIdx.x & 3;
+  const int rid = blockIdx.x >> 2;             // unit * HG + head
+  const int unit = rid / HG, h = rid % HG;
   const int NG = a.H / HG;
   const int g = unit % NG, bs = unit / NG;
-  const float* lse_p = a.ws_lse + static_cast<int64_t>(unit) * a.splits * HG + h;
+  const int S = a.splits;
+  const float* lse_p = a.ws_lse + static_cast<int64_t>(unit) * S * HG + h;
   const float4* o_p = reinterpret_cast<const float4*>(
-      a.ws_o + (static_cast<int64_t>(unit) * a.splits * HG + h) * kLatent);
+      a.ws_o + (static_cast<int64_t>(unit) * S * HG + h) * kLatent) + quarter * 32 + lane;
   const int64_t o_stride = static_cast<int64_t>(HG) * kLatent / 4;   // float4 per split
   float m = -INFINITY;
-  for (int i = 0; i < a.splits; ++i) m = fmaxf(m, lse_p[i * HG]);
-  float4 acc[4];
+  for (int i = lane; i < S; i += 32) m = fmaxf(m, lse_p[i * HG]);
 #pragma unroll
-  for (int j = 0; j < 4; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   float wsum = 0.0f;
   if (m != -INFINITY) {
-    // in split order, without branches, eight partials' loads in flight at a
-    // time (a split with no key has lse = -inf and weight 0; its o is 0)
+    // without branches (a split with no key has lse = -inf and weight 0;
+    // its o is 0)
 #pragma unroll 8
-    for (int i = 0; i < a.splits; ++i) {
+    for (int i = warp; i < S; i += group) {
       const float li = lse_p[i * HG];
       const float w = li != -INFINITY ? fast_exp2((li - m) * 1.4426950408889634f) : 0.0f;
       wsum += w;
-      const float4* o = o_p + i * o_stride;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float4 v = o[j * 32 + lane];
-        acc[j].x += w * v.x; acc[j].y += w * v.y; acc[j].z += w * v.z; acc[j].w += w * v.w;
-      }
+      const float4 v = o_p[i * o_stride];
+      acc.x += w * v.x; acc.y += w * v.y; acc.z += w * v.z; acc.w += w * v.w;
     }
+  }
+  part_acc[warp][lane] = acc;
+  if (lane == 0) part_w[warp] = wsum;
+  __syncthreads();
+  if (warp != 0) return;
+  for (int k = 1; k < group; ++k) {
+    const float4 t = part_acc[k][lane];
+    acc.x += t.x; acc.y += t.y; acc.z += t.z; acc.w += t.w;
+    wsum += part_w[k];
   }
   const int64_t row = static_cast<int64_t>(bs) * a.H + g * HG + h;
   const float inv = wsum > 0.0f ? __frcp_rn(wsum) : 0.0f;
-#pragma unroll
-  for (int j = 0; j < 4; ++j)
-    store_out4(a.out, row * kLatent + j * 128 + lane * 4,
-               make_float4(acc[j].x * inv, acc[j].y * inv, acc[j].z * inv, acc[j].w * inv),
-               a.out_f32 != 0);
-  if (lane == 0)
+  store_out4(a.out, row * kLatent + quarter * 128 + lane * 4,
+             make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv), a.out_f32 != 0);
+  if (quarter == 0 && lane == 0)
     a.lse[row] = (wsum > 0.0f) ? m + fast_log2(wsum) * 0.69314718055994531f : -INFINITY;
 }
 
@@ -1301,9 +1314,12 @@ cudaError_t launch_decode_hg(const DecodeArgs& a, cudaStream_t stream) {
                  a.cluster_merge ? a.splits : 1, a);
   if (e == cudaSuccess && a.after_decode != nullptr) e = cudaEventRecord(a.after_decode, stream);
   if (e != cudaSuccess || a.splits == 1 || a.cluster_merge) return e;
-  const int warps = units * HG;
-  return launch_pdl(merge_kernel, static_cast<unsigned>((warps + 7) / 8), 256, 0, stream, 1, a,
-                    units);
+  // a group of warps per (unit, head, column quarter), at most eight
+  // partials per warp
+  const int group = (a.splits + 7) / 8 < kMergeMaxWarps ? (a.splits + 7) / 8 : kMergeMaxWarps;
+  if (static_cast<int64_t>(units) * HG * 4 > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
+  return launch_pdl(merge_kernel, static_cast<unsigned>(units * HG * 4),
+                    static_cast<unsigned>(32 * group), 0, stream, 1, a, units, group);
 }
 
 template <int FMT>
