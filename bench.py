@@ -417,8 +417,14 @@ def run_gpu(args):
     max_ms, tot_bytes = reduce_over_ranks(t_ms, kv_bytes, dev if world > 1 else None)
     value = tot_bytes / (max_ms * 1e-3) / 1e9
 
-    # end to end through the public API, host buffers in and out
+    # end to end through the public API, host buffers in and out; whole job:
+    # the slowest rank's step time, every rank's bytes
     e2e = run_e2e(kv, w, dev, pool, pt, flush, args)
+    if world > 1:
+        e2e_ms, e2e_bytes = reduce_over_ranks(e2e["ms_per_step"], kv_bytes, dev)
+        e2e.update({"value": e2e_bytes / (e2e_ms * 1e-3) / 1e9, "ms_per_step": e2e_ms,
+                    "h2d_bytes_per_step": e2e["h2d_bytes_per_step"] * world,
+                    "d2h_bytes_per_step": e2e["d2h_bytes_per_step"] * world})
     cache_write = run_cache_write(kv, dev, flush, args)
     per_config = None
     if rank == 0 and not args.skip_per_config:
