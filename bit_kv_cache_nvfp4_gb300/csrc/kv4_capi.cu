@@ -342,6 +342,47 @@ namespace {
 
 size_t round256(size_t n) { return (n + 255) & ~static_cast<size_t>(255); }
 
+// A step's small inputs (lengths, new tokens, slots), read by one kernel
+// straight from page-locked host memory (which the device can address) into
+// device staging.  Each small cudaMemcpyAsync from the host carried a fixed
+// cost of several microseconds, which the copy-in stream paid once per
+// input; one launch pays it once.
+constexpr int kGatherMax = 4;
+struct HostGather {
+  const uint8_t* src[kGatherMax];
+  uint8_t* dst[kGatherMax];
+  size_t bytes[kGatherMax];
+  int n;
+};
+
+__global__ void __launch_bounds__(256) host_gather_kernel(HostGather g) {
+  const size_t tid = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+  for (int i = 0; i < g.n; ++i) {
+    const size_t n = g.bytes[i];
+    const bool vec = ((reinterpret_cast<uintptr_t>(g.src[i]) | reinterpret_cast<uintptr_t>(g.dst[i]) |
+                       n) & 15u) == 0;
+    if (vec) {
+      const uint4* s4 = reinterpret_cast<const uint4*>(g.src[i]);
+      uint4* d4 = reinterpret_cast<uint4*>(g.dst[i]);
+      for (size_t k = tid; k < n / 16; k += stride) d4[k] = s4[k];
+    } else {
+      for (size_t k = tid; k < n; k += stride) g.dst[i][k] = g.src[i][k];
+    }
+  }
+}
+
+// The device address of page-locked host memory, or nullptr when `p` is not
+// page-locked host memory that this device can address.
+const void* mapped_host(const void* p) {
+  cudaPointerAttributes attr{};
+  if (cudaPointerGetAttributes(&attr, p) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return nullptr;
+  }
+  return attr.type == cudaMemoryTypeHost ? attr.devicePointer : nullptr;
+}
+
 // Byte sizes of one staging area's buffers and of the whole staging memory.
 struct PipeSizes {
   size_t q, topk, lens, latent, rope, slots, out, lse, area, ws, total;
@@ -499,10 +540,39 @@ kv4_status kv4_host_pipe_step(kv4_host_pipe* p, const void* latent_host, const v
   if (p->used[s]) wait_on(p->s_in, p->comp_done[s]);
   h2d(a.q, q_host, p->q_bytes);
   h2d(a.topk, topk_host, p->topk_bytes);
-  h2d(a.lens, seq_lens_host, p->lens_bytes);
-  h2d(a.latent, latent_host, latent_bytes);
-  h2d(a.rope, rope_host, rope_bytes);
-  h2d(a.slots, slots_host, slot_bytes);
+  // the small inputs: one gather kernel when all are device-addressable
+  // page-locked memory, else one copy each
+  {
+    HostGather gat{};
+    const void* srcs[kGatherMax] = {seq_lens_host, latent_host, rope_host, slots_host};
+    void* dsts[kGatherMax] = {a.lens, a.latent, a.rope, a.slots};
+    const size_t sizes[kGatherMax] = {p->lens_bytes, latent_bytes, rope_bytes, slot_bytes};
+    bool mapped = true;
+    size_t total = 0;
+    for (int i = 0; i < kGatherMax && mapped; ++i) {
+      if (sizes[i] == 0) continue;
+      const void* dev = mapped_host(srcs[i]);
+      if (dev == nullptr) {
+        mapped = false;
+        break;
+      }
+      gat.src[gat.n] = static_cast<const uint8_t*>(dev);
+      gat.dst[gat.n] = static_cast<uint8_t*>(dsts[i]);
+      gat.bytes[gat.n] = sizes[i];
+      ++gat.n;
+      total += sizes[i];
+    }
+    if (mapped) {
+      if (ok && gat.n > 0) {
+        const size_t blocks = (total / 16 + 255) / 256;
+        host_gather_kernel<<<static_cast<unsigned>(blocks < 64 ? (blocks > 0 ? blocks : 1) : 64), 256,
+                             0, p->s_in>>>(gat);
+        ok = cudaGetLastError() == cudaSuccess;
+      }
+    } else {
+      for (int i = 0; i < kGatherMax; ++i) h2d(dsts[i], srcs[i], sizes[i]);
+    }
+  }
   record(p->in_ready[s], p->s_in);
   // the step, once its inputs are in and the step two before has read its
   // results out of area s

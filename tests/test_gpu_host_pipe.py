@@ -18,10 +18,12 @@ from gpu_common import assert_close, bits, gpu_pool, need_gpu, oracle_decode, wo
 pytestmark = pytest.mark.gpu
 
 
-def _host_steps(w, n):
+def _host_steps(w, n, pinned=True):
     """Per-step host inputs: step 0 the workload's own; step i > 0 scales q
     and the new tokens' values and shifts the top-k positions; step 2 writes
-    no token."""
+    no token.  With pinned=False the small inputs (lengths, new tokens,
+    slots) stay in pageable memory, which the pipe copies instead of reading
+    them through their device address."""
     q = wl.queries(w)
     L = w.seq_lens.to(torch.int64).view(-1, 1, 1)
     lat, rope, slots = wl.newest_tokens(w)
@@ -33,15 +35,16 @@ def _host_steps(w, n):
         k = 0 if i == 2 else slots.shape[0]
         li = lat[:k] if i == 0 else (lat[:k].float() * f).to(torch.bfloat16)
         ri = rope[:k] if i == 0 else (rope[:k].float() * f).to(torch.bfloat16)
+        small = (lambda t: t.pin_memory()) if pinned else (lambda t: t)
         steps.append(dict(q=qi.contiguous().pin_memory(), topk=ti.contiguous().pin_memory(),
-                          lens=w.seq_lens.clone().pin_memory(), lat=li.contiguous().pin_memory(),
-                          rope=ri.contiguous().pin_memory(),
-                          slots=slots[:k].clone().pin_memory()))
+                          lens=small(w.seq_lens.clone()), lat=small(li.contiguous()),
+                          rope=small(ri.contiguous()), slots=small(slots[:k].clone())))
     return steps
 
 
-@pytest.mark.parametrize("name,force_splits", [("tiny", 0), ("decode", 0), ("decode", 2)])
-def test_host_pipe_matches_device_steps(name, force_splits):
+@pytest.mark.parametrize("name,force_splits,pinned", [("tiny", 0, True), ("tiny", 0, False),
+                                                       ("decode", 0, True), ("decode", 2, True)])
+def test_host_pipe_matches_device_steps(name, force_splits, pinned):
     need_gpu()
     import bit_kv_cache_nvfp4_gb300 as kv
     dev = torch.device("cuda")
@@ -49,7 +52,7 @@ def test_host_pipe_matches_device_steps(name, force_splits):
     base = gpu_pool(w)
     pool_pipe, pool_ref = base.clone(), base.clone()
     pt = w.page_table.to(dev)
-    steps = _host_steps(w, 5)
+    steps = _host_steps(w, 5, pinned)
     n_max = max(s["slots"].shape[0] for s in steps)
     outs = [torch.full((w.B, w.Sq, w.H, 512), float("nan"), dtype=torch.bfloat16).pin_memory()
             for _ in steps]
@@ -78,7 +81,8 @@ def test_host_pipe_matches_device_steps(name, force_splits):
     requests = [0, w.B - 1] if w.B > 1 else [0]
     o_ref, l_ref = oracle_decode(w, requests)
     assert_close(outs[0][requests], lses[0][requests], o_ref, l_ref,
-                 f"{name} host pipe step 0 (S={force_splits or 'plan'})")
+                 f"{name} host pipe step 0 (S={force_splits or 'plan'}"
+                 f"{'' if pinned else ', pageable small inputs'})")
 
 
 def test_host_pipe_rejects_bad_arguments():
