@@ -342,12 +342,12 @@ namespace {
 
 size_t round256(size_t n) { return (n + 255) & ~static_cast<size_t>(255); }
 
-// A step's small inputs (lengths, new tokens, slots), read by one kernel
-// straight from page-locked host memory (which the device can address) into
-// device staging.  Each small cudaMemcpyAsync from the host carried a fixed
-// cost of several microseconds, which the copy-in stream paid once per
-// input; one launch pays it once.
-constexpr int kGatherMax = 4;
+// A step's smaller inputs (lengths, new tokens, slots, the top-k list), read
+// by one kernel straight from page-locked host memory (which the device can
+// address) into device staging.  Each small cudaMemcpyAsync from the host
+// carried a fixed cost of several microseconds, which the copy-in stream
+// paid once per input; one launch pays it once.
+constexpr int kGatherMax = 5;
 struct HostGather {
   const uint8_t* src[kGatherMax];
   uint8_t* dst[kGatherMax];
@@ -539,14 +539,14 @@ kv4_status kv4_host_pipe_step(kv4_host_pipe* p, const void* latent_host, const v
   // inputs into area s once the step two before has finished computing from it
   if (p->used[s]) wait_on(p->s_in, p->comp_done[s]);
   h2d(a.q, q_host, p->q_bytes);
-  h2d(a.topk, topk_host, p->topk_bytes);
-  // the small inputs: one gather kernel when all are device-addressable
+  // the other inputs: one gather kernel when all are device-addressable
   // page-locked memory, else one copy each
   {
     HostGather gat{};
-    const void* srcs[kGatherMax] = {seq_lens_host, latent_host, rope_host, slots_host};
-    void* dsts[kGatherMax] = {a.lens, a.latent, a.rope, a.slots};
-    const size_t sizes[kGatherMax] = {p->lens_bytes, latent_bytes, rope_bytes, slot_bytes};
+    const void* srcs[kGatherMax] = {topk_host, seq_lens_host, latent_host, rope_host, slots_host};
+    void* dsts[kGatherMax] = {a.topk, a.lens, a.latent, a.rope, a.slots};
+    const size_t sizes[kGatherMax] = {p->topk_bytes, p->lens_bytes, latent_bytes, rope_bytes,
+                                      slot_bytes};
     bool mapped = true;
     size_t total = 0;
     for (int i = 0; i < kGatherMax && mapped; ++i) {
@@ -565,8 +565,8 @@ kv4_status kv4_host_pipe_step(kv4_host_pipe* p, const void* latent_host, const v
     if (mapped) {
       if (ok && gat.n > 0) {
         const size_t blocks = (total / 16 + 255) / 256;
-        host_gather_kernel<<<static_cast<unsigned>(blocks < 64 ? (blocks > 0 ? blocks : 1) : 64), 256,
-                             0, p->s_in>>>(gat);
+        host_gather_kernel<<<static_cast<unsigned>(blocks < 152 ? (blocks > 0 ? blocks : 1) : 152),
+                             256, 0, p->s_in>>>(gat);
         ok = cudaGetLastError() == cudaSuccess;
       }
     } else {
@@ -579,17 +579,22 @@ kv4_status kv4_host_pipe_step(kv4_host_pipe* p, const void* latent_host, const v
   wait_on(p->s_comp, p->in_ready[s]);
   if (p->used[s]) wait_on(p->s_comp, p->out_done[s]);
   if (!ok) return KV4_ERR_LAUNCH;
+  // lse (a few KB) is written by the decode straight into the host buffer
+  // when that is device-addressable page-locked memory, instead of one more
+  // small copy; out goes back by one copy
+  float* lse_mapped = static_cast<float*>(const_cast<void*>(mapped_host(lse_host)));
+  if ((reinterpret_cast<uintptr_t>(lse_mapped) & 3u) != 0) lse_mapped = nullptr;
   const kv4_status r = kv4_quantize_write_and_decode(
       a.latent, KV4_LATENT, a.rope, KV4_ROPE, a.slots, n_new, pool_dev, num_slots, a.q,
       page_table_dev, pt_stride, page_size, a.topk, p->K, a.lens, p->B, p->Sq, p->H, sm_scale,
-      a.out, a.lse, p->ws, p->ws_bytes, p->force_splits, dev_err,
+      a.out, lse_mapped ? lse_mapped : a.lse, p->ws, p->ws_bytes, p->force_splits, dev_err,
       reinterpret_cast<kv4_stream_t>(p->s_comp));
   if (r != KV4_OK) return r;
   record(p->comp_done[s], p->s_comp);
   // results back to the host
   wait_on(p->s_out, p->comp_done[s]);
   d2h(out_host, a.out, p->out_bytes);
-  d2h(lse_host, a.lse, p->lse_bytes);
+  if (!lse_mapped) d2h(lse_host, a.lse, p->lse_bytes);
   record(p->out_done[s], p->s_out);
   if (!ok) return KV4_ERR_LAUNCH;
   p->used[s] = true;

@@ -231,10 +231,12 @@ kv4_status kv4_quantize_write_and_decode(
  *       kv4_quantize_write_and_decode on the same values bit for bit.
  *       Host buffers should be page-locked (cudaHostAlloc /
  *       cudaHostRegister): with pageable memory the copies still happen but
- *       block the calling thread.  q and the top-k list are copied on
- *       copy_in; the small inputs (seq_lens, the new tokens and their slots)
- *       are read there by one kernel through their device addresses when all
- *       of them are page-locked, and copied one by one otherwise.  A step's host inputs must stay unchanged,
+ *       block the calling thread.  q is copied on copy_in; the other inputs
+ *       (the top-k list, seq_lens, the new tokens and their slots) are read
+ *       there by one kernel through their device addresses when all of them
+ *       are page-locked, and copied one by one otherwise.  out is copied back
+ *       on copy_out; lse is written by the decode straight into lse_host when
+ *       that is page-locked, and copied otherwise.  A step's host inputs must stay unchanged,
  *       and its host outputs unread, until copy_out has passed the step
  *       (synchronize copy_out, or wait on an event recorded on it after the
  *       call).  Argument errors return nonzero before anything is enqueued;
