@@ -820,11 +820,20 @@ def main(argv=None):
                    help="skip the graph-timed measurement of every workload configuration")
     p.add_argument("--splits", type=int, default=0,
                    help="force the split-K count (0: the library's plan)")
+    p.add_argument("--cache-write-only", action="store_true",
+                   help="time only the 1M-token cache write (amax and MSE scales) and print it")
     args = p.parse_args(argv)
     if args.warmup < 3:
         p.error("--warmup must be >= 3")
     if args.impl == "reference":
         return run_reference(args)
+    if args.cache_write_only:
+        import bit_kv_cache_nvfp4_gb300 as kv
+        dev = torch.device("cuda", dist_env()[2])
+        torch.cuda.set_device(dev)
+        flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        print(json.dumps({"cache_write_1M_tokens": run_cache_write(kv, dev, flush, args)}))
+        return 0
     return run_gpu(args)
 
 
