@@ -429,7 +429,7 @@ def run_gpu(args):
     per_config = None
     if rank == 0 and not args.skip_per_config:
         per_config = run_per_config(kv, dev, flush, args, long_inputs=(w, pool))
-    latent = fp8 = None
+    latent = fp8 = dcp = None
     if not args.skip_variants:
         scratch = run_scratch_path(kv, w, dev, pool, q, pt, topk, lens, flush, args)
         del pool
@@ -440,6 +440,8 @@ def run_gpu(args):
         fp8["nvfp4_decode_us"] = dec_ms_avg * 1e3
         fp8["nvfp4_vs_scratch_path"] = fp8["scratch_path_us"] / (dec_ms_avg * 1e3)
         fp8["nvfp4_vs_fp8_rows"] = fp8["fp8_rows_decode_us"] / (dec_ms_avg * 1e3)
+        if rank == 0:
+            dcp = run_dcp(kv, w, dev, q, pt, topk, lens, flush)
 
     peak_gbs, peak_tflops, peak_kind = measured_peaks()
     achieved_gbs = alg_bytes / (dec_ms_avg * 1e-3) / 1e9
@@ -497,6 +499,7 @@ def run_gpu(args):
             "e2e": e2e,
             "latent_rows_288B": latent,
             "fp8_comparison": fp8,
+            "dcp": dcp,
             "cache_write_1M_tokens": cache_write,
             "per_config": per_config,
             "gpu_launches": launches_per_step * args.steps,
@@ -752,6 +755,60 @@ def run_latent_rows(kv, w, dev, q, pt, topk, lens, flush, err, args, valid):
             "decode_tflops": flops / (d_ms * 1e-3) / 1e12,
             "decode_algorithmic_gbs": alg / (d_ms * 1e-3) / 1e9,
             "note": "QK over the 512 latent columns, PV over the same 512; same workload"}
+
+
+def run_dcp(kv, w, dev, q, pt, topk, lens, flush, worlds=(2, 8)):
+    """Decode-context parallelism (README "Parallelism and disaggregation")
+    on the long workload, its R ranks emulated one after another on this GPU,
+    each with a pool of only its own pages.  Per rank, one step is its top-k
+    by page ownership, its local page table and its fp32 partial decode;
+    timed with CUDA-graph replays (cold L2) both with the masked full lists
+    and with the rank's keys compacted to the front of its lists and a decode
+    walking only those.  The log-sum-exp merge of the R partials is timed
+    too.  The all-gather between ranks is not (one GPU)."""
+    res = {}
+    for R in worlds:
+        o_parts = torch.empty((R, w.B, w.Sq, w.H, 512), dtype=torch.float32, device=dev)
+        l_parts = torch.empty((R, w.B, w.Sq, w.H), dtype=torch.float32, device=dev)
+        masked, compacted, pool_bytes = [], [], 0
+        splits, wsb = kv.decode_plan(w.B, w.Sq, w.H, w.K)
+        ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device=dev)
+        for r in range(R):
+            n_pages = kv.dcp_local_pages(w.num_slots // 64, R, r)
+            pool = torch.zeros((n_pages * 64, 352), dtype=torch.uint8, device=dev)
+            for lat, rope, slots in wl.iter_pool_chunks(w, chunk=1 << 18, device=dev):
+                kv.quantize_write(lat, rope, kv.dcp_local_slots(slots, R, r), pool)
+            pool_bytes = max(pool_bytes, pool.numel())
+
+            def step_masked(r=r, pool=pool):
+                mine = kv.dcp_mask_topk(topk, pt, lens, R, r)
+                ptl = kv.dcp_local_page_table(pt, R, r)
+                kv.sparse_mla_decode_partial(q, pool, ptl, mine, lens, w.sm_scale,
+                                             out=o_parts[r], lse=l_parts[r], workspace=ws)
+
+            def step_compacted(r=r, pool=pool):
+                mine, count = kv.dcp_compact_topk(topk, pt, lens, R, r)
+                ptl = kv.dcp_local_page_table(pt, R, r)
+                kv.sparse_mla_decode_partial(q, pool, ptl, mine, lens, w.sm_scale,
+                                             out=o_parts[r], lse=l_parts[r], workspace=ws,
+                                             k_count=count)
+
+            masked.append(graph_time_us(step_masked, flush)[0])
+            compacted.append(graph_time_us(step_compacted, flush)[0])
+            del pool
+            torch.cuda.empty_cache()
+        merge_cold, _ = graph_time_us(lambda: kv.merge_partials(o_parts, l_parts), flush)
+        res[f"R={R}"] = {
+            "rank_step_us_max": {"masked": max(masked), "compacted": max(compacted)},
+            "rank_step_us_mean": {"masked": sum(masked) / R, "compacted": sum(compacted) / R},
+            "merge_us": merge_cold,
+            "rank_pool_bytes": pool_bytes,
+            "partials_bytes_per_rank": o_parts[0].numel() * 4 + l_parts[0].numel() * 4,
+        }
+        del o_parts, l_parts
+    res["note"] = ("ranks emulated one after another on one GPU; cold-L2 graph replays; the "
+                   "all-gather of the fp32 partials is not measured")
+    return res
 
 
 def run_e2e(kv, w, dev, pool, pt, flush, args, variants: int = 4):

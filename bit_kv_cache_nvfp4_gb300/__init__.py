@@ -27,7 +27,7 @@ __all__ = [
     "fp8_scratch", "scratch_index", "ROW_BYTES_FP8", "quantize_write_and_decode", "quantize_write_latent", "decode_plan_latent", "sparse_mla_decode_latent",
     "debug_gather_dequant_latent", "sparse_mla_decode_partial", "dcp_mask_topk",
     "merge_partials", "gather_partials", "dcp_sparse_mla_decode", "dcp_local_page_table",
-    "dcp_local_slots", "dcp_local_pages", "ROW_BYTES", "ROW_BYTES_LATENT", "LATENT", "ROPE", "QK_DIM", "PAGE", "DEV_BAD_SLOT", "DEV_BAD_PAGE",
+    "dcp_local_slots", "dcp_local_pages", "dcp_compact_topk", "ROW_BYTES", "ROW_BYTES_LATENT", "LATENT", "ROPE", "QK_DIM", "PAGE", "DEV_BAD_SLOT", "DEV_BAD_PAGE",
     "DEV_TIMEOUT", "HostPipe",
 ]
 
@@ -92,6 +92,11 @@ def load_library():
         lib.kv4_sparse_mla_decode_partial.restype = i32
         lib.kv4_dcp_mask_topk.argtypes = [P, P, i64, P, i32, i32, i32, i32, i32, P, P]
         lib.kv4_dcp_mask_topk.restype = i32
+        lib.kv4_dcp_compact_topk.argtypes = [P, P, i64, P, i32, i32, i32, i32, i32, P, P, P]
+        lib.kv4_dcp_compact_topk.restype = i32
+        lib.kv4_sparse_mla_decode_partial_counted.argtypes = (
+            lib.kv4_sparse_mla_decode.argtypes[:8] + [P] + lib.kv4_sparse_mla_decode.argtypes[8:])
+        lib.kv4_sparse_mla_decode_partial_counted.restype = i32
         lib.kv4_dcp_local_page_table.argtypes = [P, i64, i32, i32, i32, P, P]
         lib.kv4_dcp_local_page_table.restype = i32
         lib.kv4_dcp_local_slots.argtypes = [P, i64, i32, i32, P, P]
@@ -330,14 +335,42 @@ def sparse_mla_decode_partial(q: torch.Tensor, pool: torch.Tensor, page_table: t
                               topk_idx: torch.Tensor, seq_lens: torch.Tensor, sm_scale: float,
                               out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
                               workspace: torch.Tensor | None = None, force_splits: int = 0,
-                              dev_err: torch.Tensor | None = None):
+                              dev_err: torch.Tensor | None = None,
+                              k_count: torch.Tensor | None = None):
     """sparse_mla_decode with an fp32 output: one context-parallel rank's
-    normalized partial (o fp32 [B,Sq,H,512], lse fp32 [B,Sq,H])."""
+    normalized partial (o fp32 [B,Sq,H,512], lse fp32 [B,Sq,H]).  With
+    k_count (int32 [B*Sq], e.g. from dcp_compact_topk) each query walks only
+    the first k_count entries of its list (kv4_sparse_mla_decode_partial_counted)."""
+    B, Sq, H, _ = q.shape
     if out is None:
-        B, Sq, H, _ = q.shape
         out = torch.empty((B, Sq, H, LATENT), dtype=torch.float32, device=q.device)
-    return _decode("nvfp4", q, pool, page_table, topk_idx, seq_lens, sm_scale, out, lse, workspace,
-                   force_splits, dev_err, partial=True)
+    if k_count is None:
+        return _decode("nvfp4", q, pool, page_table, topk_idx, seq_lens, sm_scale, out, lse,
+                       workspace, force_splits, dev_err, partial=True)
+    lib = load_library()
+    if q.shape[3] != QK_DIM or pool.dim() != 2 or pool.shape[1] != ROW_BYTES:
+        raise ValueError(f"q must be [B, Sq, H, {QK_DIM}] and pool [num_slots, {ROW_BYTES}]")
+    K = topk_idx.shape[2]
+    if (tuple(topk_idx.shape[:2]) != (B, Sq) or seq_lens.shape[0] != B or
+            page_table.shape[0] != B or k_count.numel() != B * Sq):
+        raise ValueError("topk_idx [B,Sq,K], seq_lens [B], page_table [B,*] and k_count [B*Sq] "
+                         "must agree with q")
+    if lse is None:
+        lse = torch.empty((B, Sq, H), dtype=torch.float32, device=q.device)
+    splits, ws_bytes = decode_plan(B, Sq, H, K, force_splits)
+    if workspace is None:
+        workspace = _workspace(q.device, ws_bytes)
+    ws_ptr = None if workspace is None else _dev(workspace, "workspace", workspace.dtype)
+    ws_len = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    fn = "kv4_sparse_mla_decode_partial_counted"
+    _check(fn, lib.kv4_sparse_mla_decode_partial_counted(
+        _dev(q, "q", torch.bfloat16), _dev(pool, "pool", torch.uint8), pool.shape[0],
+        _dev(page_table, "page_table", torch.int32), page_table.shape[1], PAGE,
+        _dev(topk_idx, "topk_idx", torch.int32), K, _dev(k_count, "k_count", torch.int32),
+        _dev(seq_lens, "seq_lens", torch.int32), B, Sq, H, float(sm_scale),
+        _dev(out, "out", torch.float32), _dev(lse, "lse", torch.float32), ws_ptr, ws_len,
+        force_splits, _err_ptr(dev_err), _stream(q.device)))
+    return out, lse
 
 
 def dcp_mask_topk(topk_idx: torch.Tensor, page_table: torch.Tensor, seq_lens: torch.Tensor,
@@ -352,6 +385,23 @@ def dcp_mask_topk(topk_idx: torch.Tensor, page_table: torch.Tensor, seq_lens: to
         page_table.shape[1], _dev(seq_lens, "seq_lens", torch.int32), B, Sq, K, int(world),
         int(rank), _dev(out, "topk_out", torch.int32), _stream(topk_idx.device)))
     return out
+
+
+def dcp_compact_topk(topk_idx: torch.Tensor, page_table: torch.Tensor, seq_lens: torch.Tensor,
+                     world: int, rank: int):
+    """The positions dcp_mask_topk keeps for rank ``rank``, moved to the front
+    of each query's list in their order (-1 after them), and their number per
+    query: (topk int32 [B,Sq,K], count int32 [B*Sq])."""
+    lib = load_library()
+    B, Sq, K = topk_idx.shape
+    out = torch.empty_like(topk_idx)
+    count = torch.empty(B * Sq, dtype=torch.int32, device=topk_idx.device)
+    _check("kv4_dcp_compact_topk", lib.kv4_dcp_compact_topk(
+        _dev(topk_idx, "topk_idx", torch.int32), _dev(page_table, "page_table", torch.int32),
+        page_table.shape[1], _dev(seq_lens, "seq_lens", torch.int32), B, Sq, K, int(world),
+        int(rank), _dev(out, "topk_out", torch.int32), _dev(count, "count_out", torch.int32),
+        _stream(topk_idx.device)))
+    return out, count
 
 
 def dcp_local_page_table(page_table: torch.Tensor, world: int, rank: int) -> torch.Tensor:
@@ -423,10 +473,10 @@ def dcp_sparse_mla_decode(q, local_pool, page_table, topk_idx, seq_lens, sm_scal
     ``page_table`` is the global (physical) one."""
     import torch.distributed as dist
     world, rank = dist.get_world_size(group), dist.get_rank(group)
-    mine = dcp_mask_topk(topk_idx, page_table, seq_lens, world, rank)
+    mine, count = dcp_compact_topk(topk_idx, page_table, seq_lens, world, rank)
     pt_local = dcp_local_page_table(page_table, world, rank)
     o, lse = sparse_mla_decode_partial(q, local_pool, pt_local, mine, seq_lens, sm_scale,
-                                       dev_err=dev_err)
+                                       dev_err=dev_err, k_count=count)
     o_parts, lse_parts = gather_partials(o, lse, group)
     return merge_partials(o_parts, lse_parts)
 

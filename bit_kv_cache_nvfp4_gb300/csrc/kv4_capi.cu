@@ -185,7 +185,8 @@ kv4_status decode_impl(const void* q_dev, const uint8_t* pool_dev, int64_t num_s
                        int Sq, int H, float sm_scale, void* out_dev, float* lse_dev,
                        void* workspace_dev, size_t workspace_bytes, int force_splits,
                        int32_t* dev_err, kv4_stream_t stream, int fmt, bool out_f32 = false,
-                       bool early_inputs = false, bool launch = true) {
+                       bool early_inputs = false, bool launch = true,
+                       const int32_t* k_count = nullptr) {
   const kv4_status args = check_decode_args(q_dev, pool_dev, num_slots, page_table_dev, pt_stride,
                                             page_size, topk_idx_dev, K, seq_lens_dev, B, Sq, H,
                                             out_dev, lse_dev);
@@ -220,6 +221,7 @@ kv4_status decode_impl(const void* q_dev, const uint8_t* pool_dev, int64_t num_s
   a.fmt = fmt;
   a.out_f32 = out_f32 ? 1 : 0;
   a.early_inputs = early_inputs ? 1 : 0;
+  a.k_count = k_count;
   if (p.splits > 1 && !p.cluster_merge) {
     a.ws_o = static_cast<float*>(workspace_dev);
     a.ws_lse = a.ws_o + static_cast<size_t>(p.units) * p.splits * p.HG * KV4_LATENT;
@@ -641,6 +643,40 @@ kv4_status kv4_sparse_mla_decode_partial(const void* q_dev, const uint8_t* pool_
                      topk_idx_dev, K, seq_lens_dev, B, Sq, H, sm_scale, o_dev, lse_dev,
                      workspace_dev, workspace_bytes, force_splits, dev_err, stream,
                      kv4::kFmtNvfp4, true);
+}
+
+kv4_status kv4_sparse_mla_decode_partial_counted(
+    const void* q_dev, const uint8_t* pool_dev, int64_t num_slots, const int32_t* page_table_dev,
+    int64_t pt_stride, int page_size, const int32_t* topk_idx_dev, int K,
+    const int32_t* k_count_dev, const int32_t* seq_lens_dev, int B, int Sq, int H, float sm_scale,
+    float* o_dev, float* lse_dev, void* workspace_dev, size_t workspace_bytes, int force_splits,
+    int32_t* dev_err, kv4_stream_t stream) {
+  if (B > 0 && (k_count_dev == nullptr || (reinterpret_cast<uintptr_t>(k_count_dev) & 3u) != 0))
+    return KV4_ERR_INVALID_ARG;
+  return decode_impl(q_dev, pool_dev, num_slots, page_table_dev, pt_stride, page_size,
+                     topk_idx_dev, K, seq_lens_dev, B, Sq, H, sm_scale, o_dev, lse_dev,
+                     workspace_dev, workspace_bytes, force_splits, dev_err, stream,
+                     kv4::kFmtNvfp4, true, false, true, k_count_dev);
+}
+
+kv4_status kv4_dcp_compact_topk(const int32_t* topk_idx_dev, const int32_t* page_table_dev,
+                                int64_t pt_stride, const int32_t* seq_lens_dev, int B, int Sq,
+                                int K, int world, int rank, int32_t* topk_out_dev,
+                                int32_t* count_out_dev, kv4_stream_t stream) {
+  if (B < 0 || Sq < 1 || K < 0 || pt_stride < 1 || world < 1 || rank < 0 || rank >= world)
+    return KV4_ERR_INVALID_ARG;
+  if (B == 0) return KV4_OK;
+  if ((K > 0 && (!topk_idx_dev || !topk_out_dev)) || !page_table_dev || !seq_lens_dev ||
+      !count_out_dev || (K > 0 && topk_idx_dev == topk_out_dev))
+    return KV4_ERR_INVALID_ARG;
+  int sms = 0;
+  const kv4_status st = device_info(&sms);
+  if (st != KV4_OK) return st;
+  return kv4::launch_dcp_compact_topk(topk_idx_dev, page_table_dev, pt_stride, seq_lens_dev, B,
+                                      Sq, K, world, rank, topk_out_dev, count_out_dev,
+                                      reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? KV4_OK
+             : KV4_ERR_LAUNCH;
 }
 
 kv4_status kv4_dcp_mask_topk(const int32_t* topk_idx_dev, const int32_t* page_table_dev,

@@ -51,6 +51,78 @@ __global__ void __launch_bounds__(256) dcp_mask_topk_kernel(const int32_t* topk,
   }
 }
 
+// The same ownership rule, with the rank's kept positions moved to the front
+// of each query's list in their order and -1 after them, and their number
+// in count_out[b * Sq + s]: a decode that walks only that many entries
+// (kv4_sparse_mla_decode_partial_counted) then does the rank's share of the
+// keys instead of every tile of the list.  One block of 256 threads per
+// query: thread t decides a contiguous run of kCompactPer entries at a time
+// (all of their loads in flight), and a block-wide prefix sum of the kept
+// counts places them.
+constexpr int kCompactThreads = 256;
+constexpr int kCompactPer = 8;
+
+__global__ void __launch_bounds__(kCompactThreads) dcp_compact_topk_kernel(
+    const int32_t* topk, const int32_t* page_table, int64_t pt_stride, const int32_t* seq_lens,
+    int B, int Sq, int K, int world, int rank, int32_t* topk_out, int32_t* count_out) {
+  grid_dependency_wait();
+  grid_launch_dependents();
+  __shared__ int warp_sums[kCompactThreads / 32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t rows = static_cast<int64_t>(B) * Sq;
+  for (int64_t bs = blockIdx.x; bs < rows; bs += gridDim.x) {
+    const int b = static_cast<int>(bs / Sq), s = static_cast<int>(bs % Sq);
+    const int64_t l_eff = static_cast<int64_t>(seq_lens[b]) - (Sq - 1 - s);
+    const int32_t* in = topk + bs * K;
+    int32_t* out = topk_out + bs * K;
+    int base = 0;                                   // kept entries of earlier rounds
+    for (int k0 = 0; k0 < K; k0 += kCompactThreads * kCompactPer) {
+      int32_t keep[kCompactPer];
+      int n = 0;
+#pragma unroll
+      for (int j = 0; j < kCompactPer; ++j) {
+        const int k = k0 + tid * kCompactPer + j;
+        keep[j] = -1;
+        if (k < K) {
+          const int32_t idx = in[k];
+          if (idx >= 0 && idx < l_eff) {
+            const int64_t pi = idx / kPage;
+            const int32_t page =
+                pi < pt_stride ? page_table[static_cast<int64_t>(b) * pt_stride + pi] : -1;
+            if (page < 0) keep[j] = rank == 0 ? idx : -1;  // unreadable: rank 0 reports it
+            else if (page % world == rank) keep[j] = idx;
+          }
+        }
+        n += keep[j] >= 0;
+      }
+      // exclusive prefix of n over the block, in thread order
+      int incl = n;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int v = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+        if (lane >= off) incl += v;
+      }
+      if (lane == 31) warp_sums[warp] = incl;
+      __syncthreads();
+      int before = 0, total = 0;
+#pragma unroll
+      for (int w2 = 0; w2 < kCompactThreads / 32; ++w2) {
+        const int ws = warp_sums[w2];
+        before += w2 < warp ? ws : 0;
+        total += ws;
+      }
+      int pos = base + before + incl - n;
+#pragma unroll
+      for (int j = 0; j < kCompactPer; ++j)
+        if (keep[j] >= 0) out[pos++] = keep[j];
+      base += total;
+      __syncthreads();                              // warp_sums is reused
+    }
+    for (int k = base + tid; k < K; k += kCompactThreads) out[k] = -1;
+    if (tid == 0) count_out[bs] = base;
+  }
+}
+
 // Rank-local page table: entry p (a physical page) becomes p / world where
 // the rank owns it (p >= 0, p % world == rank) and -1 elsewhere -- a
 // position on another rank's page never reaches this rank's decode (its
@@ -141,6 +213,19 @@ cudaError_t launch_dcp_mask_topk(const int32_t* topk, const int32_t* page_table,
   if (blocks > 4096) blocks = 4096;
   return launch_pdl(dcp_mask_topk_kernel, static_cast<unsigned>(blocks), 256, 0, stream, 1, topk,
                     page_table, pt_stride, seq_lens, B, Sq, K, world, rank, topk_out);
+}
+
+cudaError_t launch_dcp_compact_topk(const int32_t* topk, const int32_t* page_table,
+                                    int64_t pt_stride, const int32_t* seq_lens, int B, int Sq,
+                                    int K, int world, int rank, int32_t* topk_out,
+                                    int32_t* count_out, cudaStream_t stream) {
+  const int64_t rows = static_cast<int64_t>(B) * Sq;
+  if (rows <= 0) return cudaSuccess;
+  const int64_t blocks = rows < 4096 ? rows : 4096;      // one block per query
+  return launch_pdl(dcp_compact_topk_kernel, static_cast<unsigned>(blocks), kCompactThreads, 0,
+                    stream, 1,
+                    topk, page_table, pt_stride, seq_lens, B, Sq, K, world, rank, topk_out,
+                    count_out);
 }
 
 cudaError_t launch_dcp_local_page_table(const int32_t* page_table, int64_t n, int world,

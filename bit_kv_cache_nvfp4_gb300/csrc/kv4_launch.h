@@ -58,6 +58,9 @@ struct DecodeArgs {
   int out_f32;                 // 1: out is fp32 (a context-parallel rank's partial), else bf16
   int early_inputs;            // 1: q, page table, top-k and lengths may be read before the
                                //    previous kernel (this call's cache write) has finished
+  const int32_t* k_count;      // int32 [B * Sq] or null: each query walks only the first
+                               //    k_count[b * Sq + s] entries of its list (never with
+                               //    early_inputs)
 };
 
 struct GatherArgs {
@@ -110,6 +113,10 @@ cudaError_t launch_dcp_mask_topk(const int32_t* topk, const int32_t* page_table,
                                  int64_t pt_stride, const int32_t* seq_lens, int B, int Sq,
                                  int K, int world, int rank, int32_t* topk_out,
                                  cudaStream_t stream);
+cudaError_t launch_dcp_compact_topk(const int32_t* topk, const int32_t* page_table,
+                                    int64_t pt_stride, const int32_t* seq_lens, int B, int Sq,
+                                    int K, int world, int rank, int32_t* topk_out,
+                                    int32_t* count_out, cudaStream_t stream);
 cudaError_t launch_dcp_local_page_table(const int32_t* page_table, int64_t n, int world,
                                         int rank, int32_t* out, cudaStream_t stream);
 cudaError_t launch_dcp_local_slots(const int64_t* slots, int64_t n, int world, int rank,

@@ -329,10 +329,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
   const int s = bs % a.Sq;
   const int32_t* topk_row = a.topk + static_cast<int64_t>(bs) * a.K;
   const int32_t* pt_row = a.page_table + static_cast<int64_t>(b) * a.pt_stride;
-  const int num_tiles = (a.K + kTileKeys - 1) / kTileKeys;
-  const int tile_begin = split * a.tiles_per_split;
-  const int tile_end = min(num_tiles, tile_begin + a.tiles_per_split);
-  const int my_tiles = max(0, tile_end - tile_begin);
 
   uint8_t* q_s = smem;
   uint8_t* kv_s = smem + L::kv_off;
@@ -392,6 +388,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
   // waits just before its first read of pool rows.
   if (!a.early_inputs) grid_dependency_wait();
   grid_launch_dependents();
+  // The entries of the top-k list this unit walks: all K, or only the first
+  // k_count[b, s] of them (a context-parallel rank's own keys, moved to the
+  // front of its list; the rest of the list is masked).
+  // With a count, the unit's own tiles are shared evenly by its splits.
+  const int k_walk = a.k_count != nullptr ? min(a.K, max(0, __ldg(a.k_count + bs))) : a.K;
+  const int num_tiles = (k_walk + kTileKeys - 1) / kTileKeys;
+  const int tiles_per_split =
+      a.k_count != nullptr ? (num_tiles + a.splits - 1) / a.splits : a.tiles_per_split;
+  const int tile_begin = split * tiles_per_split;
+  const int tile_end = min(num_tiles, tile_begin + tiles_per_split);
+  const int my_tiles = max(0, tile_end - tile_begin);
   // The HG x QK bf16 rows of Q (contiguous) go into the K/V region, which
   // holds no tile yet, by one bulk copy; the compute warps convert them.
   constexpr uint32_t kQBytes = HG * L::QK * 2;

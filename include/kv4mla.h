@@ -398,6 +398,17 @@ kv4_status kv4_fp8_scratch_index(const int32_t* topk_idx_dev, int K, const int32
  *      log-sum-exp over the R partials (a partial with lse = -inf has weight
  *      0; no finite lse gives out = 0, lse = -inf).  o_parts and out 16-byte
  *      aligned.
+ * Steps 1-2 with each rank's work in proportion to its share of the keys:
+ *   1'. kv4_dcp_compact_topk: the same kept positions, moved to the front of
+ *      each query's list in their order, -1 after them (topk_out [B,Sq,K]
+ *      int32, not overlapping topk_idx), and their number per query in
+ *      count_out int32 [B*Sq].
+ *   2'. kv4_sparse_mla_decode_partial_counted: kv4_sparse_mla_decode_partial
+ *      walking only the first k_count_dev[b*Sq + s] entries of each query's
+ *      list (k_count_dev int32 [B*Sq], 4-byte aligned, read on the device;
+ *      values are clamped to [0, K]).  A split whose tiles lie past the
+ *      count contributes lse = -inf.  With 1'.'s output a rank at world R
+ *      walks about K/R keys instead of K.
  * ------------------------------------------------------------------------- */
 kv4_status kv4_dcp_mask_topk(const int32_t* topk_idx_dev, const int32_t* page_table_dev,
                              int64_t pt_stride, const int32_t* seq_lens_dev, int B, int Sq,
@@ -417,6 +428,16 @@ kv4_status kv4_sparse_mla_decode_partial(const void* q_dev, const uint8_t* pool_
                                          void* workspace_dev, size_t workspace_bytes,
                                          int force_splits, int32_t* dev_err,
                                          kv4_stream_t stream);
+kv4_status kv4_dcp_compact_topk(const int32_t* topk_idx_dev, const int32_t* page_table_dev,
+                                int64_t pt_stride, const int32_t* seq_lens_dev, int B, int Sq,
+                                int K, int world, int rank, int32_t* topk_out_dev,
+                                int32_t* count_out_dev, kv4_stream_t stream);
+kv4_status kv4_sparse_mla_decode_partial_counted(
+    const void* q_dev, const uint8_t* pool_dev, int64_t num_slots, const int32_t* page_table_dev,
+    int64_t pt_stride, int page_size, const int32_t* topk_idx_dev, int K,
+    const int32_t* k_count_dev, const int32_t* seq_lens_dev, int B, int Sq, int H, float sm_scale,
+    float* o_dev, float* lse_dev, void* workspace_dev, size_t workspace_bytes, int force_splits,
+    int32_t* dev_err, kv4_stream_t stream);
 kv4_status kv4_merge_partials(const float* o_parts_dev, const float* lse_parts_dev, int R,
                               int64_t n_rows, void* out_dev, float* lse_dev,
                               kv4_stream_t stream);

@@ -182,3 +182,26 @@ def test_host_pipe_checks_arguments_without_a_device(lib):
     assert lib.kv4_host_pipe_step(None, None, None, None, 0, None, 0, None, 1, 64, None, None,
                                   None, 0.1, None, None, None) == 1
     assert lib.kv4_host_pipe_destroy(None) == 1
+
+
+def test_dcp_compaction_and_counted_decode_check_arguments(lib):
+    """The compaction and the counted partial decode refuse bad arguments
+    before any device call."""
+    P, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+    c = lib.kv4_dcp_compact_topk
+    c.argtypes = [P, P, i64, P, i32, i32, i32, i32, i32, P, P, P]
+    c.restype = i32
+    buf = ctypes.create_string_buffer(1 << 12)
+    ptr = ctypes.cast(buf, P)
+    assert c(ptr, ptr, 1, ptr, 1, 1, 8, 2, 2, ptr, ptr, None) == 1     # rank >= world
+    assert c(ptr, ptr, 1, ptr, 1, 1, 8, 2, 0, ptr, None, None) == 1    # no count output
+    assert c(ptr, ptr, 1, ptr, 1, 1, 8, 2, 0, ptr, ptr, None) == 1     # output overlaps input
+    assert c(None, None, 1, None, 0, 1, 8, 2, 0, None, None, None) == 0  # empty batch
+    d = lib.kv4_sparse_mla_decode_partial_counted
+    f = ctypes.c_float
+    d.argtypes = [P, P, i64, P, i64, i32, P, i32, P, P, i32, i32, i32, f, P, P, P,
+                  ctypes.c_size_t, i32, P, P]
+    d.restype = i32
+    # no count array
+    assert d(ptr, ptr, 64, ptr, 1, 64, ptr, 8, None, ptr, 1, 1, 16, 0.1, ptr, ptr, None, 0, 0,
+             None, None) == 1

@@ -5,7 +5,10 @@ another rank).  For R ranks, every rank holds only its own pages: its pool
 has the pages p with p % R == rank, as page p // R, written through
 kv4_dcp_local_slots; kv4_dcp_mask_topk gives it its keys,
 kv4_dcp_local_page_table its page table over that pool,
-kv4_sparse_mla_decode_partial its fp32 (o, lse), and kv4_merge_partials
+kv4_sparse_mla_decode_partial its fp32 (o, lse) -- or, compacted,
+kv4_dcp_compact_topk its keys at the front of its lists and
+kv4_sparse_mla_decode_partial_counted a decode over those only -- and
+kv4_merge_partials
 combines the stacked partials -- which must agree with the oracle's decode
 over all keys within the decode tolerances.  The mask, the local page table
 and the local slots are checked bit for bit against the rules written out in
@@ -46,6 +49,30 @@ def test_mask_matches_ownership_rule(world):
 
 
 @pytest.mark.parametrize("world", [2, 3, 8])
+def test_compaction_matches_ownership_rule(world):
+    """kv4_dcp_compact_topk: each query's kept positions (the mask's rule) in
+    their order at the front of its list, -1 after them, and their count."""
+    need_gpu()
+    w = workload("decode")
+    _, pt, topk, lens = device_inputs(w)
+    topk_np = w.topk.numpy().copy()
+    topk_np[0, 0, :7] = -1                              # padding
+    topk_np[1, 0, 3] = int(w.seq_lens[1]) + 5           # past the sequence
+    t = torch.from_numpy(topk_np).cuda()
+    for r in range(world):
+        got, cnt = kv().dcp_compact_topk(t, pt, lens, world, r)
+        got, cnt = got.cpu().numpy(), cnt.cpu().numpy()
+        kept = owned_topk(topk_np, w.page_table.numpy(), w.seq_lens.numpy(), world, r)
+        for bs in range(w.B * w.Sq):
+            row = kept.reshape(-1, w.K)[bs]
+            ref = row[row >= 0]
+            n = int(cnt[bs])
+            assert n == ref.size, (r, bs)
+            assert np.array_equal(got.reshape(-1, w.K)[bs, :n], ref), (r, bs)
+            assert np.all(got.reshape(-1, w.K)[bs, n:] == -1), (r, bs)
+
+
+@pytest.mark.parametrize("world", [2, 3, 8])
 def test_local_addressing_matches_rule(world):
     need_gpu()
     w = workload("decode")
@@ -74,9 +101,14 @@ def local_pool(w, world, rank, dev):
     return pool
 
 
-@pytest.mark.parametrize("name,world", [("decode", 1), ("decode", 2), ("decode", 4),
-                                        ("decode", 8), ("long", 8)])
-def test_emulated_ranks_match_oracle(name, world):
+@pytest.mark.parametrize("name,world,compact", [("decode", 1, False), ("decode", 2, False),
+                                                ("decode", 4, False), ("decode", 8, False),
+                                                ("long", 8, False), ("decode", 2, True),
+                                                ("decode", 8, True), ("long", 8, True)])
+def test_emulated_ranks_match_oracle(name, world, compact):
+    """compact: each rank's keys moved to the front of its lists and its
+    decode walking only those (kv4_dcp_compact_topk and
+    kv4_sparse_mla_decode_partial_counted); else the masked full lists."""
     need_gpu()
     w = workload(name)
     q, pt, topk, lens = device_inputs(w)
@@ -86,11 +118,15 @@ def test_emulated_ranks_match_oracle(name, world):
     for r in range(world):
         pool = local_pool(w, world, r, q.device)          # this rank's pages only
         pages.append(pool.shape[0] // 64)
-        mine = m.dcp_mask_topk(topk, pt, lens, world, r)
+        count = None
+        if compact:
+            mine, count = m.dcp_compact_topk(topk, pt, lens, world, r)
+        else:
+            mine = m.dcp_mask_topk(topk, pt, lens, world, r)
         pt_local = m.dcp_local_page_table(pt, world, r)
         err = torch.zeros(1, dtype=torch.int32, device=q.device)
         o, l = m.sparse_mla_decode_partial(q, pool, pt_local, mine, lens, w.sm_scale,
-                                           dev_err=err)
+                                           dev_err=err, k_count=count)
         torch.cuda.synchronize()
         assert int(err.item()) == 0
         assert o.dtype == torch.float32
@@ -104,8 +140,9 @@ def test_emulated_ranks_match_oracle(name, world):
     torch.cuda.synchronize()
     req = [0, 7, 15] if name == "decode" else [0, 41]
     out_ref, lse_ref = oracle_decode(w, req)
-    mo, ml = assert_close(out[req], lse[req], out_ref, lse_ref, f"{name} world={world}")
-    print(f"{name} DCP world={world}: max|out err| {mo:.3g}  max|lse err| {ml:.3g}")
+    what = f"{name} world={world}" + (" compacted" if compact else "")
+    mo, ml = assert_close(out[req], lse[req], out_ref, lse_ref, what)
+    print(f"{what}: max|out err| {mo:.3g}  max|lse err| {ml:.3g}")
 
 
 def test_merge_of_empty_partials():
