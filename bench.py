@@ -760,12 +760,13 @@ def run_latent_rows(kv, w, dev, q, pt, topk, lens, flush, err, args, valid):
 def run_dcp(kv, w, dev, q, pt, topk, lens, flush, worlds=(2, 8)):
     """Decode-context parallelism (README "Parallelism and disaggregation")
     on the long workload, its R ranks emulated one after another on this GPU,
-    each with a pool of only its own pages.  Per rank, one step is its top-k
-    by page ownership, its local page table and its fp32 partial decode;
-    timed with CUDA-graph replays (cold L2) both with the masked full lists
-    and with the rank's keys compacted to the front of its lists and a decode
-    walking only those.  The log-sum-exp merge of the R partials is timed
-    too.  The all-gather between ranks is not (one GPU)."""
+    each with a pool of only its own pages and its page table over that pool
+    (kept by the rank, as its pool is: built once here).  Per rank, one step
+    is its top-k by page ownership and its fp32 partial decode; timed with
+    CUDA-graph replays (cold L2) both with the masked full lists and with the
+    rank's keys compacted to the front of its lists and a decode walking only
+    those.  The log-sum-exp merge of the R partials is timed too.  The
+    all-gather between ranks is not (one GPU)."""
     res = {}
     for R in worlds:
         o_parts = torch.empty((R, w.B, w.Sq, w.H, 512), dtype=torch.float32, device=dev)
@@ -779,23 +780,22 @@ def run_dcp(kv, w, dev, q, pt, topk, lens, flush, worlds=(2, 8)):
             for lat, rope, slots in wl.iter_pool_chunks(w, chunk=1 << 18, device=dev):
                 kv.quantize_write(lat, rope, kv.dcp_local_slots(slots, R, r), pool)
             pool_bytes = max(pool_bytes, pool.numel())
+            ptl = kv.dcp_local_page_table(pt, R, r)
 
-            def step_masked(r=r, pool=pool):
+            def step_masked(r=r, pool=pool, ptl=ptl):
                 mine = kv.dcp_mask_topk(topk, pt, lens, R, r)
-                ptl = kv.dcp_local_page_table(pt, R, r)
                 kv.sparse_mla_decode_partial(q, pool, ptl, mine, lens, w.sm_scale,
                                              out=o_parts[r], lse=l_parts[r], workspace=ws)
 
-            def step_compacted(r=r, pool=pool):
+            def step_compacted(r=r, pool=pool, ptl=ptl):
                 mine, count = kv.dcp_compact_topk(topk, pt, lens, R, r)
-                ptl = kv.dcp_local_page_table(pt, R, r)
                 kv.sparse_mla_decode_partial(q, pool, ptl, mine, lens, w.sm_scale,
                                              out=o_parts[r], lse=l_parts[r], workspace=ws,
                                              k_count=count)
 
             masked.append(graph_time_us(step_masked, flush)[0])
             compacted.append(graph_time_us(step_compacted, flush)[0])
-            del pool
+            del pool, ptl
             torch.cuda.empty_cache()
         merge_cold, _ = graph_time_us(lambda: kv.merge_partials(o_parts, l_parts), flush)
         res[f"R={R}"] = {
