@@ -467,9 +467,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
   // Q -> f16, 128-byte-swizzled K-major operand, by the compute threads
   // while their first slot lookups are in flight.  Each head is scaled by
   // 2^-e_h (exact) so that its largest magnitude lies in [2^14, 2^15): every
-  // bf16 element then converts to f16 without loss (apart from elements
-  // below 2^-24 of the head's maximum); 2^e_h is folded into the head's
-  // score scale.  TPH threads own a head (its QK/8 16-byte units interleaved
+  // bf16 element of at least 2^-31 of the head's maximum then converts to f16
+  // without loss (smaller ones fall into f16's subnormal range); 2^e_h is
+  // folded into the head's score scale.  TPH threads own a head (its QK/8 16-byte units interleaved
   // among them, the order rotated by head so that a warp's reads of the
   // staged rows spread over all banks) and reduce its maximum with shuffles.
   auto convert_q = [&] {
