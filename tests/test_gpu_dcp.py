@@ -72,6 +72,35 @@ def test_compaction_matches_ownership_rule(world):
             assert np.all(got.reshape(-1, w.K)[bs, n:] == -1), (r, bs)
 
 
+@pytest.mark.parametrize("K", [5, 3000])
+def test_compaction_ragged_and_multi_round(K):
+    """Lists shorter than one round and longer than one round of the
+    compaction block (256 threads x 8 entries), with padding, duplicates and
+    positions past the sequence."""
+    need_gpu()
+    w = workload("decode")
+    _, pt, _, lens = device_inputs(w)
+    g = torch.Generator().manual_seed(11)
+    L = w.seq_lens.to(torch.int64).view(-1, 1, 1)
+    topk = (torch.randint(0, 1 << 30, (w.B, w.Sq, K), generator=g) % (L + 8) - 4).to(torch.int32)
+    topk_np = topk.numpy()
+    t = topk.cuda()
+    world = 3
+    total = np.zeros(w.B * w.Sq, dtype=np.int64)
+    for r in range(world):
+        got, cnt = kv().dcp_compact_topk(t, pt, lens, world, r)
+        got, cnt = got.cpu().numpy().reshape(-1, K), cnt.cpu().numpy()
+        kept = owned_topk(topk_np, w.page_table.numpy(), w.seq_lens.numpy(), world, r)
+        for bs in range(w.B * w.Sq):
+            ref = kept.reshape(-1, K)[bs]
+            ref = ref[ref >= 0]
+            assert int(cnt[bs]) == ref.size and np.array_equal(got[bs, :ref.size], ref)
+            assert np.all(got[bs, ref.size:] == -1)
+        total += cnt
+    valid = ((topk_np >= 0) & (topk_np < w.seq_lens.numpy()[:, None, None])).reshape(-1, K)
+    assert np.array_equal(total, valid.sum(axis=1))      # the ranks partition the valid keys
+
+
 @pytest.mark.parametrize("world", [2, 3, 8])
 def test_local_addressing_matches_rule(world):
     need_gpu()
