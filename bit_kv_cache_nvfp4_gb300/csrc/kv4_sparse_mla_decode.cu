@@ -390,7 +390,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
   grid_launch_dependents();
   // The entries of the top-k list this unit walks: all K, or only the first
   // k_count[b, s] of them (a context-parallel rank's own keys, moved to the
-  // front of its list; the rest of the list is masked).
+  // front of its list); entries at or past k_walk are masked like -1.
   // With a count, the unit's own tiles are shared evenly by its splits.
   const int k_walk = a.k_count != nullptr ? min(a.K, max(0, __ldg(a.k_count + bs))) : a.K;
   const int num_tiles = (k_walk + kTileKeys - 1) / kTileKeys;
@@ -653,7 +653,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
       const int t0 = lane >> 4, r0 = warp * 16 + (lane & 15);
       if (t0 < my_tiles) {
         const int k0 = (tile_begin + t0) * kTileKeys + r0;
-        const int32_t idx = k0 < a.K ? __ldg(topk_row + k0) : -1;
+        const int32_t idx = k0 < k_walk ? __ldg(topk_row + k0) : -1;
         const int32_t pi = slot_page_index(idx, l_eff, a.pt_stride, a.dev_err);
         const int32_t sl =
             pi >= 0 ? slot_from_page(__ldg(pt_row + pi), idx, a.num_slots, a.dev_err) : -1;
@@ -740,7 +740,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
       const bool resolve_ahead = (it + 2 < my_tiles) && lane < 16;
       const int k_ahead = (tile + 2) * kTileKeys + warp * 16 + lane;
       int32_t idx_ahead = -1, page_ahead = -1, pi_ahead = -1;
-      if (resolve_ahead && k_ahead < a.K) idx_ahead = __ldg(topk_row + k_ahead);
+      if (resolve_ahead && k_ahead < k_walk) idx_ahead = __ldg(topk_row + k_ahead);
 
       // ---- a3/a4 in three passes, each into slabs that the previous tile's
       // PV has released; QK starts on each part as soon as all warps wrote it.

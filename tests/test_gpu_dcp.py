@@ -185,3 +185,41 @@ def test_merge_of_empty_partials():
     assert torch.all(out[[0, 1, 3, 4]] == 0)
     assert abs(float(lse[2]) - 0.5) < 1e-6
     assert torch.equal(out[2], o[1, 2].to(torch.bfloat16))
+
+
+def test_counted_decode_walks_only_the_counted_entries():
+    """kv4_sparse_mla_decode_partial_counted with arbitrary counts (0, 1, K,
+    and values that are not multiples of 128): the same result as the
+    oracle's decode of the lists with every entry past the count masked."""
+    need_gpu()
+    import oracle
+    from gpu_common import bits, gpu_pool
+    w = workload("decode")
+    q, pt, topk, lens = device_inputs(w)
+    counts = torch.tensor([0, 1, 2048, 130, 1000, 127, 128, 2047, 5, 700, 1500, 64, 2000, 333,
+                           256, 1919], dtype=torch.int32)[: w.B * w.Sq]
+    o, l = kv().sparse_mla_decode_partial(q, gpu_pool(w), pt, topk, lens, w.sm_scale,
+                                          k_count=counts.cuda())
+    torch.cuda.synchronize()
+    trunc = w.topk.clone()
+    for bs in range(w.B * w.Sq):
+        trunc.view(-1, w.K)[bs, int(counts[bs]):] = -1
+    req = [0, 1, 3, 5, 7]
+    qids = [(b, s) for b in req for s in range(w.Sq)]
+    pt_c, pages = wl.compact_pool_plan(w, qids)[:2]
+    ns = wl.compact_pool_plan(w, qids)[2]
+    ids, cslots = wl.compact_pool_tokens(w, pages, qids)
+    pool = np.zeros((max(ns, 64), 352), dtype=np.uint8)
+    lat, rope = wl.token_rows(w, ids)
+    assert oracle.quantize_write(bits(lat), bits(rope), cslots.numpy(), pool) == oracle.OK
+    qb = bits(wl.queries(w))
+    outs, lses = [], []
+    for b in req:
+        st, out, lse = oracle.sparse_mla_decode(
+            np.ascontiguousarray(qb[b:b + 1]), pool, np.ascontiguousarray(pt_c[b:b + 1].numpy()),
+            np.ascontiguousarray(trunc[b:b + 1].numpy()),
+            np.ascontiguousarray(w.seq_lens[b:b + 1].numpy()), w.sm_scale)
+        assert st == oracle.OK
+        outs.append(out[0])
+        lses.append(lse[0])
+    assert_close(o[req], l[req], np.stack(outs), np.stack(lses), "decode, counted walk")
