@@ -139,7 +139,7 @@ def assert_close(out_gpu: torch.Tensor, lse_gpu: torch.Tensor, out_ref: np.ndarr
     both_inf = np.isneginf(l) & np.isneginf(lse_ref)
     assert np.array_equal(np.isneginf(l), np.isneginf(lse_ref)), f"{what}: -inf lse pattern differs"
     err_o = np.abs(o.astype(np.float64) - out_ref)
-    err_l = np.where(both_inf, 0.0, np.abs(l - lse_ref))
+    err_l = np.abs(np.where(both_inf, 0.0, l) - np.where(both_inf, 0.0, lse_ref))
     assert np.isfinite(o).all(), f"{what}: non-finite output"
     bound = out_bound(out_ref)
     excess = err_o - bound
