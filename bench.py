@@ -491,7 +491,8 @@ def run_gpu(args):
             "config": {"workload": WORKLOAD_DESC, "B": w.B, "Sq": w.Sq, "H": w.H, "K": w.K,
                        "seq_len": int(w.seq_lens[0]), "pool_bytes": w.num_slots * 352,
                        "splits": splits, "l2": "flushed between timed steps (256 MiB write)",
-                       "parallelism": f"{world} independent ranks (sessions sharded)"},
+                       "parallelism": (f"{world} independent ranks (sessions sharded)" if world > 1
+                                       else "1 GPU")},
             "kv_bytes_per_step": kv_bytes * world, "algorithmic_bytes_per_step": alg_bytes * world,
             "decode_kernel_us": dec_ms_avg * 1e3,
             "roofline": roof,
